@@ -1,0 +1,340 @@
+"""Pins of the fp64 oracle to facts the MAPL paper and mathematics fix.
+
+Each pin takes the oracle module ``o`` so that the mutation tests can run the
+same pins against an oracle with a planted mistake and show that some pin
+fails.  Every pin states the fact it relies on; none re-types the oracle's own
+formula.
+"""
+from __future__ import annotations
+
+import numpy as np
+from scipy.spatial import cKDTree
+
+from pipeline_activation_compression_gb300 import synth
+
+
+def _orth(rng, d, r):
+    q, _ = np.linalg.qr(rng.standard_normal((d, r)))
+    return q
+
+
+# ---------------------------------------------------------------- §3.2 codec
+def pin_exact_reconstruction(o):
+    """§3.2: A^T is the exact inverse of A on col(A).  If X - anchor lies in
+    span(A) (X = E[t] P + S A^T) and the receiver uses the same anchor, the
+    codec returns X, and Z equals the coordinates S."""
+    rng = np.random.default_rng(1)
+    d, r, V, n = 48, 12, 37, 64
+    A = _orth(rng, d, r)
+    P = _orth(rng, d, r).T
+    E = rng.standard_normal((V, r))
+    S = rng.standard_normal((n, r))
+    t = rng.integers(0, V, n)
+    X = np.stack([E[t[i]] @ P for i in range(n)]) + S @ A.T
+    Z = o.compress(X, t, A, E, P)
+    assert np.max(np.abs(Z - S)) < 1e-12
+    Xh = o.reconstruct(Z, t, A, E, P)
+    assert np.linalg.norm(Xh - X) / np.linalg.norm(X) < 1e-12
+
+
+def pin_anchor_one_hot(o):
+    """eq. (3): with one-hot anchor rows E[v] = e_{j(v)}, the anchor of token v
+    is row j(v) of P, the receiver adds row j(v) of P_next, and Z of a zero
+    activation is minus that row projected."""
+    rng = np.random.default_rng(2)
+    d, r, V = 20, 5, 9
+    P = rng.standard_normal((r, d))
+    Pn = rng.standard_normal((r, d))
+    A = _orth(rng, d, r)
+    E = np.zeros((V, r))
+    j = (np.arange(V) * 3) % r
+    E[np.arange(V), j] = 1.0
+    t = np.array([0, 4, 8, 1, 1, 7])
+    an = o.anchor(E, P, t)
+    assert np.array_equal(an, P[j[t]])
+    Xh = o.reconstruct(np.zeros((len(t), r)), t, A, E, Pn)
+    assert np.array_equal(Xh, Pn[j[t]])
+    Z = o.compress(np.zeros((len(t), d)), t, A, E, P)
+    assert np.max(np.abs(Z + P[j[t]] @ A)) < 1e-12
+
+
+def pin_isometry(o):
+    """§3.2: projection and reconstruction are isometric on col(A):
+    ||Z A^T||_F = ||Z||_F for any Z (zero anchor at the receiver), and
+    compressing Z A^T returns Z."""
+    rng = np.random.default_rng(3)
+    d, r, n = 40, 7, 30
+    A = _orth(rng, d, r)
+    Z = rng.standard_normal((n, r))
+    E0 = np.zeros((3, r))
+    P0 = np.zeros((r, d))
+    t = np.zeros(n, dtype=np.int64)
+    Xh = o.reconstruct(Z, t, A, E0, P0)
+    assert abs(np.linalg.norm(Xh) - np.linalg.norm(Z)) < 1e-12 * np.linalg.norm(Z)
+    assert np.max(np.abs(o.compress(Xh, t, A, E0, P0) - Z)) < 1e-12
+
+
+def pin_projection_against_lstsq(o):
+    """With a zero anchor, Z holds the least-squares coordinates of X in the
+    orthonormal basis A (numpy.linalg.lstsq, a library routine), because
+    A^T A = I makes the normal equations read Z = X A."""
+    rng = np.random.default_rng(4)
+    d, r, n = 33, 6, 17
+    A = _orth(rng, d, r)
+    X = rng.standard_normal((n, d))
+    t = np.zeros(n, dtype=np.int64)
+    Z = o.compress(X, t, A, np.zeros((1, r)), np.zeros((r, d)))
+    ref = np.linalg.lstsq(A, X.T, rcond=None)[0].T
+    assert np.max(np.abs(Z - ref)) < 1e-12
+
+
+def pin_fold(o):
+    """Folding the anchor through M = P A is an algebraic identity of eq. (1)."""
+    rng = np.random.default_rng(5)
+    d, r, V, n = 64, 16, 50, 40
+    X = rng.standard_normal((n, d))
+    A = _orth(rng, d, r)
+    P = rng.standard_normal((r, d))
+    E = rng.standard_normal((V, r))
+    t = rng.integers(0, V, n)
+    a = o.compress(X, t, A, E, P)
+    b = o.compress_folded(X, t, A, E, P)
+    assert np.max(np.abs(a - b)) < 1e-12 * max(1.0, np.max(np.abs(a)))
+
+
+def pin_payload(o):
+    """Table 1 and Fig. 1: at d = 1024 the uncompressed bf16 boundary is 2048
+    B/token; MAPL at r = 256 sends 512 B (4x); r = 64...512 gives 128...1024
+    B; MAPL+VQ (K = 256, R = 2, group size 2 at r = 256) sends 256 B (8x)."""
+    assert o.payload_bytes_per_token(r=1024) == 2048
+    assert o.payload_bytes_per_token(r=256) == 512
+    assert [o.payload_bytes_per_token(r=x) for x in (64, 128, 256, 512)] == [128, 256, 512, 1024]
+    assert o.payload_bytes_per_token(r=256, G=128, R=2, K=256) == 256
+    # compression ratio r/d (§3.2)
+    assert o.payload_bytes_per_token(r=128) / o.payload_bytes_per_token(r=1024) == 128 / 1024
+
+
+# ------------------------------------------------------------------ §3.5 RVQ
+def pin_rvq_nearest_kdtree(o):
+    """R = 1, G = 1 is textbook nearest-neighbour search: agree with a
+    KD-tree query (scipy, a library routine)."""
+    rng = np.random.default_rng(6)
+    n, K, gd = 300, 40, 5
+    C = rng.standard_normal((1, 1, K, gd))
+    Z = rng.standard_normal((n, gd))
+    res = o.rvq_encode(Z, C)
+    dist, ref = cKDTree(C[0, 0]).query(Z, k=2)
+    assert np.array_equal(res["idx"][:, 0, 0], ref[:, 0])
+    assert np.allclose(res["gap"][:, 0, 0], dist[:, 1] ** 2 - dist[:, 0] ** 2, atol=1e-10)
+    assert np.allclose(Z - C[0, 0][ref[:, 0]], res["residual"], atol=0)
+
+
+def pin_rvq_sort_ranking(o):
+    """Multi-group, multi-round encode equals an independent ranking that
+    sorts the expanded distances ||c||^2 - 2 v.c (+ ||v||^2) with a stable sort
+    (first index on ties), group by group, round by round."""
+    rng = np.random.default_rng(7)
+    n, R, G, K, gd = 200, 3, 4, 16, 3
+    C = rng.standard_normal((R, G, K, gd))
+    Z = rng.standard_normal((n, G * gd)) * 2
+    res = o.rvq_encode(Z, C)
+    u = Z.copy()
+    for rho in range(R):
+        for g in range(G):
+            v = u[:, g * gd:(g + 1) * gd]
+            D = (C[rho, g] ** 2).sum(1)[None, :] - 2 * v @ C[rho, g].T
+            k = np.argsort(D, axis=1, kind="stable")[:, 0]
+            assert np.array_equal(res["idx"][:, rho, g], k)
+            u[:, g * gd:(g + 1) * gd] = v - C[rho, g][k]
+    assert np.max(np.abs(u - res["residual"])) < 1e-12
+
+
+def pin_rvq_special_cases(o):
+    """K = 1 always picks code 0; a codebook holding v exactly picks it with
+    zero distance and leaves a zero residual; duplicated codes resolve to the
+    lowest index and are flagged as ties."""
+    rng = np.random.default_rng(8)
+    Z = rng.standard_normal((10, 6))
+    C1 = rng.standard_normal((2, 2, 1, 3))
+    r1 = o.rvq_encode(Z, C1)
+    assert np.all(r1["idx"] == 0)
+    C = rng.standard_normal((1, 2, 8, 3)) * 5
+    C[0, 1, 5] = Z[3, 3:6]
+    r2 = o.rvq_encode(Z, C)
+    assert r2["idx"][3, 0, 1] == 5
+    assert np.all(r2["residual"][3, 3:6] == 0)
+    Cd = rng.standard_normal((1, 1, 6, 6))
+    Cd[0, 0, 4] = Cd[0, 0, 2]
+    near = Cd[0, 0, 2] + 1e-3 * rng.standard_normal((5, 6))
+    r3 = o.rvq_encode(near, Cd)
+    assert np.all(r3["idx"][:, 0, 0] == 2)
+    assert np.all(r3["flag"][:, 0, 0]) and np.all(r3["gap"][:, 0, 0] == 0)
+
+
+def pin_rvq_progressive(o):
+    """§3.5: each round quantises the residual of the previous one, so the
+    residual norm never grows when every codebook holds the zero vector, and
+    decode(encode(Z)) + residual reproduces Z."""
+    rng = np.random.default_rng(9)
+    n, R, G, K, gd = 150, 4, 2, 12, 4
+    C = rng.standard_normal((R, G, K, gd)) * np.array([1.0, 0.5, 0.25, 0.125])[:, None, None, None]
+    C[:, :, 0, :] = 0.0
+    Z = rng.standard_normal((n, G * gd))
+    prev = np.linalg.norm(Z, axis=1)
+    for rr in range(1, R + 1):
+        res = o.rvq_encode(Z, C[:rr])
+        cur = np.linalg.norm(res["residual"], axis=1)
+        assert np.all(cur <= prev + 1e-12)
+        prev = cur
+        Zh = o.rvq_decode(res["idx"], C[:rr])
+        assert np.max(np.abs(Zh + res["residual"] - Z)) < 1e-12
+    # a second round whose codebook holds the exact round-1 residual zeroes it
+    C2 = rng.standard_normal((2, 1, 5, gd))
+    Z1 = rng.standard_normal((1, gd))
+    k0 = o.rvq_encode(Z1, C2[:1])["idx"][0, 0, 0]
+    C2[1, 0, 3] = Z1[0] - C2[0, 0, k0]
+    res = o.rvq_encode(Z1, C2)
+    assert res["idx"][0, 1, 0] == 3 and np.all(res["residual"] == 0)
+
+
+def pin_rvq_given(o):
+    """Conditioning on the oracle's own choices reproduces the plain encode."""
+    rng = np.random.default_rng(10)
+    C = rng.standard_normal((2, 3, 10, 2))
+    Z = rng.standard_normal((40, 6))
+    a = o.rvq_encode(Z, C)
+    b = o.rvq_encode_given(Z, C, a["idx"])
+    for k in ("idx", "flag", "gap", "residual"):
+        assert np.array_equal(a[k], b[k])
+
+
+# ----------------------------------------------------------------- §3.3 SPEL
+def pin_tangent(o):
+    """eq. (4) maps onto the tangent space of St(d,r) at A, {V : sym(A^T V) = 0};
+    it leaves tangent vectors unchanged and sends normal vectors A S (S
+    symmetric) to zero."""
+    rng = np.random.default_rng(11)
+    d, r = 30, 6
+    A = _orth(rng, d, r)
+    g = rng.standard_normal((d, r))
+    gR = o.tangent_project(A, g)
+    S = A.T @ gR
+    assert np.max(np.abs(S + S.T)) < 1e-12
+    W = rng.standard_normal((r, r))
+    H = rng.standard_normal((d, r))
+    tang = A @ (W - W.T) + (np.eye(d) - A @ A.T) @ H
+    assert np.max(np.abs(o.tangent_project(A, tang) - tang)) < 1e-12
+    Ssym = W + W.T
+    assert np.max(np.abs(o.tangent_project(A, A @ Ssym))) < 1e-12
+    Ms = rng.standard_normal((4, 4))
+    assert np.array_equal(o.sym(Ms), o.sym(Ms).T)
+    assert np.allclose(o.sym(Ms) + (Ms - Ms.T) / 2, Ms)
+
+
+def pin_momentum(o):
+    """eq. (5) with a constant input: m_t = (1 - beta^t) g_R from m_0 = 0."""
+    rng = np.random.default_rng(12)
+    gR = rng.standard_normal((5, 3))
+    m = np.zeros_like(gR)
+    beta = 0.9
+    for t in range(1, 31):
+        m = o.momentum(m, gR, beta)
+        assert np.max(np.abs(m - (1 - beta ** t) * gR)) < 1e-12
+
+
+def pin_polar_diagonal(o):
+    """An odd matrix polynomial acts on singular values only: for
+    Y = U diag(s) V^T, PolarExpress(Y) = U diag(p_n(...p_1(s))) V^T."""
+    from pipeline_activation_compression_gb300.polar import default_coeffs
+    rng = np.random.default_rng(13)
+    d, r = 25, 6
+    U = _orth(rng, d, r)
+    Vt = _orth(rng, r, r).T
+    s = np.array([1.0, 0.7, 0.3, 0.05, 0.01, 0.002])
+    co = default_coeffs(5, 0).astype(np.float64)
+    Y = U @ np.diag(s) @ Vt
+    out = o.polar_express(Y, co)
+    t = s.copy()
+    for a, b, c in co:
+        t = a * t + b * t ** 3 + c * t ** 5
+    # the first polynomials amplify fp64 rounding by about 8x per step
+    assert np.max(np.abs(out - U @ np.diag(t) @ Vt)) < 1e-10
+
+
+def pin_polar_limit(o):
+    """Enough iterations converge to the polar factor U V^T of an SVD
+    (numpy.linalg.svd, a library routine); the result lies on St(d, r)."""
+    from pipeline_activation_compression_gb300.polar import default_coeffs
+    rng = np.random.default_rng(14)
+    Y = rng.standard_normal((40, 8))
+    Y /= np.linalg.norm(Y)
+    co = default_coeffs(12, 0).astype(np.float64)
+    out = o.polar_express(Y, co)
+    U, _, Vt = np.linalg.svd(Y, full_matrices=False)
+    assert np.max(np.abs(out - U @ Vt)) < 1e-9
+    assert np.max(np.abs(out.T @ out - np.eye(8))) < 1e-9
+
+
+def pin_spel_descends(o):
+    """SPEL is a descent method on St(d, r): for f(A) = -tr(A^T B) (gradient
+    -B) small steps decrease f, every iterate stays on the manifold, and the
+    iterates approach the maximiser polar(B)."""
+    from pipeline_activation_compression_gb300.polar import default_coeffs
+    rng = np.random.default_rng(15)
+    d, r = 24, 4
+    B = rng.standard_normal((d, r))
+    A = _orth(rng, d, r)
+    m = np.zeros_like(A)
+    co = default_coeffs(5, 5).astype(np.float64)
+    f0 = -np.trace(A.T @ B)
+    f = f0
+    for _ in range(60):
+        A, m, _ = o.spel_step(A, -B, m, 0.05, 0.9, co[:5], co[5:])
+        assert np.max(np.abs(A.T @ A - np.eye(r))) < 1e-10
+        f = -np.trace(A.T @ B)
+    U, _, Vt = np.linalg.svd(B, full_matrices=False)
+    fstar = -np.trace((U @ Vt).T @ B)
+    assert f < f0 and (f - fstar) < 0.05 * (f0 - fstar)
+
+
+def pin_spel_momentum_tangent(o):
+    """Algorithm 1 feeds the momentum with the tangent projection g_R (eq. (4)
+    before eq. (5)): from m = 0 the first momentum is (1 - beta) g_R, which
+    lies in the tangent space at A (sym(A^T m) = 0) even for a gradient with
+    a large normal component."""
+    from pipeline_activation_compression_gb300.polar import default_coeffs
+    rng = np.random.default_rng(17)
+    d, r = 20, 5
+    A = _orth(rng, d, r)
+    g = rng.standard_normal((d, r)) + A @ np.diag(np.arange(1.0, r + 1))
+    co = default_coeffs(5, 5).astype(np.float64)
+    _, m, _ = o.spel_step(A, g, np.zeros_like(A), 1e-3, 0.9, co[:5], co[5:])
+    S = A.T @ m
+    assert np.max(np.abs(S + S.T)) < 1e-12
+    assert np.linalg.norm(m) > 0.01
+
+
+def pin_spel_drift(o, steps=200):
+    """Repeated steps with random gradients keep ||A^T A - I||_max tiny."""
+    from pipeline_activation_compression_gb300.polar import default_coeffs
+    rng = np.random.default_rng(16)
+    d, r = 64, 16
+    A = _orth(rng, d, r)
+    m = np.zeros_like(A)
+    co = default_coeffs(5, 5).astype(np.float64)
+    for _ in range(steps):
+        A, m, _ = o.spel_step(A, 1e-3 * rng.standard_normal((d, r)), m, 2e-3, 0.9, co[:5], co[5:])
+    assert np.max(np.abs(A.T @ A - np.eye(r))) < 1e-10
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+# -------------------------------------------------------------- generator
+def check_generator(name="tiny_d64_r16", n_tokens=None):
+    w = synth.WORKLOADS[name]
+    b = synth.make_boundary(w, n_tokens=n_tokens)
+    A, P = b["A_f64"], b["P_f64"]
+    assert np.max(np.abs(A.T @ A - np.eye(w.r))) < 1e-12      # St(d,r) definition
+    assert np.max(np.abs(P @ P.T - np.eye(w.r))) < 1e-12      # orthonormal rows
+    return w, b

@@ -1,0 +1,173 @@
+/*
+ * mapl.h -- C ABI of the MAPL boundary codec for one GB300 (sm_103a).
+ *
+ * MAPL ("Learned Subspace Compression for Communication-Efficient Pipeline
+ * Parallelism") compresses the activation that crosses a pipeline-stage
+ * boundary.  This library implements its per-micro-batch hot path and its
+ * projector update:
+ *
+ *   compress    (§3.2 eq. (1), folded):  Z = X A - E_send[tids] (P_send A)
+ *               optionally followed by multi-codebook residual VQ (§3.5)
+ *   decompress  (§3.2 eq. (2)):          X_hat = Z_hat A^T + E_recv[tids] P_recv
+ *               computed as one contraction [Z_hat | E_recv[tids]] [A^T ; P_recv]
+ *   SPEL step   (§3.3 eqs. (4)-(7)):     tangent projection, heavy-ball
+ *               momentum, PolarExpress LMO direction, PolarExpress retraction
+ *
+ * Conventions for every call below:
+ *  - Every tensor pointer is a DEVICE pointer, row-major, contiguous, with a
+ *    16-byte aligned base.  The caller owns all tensors; the library never
+ *    frees or keeps them beyond the call, except where a plan copies a
+ *    parameter (mapl_plan_create / mapl_plan_update_A).
+ *  - Element type of X, A, P, E, codebooks, Z and X_hat is the plan's dtype:
+ *    MAPL_BF16 (2-byte bfloat16 bit patterns) or MAPL_F32 (float).
+ *    Token ids are int32; VQ indices are uint8.
+ *  - Work is enqueued asynchronously on `stream` (0 = legacy default stream).
+ *    The return value reports argument and launch errors only.  Errors that
+ *    depend on data (a token id outside [0, V), an internal wait that gave up)
+ *    are recorded in the plan's device error word and reported by mapl_check;
+ *    the affected output rows are written as zeros.  No kernel traps.
+ *  - Functions are thread-safe for distinct plans.  mapl_last_error() returns
+ *    the message of the calling thread's most recent failure.
+ */
+#ifndef MAPL_H_
+#define MAPL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MAPL_OK = 0,
+  MAPL_ERR_INVALID_ARG = 1,   /* null pointer, bad size or layout          */
+  MAPL_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels handle */
+  MAPL_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed         */
+  MAPL_ERR_BAD_TOKEN = 4,     /* a token id was outside [0, V)             */
+  MAPL_ERR_TIMEOUT = 5        /* a bounded in-kernel wait gave up          */
+} mapl_status;
+
+typedef enum { MAPL_F32 = 0, MAPL_BF16 = 1 } mapl_dtype;
+
+/*
+ * Boundary configuration (§3.2, §3.5, App. E.4).
+ *   d  activation width, r  projection rank (St(d, r)), V  vocabulary size.
+ *   G  VQ groups (gd = r / G dims each), R  residual rounds, K  codes per
+ *   group and round.  G = R = K = 0 disables VQ: the payload is Z itself.
+ * Limits: d % 64 == 0, r % 16 == 0, r <= 512, 1 <= V.  With VQ: G divides r,
+ * 1 <= R <= 8, 1 <= K <= 256 (uint8 indices).  The bf16 tensor-core path
+ * additionally needs r <= 256 with VQ, gd <= 64, K % 16 == 0 and r + K <= 512.
+ * MAPL_F32 runs on CUDA cores in fp32 (any sizes within the limits above).
+ */
+typedef struct {
+  int64_t d, r, V;
+  int32_t G, R, K;
+  int32_t dtype;   /* mapl_dtype */
+  int32_t flags;   /* reserved, must be 0 */
+} mapl_config;
+
+typedef struct mapl_plan_s* mapl_plan;
+
+/*
+ * Create a plan for one boundary p.  Copies and re-lays-out the parameters:
+ *   A          d x r   projector A_p in St(d, r)                (§3.2)
+ *   P_send     r x d   sender's frozen anchor projector P_p      (eq. (3))
+ *   P_recv     r x d   receiver's anchor projector P_{p+1}       (eq. (2))
+ *   codebooks  R x G x K x gd  C[rho][g][k][:] (NULL without VQ) (§3.5)
+ * and precomputes M = P_send A (r x r, fp64 accumulation), the operand
+ * layouts of the kernels and the codebook norms.  The plan owns that device
+ * memory; mapl_plan_destroy frees it.  Blocks until the copies are done.
+ * Errors: INVALID_ARG (sizes, null), UNSUPPORTED, CUDA.
+ */
+mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void* A,
+                             const void* P_send, const void* P_recv,
+                             const void* codebooks, cudaStream_t stream);
+
+/* Replace A (d x r, plan dtype) after a projector update and refresh M and
+ * the operand layouts (§3.3: A_p changes every optimizer step). Async. */
+mapl_status mapl_plan_update_A(mapl_plan plan, const void* A, cudaStream_t stream);
+
+/* Bytes of payload per token: 2r (bf16 Z), 4r (f32 Z) or R*G (uint8 idx). */
+mapl_status mapl_payload_bytes(const mapl_config* cfg, int64_t* bytes_per_token);
+
+/*
+ * Sender side, eq. (1) with the anchor folded through M = P_send A:
+ *   X       N x d   boundary activation X^{b_p}
+ *   tids    N       token ids (int32, must lie in [0, V))
+ *   E_send  V x r   sender's anchor table E_p^small
+ *   payload without VQ: Z, N x r (plan dtype, bf16 rounded to nearest even);
+ *           with VQ: indices, N x R x G uint8, idx[n][rho][g] = nearest code of
+ *           group g's residual in round rho (lowest index on exact ties).
+ * With VQ, Z never leaves the chip.  N >= 1.  Async.
+ */
+mapl_status mapl_compress(mapl_plan plan, const void* X, const int32_t* tids, int64_t N,
+                          const void* E_send, void* payload, cudaStream_t stream);
+
+/*
+ * Diagnostic form of mapl_compress: runs the same projection (same kernel,
+ * same accumulation order) and writes the fp32 Z (N x r float) that the VQ
+ * stage would quantise, instead of the payload.  Used to bound the distance
+ * error of the VQ decision in tests.  Async.
+ */
+mapl_status mapl_compress_z32(mapl_plan plan, const void* X, const int32_t* tids, int64_t N,
+                              const void* E_send, float* Z, cudaStream_t stream);
+
+/*
+ * Receiver side, eq. (2):
+ *   payload N x r Z (plan dtype) or N x R x G uint8 indices (decoded as
+ *           Z_hat[n][g-block] = sum_rho C[rho][g][idx[n][rho][g]])
+ *   tids    N, E_recv V x r (receiver's anchor table E_{p+1}^small)
+ *   X_hat   N x d output (plan dtype; bf16 rounded to nearest even)
+ * Async.
+ */
+mapl_status mapl_decompress(mapl_plan plan, const void* payload, const int32_t* tids,
+                            int64_t N, const void* E_recv, void* X_hat, cudaStream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the plan's device error word.
+ * Returns MAPL_OK, MAPL_ERR_BAD_TOKEN, MAPL_ERR_TIMEOUT, MAPL_ERR_CUDA, or
+ * MAPL_ERR_INVALID_ARG when a decompressed payload held an index >= K (that
+ * index was read as K - 1).
+ */
+mapl_status mapl_check(mapl_plan plan, cudaStream_t stream);
+
+void mapl_plan_destroy(mapl_plan plan);
+
+/* Bytes of device workspace mapl_spel_step needs for (d, r, batch). */
+mapl_status mapl_spel_workspace_size(int64_t d, int64_t r, int32_t batch, size_t* bytes);
+
+/*
+ * SPEL projector update (§3.3 eqs. (4)-(7), Algorithm 1 step 4) for `batch`
+ * independent boundaries, fp32, in place:
+ *   A   batch x d x r  projectors on St(d, r)      (updated)
+ *   G   batch x d x r  Euclidean gradients dL/dA   (read)
+ *   m   batch x d x r  momentum buffers            (updated)
+ *   g_R = G - A sym(A^T G);  m = beta m + (1 - beta) g_R;
+ *   D = PE(m / (||m||_F + 1e-7), LMO rows);  A = PE(A - lr D, retraction rows)
+ * where PE applies Y <- Y (a I + b S + c S^2), S = Y^T Y, once per row.
+ *   coeffs     HOST pointer, (n_lmo + n_retr) x 3 floats (a, b, c): the LMO
+ *              rows first, then the retraction rows.  The pages give the
+ *              iteration counts (5 / 7) but no coefficients.
+ *   workspace  device scratch of at least mapl_spel_workspace_size bytes,
+ *              owned by the caller, 256-byte aligned.
+ * Requirements: r % 4 == 0, d % 4 == 0, r <= d, 1 <= n_lmo + n_retr <= 32.
+ * Async.
+ */
+mapl_status mapl_spel_step(float* A, const float* G, float* m, int64_t d, int64_t r,
+                           int32_t batch, float lr, float beta, const float* coeffs,
+                           int32_t n_lmo, int32_t n_retr, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char* mapl_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t mapl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAPL_H_ */

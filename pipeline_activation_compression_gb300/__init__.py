@@ -1,0 +1,242 @@
+"""MAPL boundary codec on GB300: thin Python binding of ``libmapl.so``.
+
+Functions carry the names of the C ABI in ``include/mapl.h`` and only marshal
+arguments: torch tensors become device pointers, the current torch stream
+becomes the CUDA stream.  Every step of the codec runs in the library's CUDA
+kernels; there is no other implementation behind these calls.  Importing the
+package does not need a GPU; calling into the library needs the built
+``libmapl.so`` (``build()``) and fails loudly without it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "MaplError", "MaplConfig", "Plan", "load_library", "library_path", "build",
+    "mapl_plan_create", "mapl_plan_update_A", "mapl_payload_bytes", "mapl_compress",
+    "mapl_compress_z32", "mapl_decompress", "mapl_check", "mapl_plan_destroy",
+    "mapl_spel_workspace_size", "mapl_spel_step", "mapl_last_error", "mapl_version",
+    "MAPL_F32", "MAPL_BF16", "STATUS",
+]
+
+MAPL_F32, MAPL_BF16 = 0, 1
+STATUS = {0: "MAPL_OK", 1: "MAPL_ERR_INVALID_ARG", 2: "MAPL_ERR_UNSUPPORTED",
+          3: "MAPL_ERR_CUDA", 4: "MAPL_ERR_BAD_TOKEN", 5: "MAPL_ERR_TIMEOUT"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+
+class MaplError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        super().__init__(f"{self.name}: {message}")
+
+
+class MaplConfig(ctypes.Structure):
+    _fields_ = [("d", ctypes.c_int64), ("r", ctypes.c_int64), ("V", ctypes.c_int64),
+                ("G", ctypes.c_int32), ("R", ctypes.c_int32), ("K", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libmapl.so")
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force, verbose=verbose)
+
+
+def load_library():
+    """Load libmapl.so (built in-tree); raise if it is missing."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built: call pipeline_activation_compression_gb300.build()")
+    lib = ctypes.CDLL(path)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    sig = {
+        "mapl_plan_create": [ctypes.POINTER(P), ctypes.POINTER(MaplConfig), P, P, P, P, P],
+        "mapl_plan_update_A": [P, P, P],
+        "mapl_payload_bytes": [ctypes.POINTER(MaplConfig), ctypes.POINTER(I64)],
+        "mapl_compress": [P, P, P, I64, P, P, P],
+        "mapl_compress_z32": [P, P, P, I64, P, P, P],
+        "mapl_decompress": [P, P, P, I64, P, P, P],
+        "mapl_check": [P, P],
+        "mapl_spel_workspace_size": [I64, I64, I32, ctypes.POINTER(SZ)],
+        "mapl_spel_step": [P, P, P, I64, I64, I32, ctypes.c_float, ctypes.c_float, P, I32, I32,
+                           P, SZ, P],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.mapl_plan_destroy.argtypes = [P]
+    lib.mapl_plan_destroy.restype = None
+    lib.mapl_last_error.argtypes = []
+    lib.mapl_last_error.restype = ctypes.c_char_p
+    lib.mapl_version.argtypes = []
+    lib.mapl_version.restype = ctypes.c_int32
+    _LIB = lib
+    return lib
+
+
+def mapl_last_error() -> str:
+    return load_library().mapl_last_error().decode()
+
+
+def mapl_version() -> int:
+    return int(load_library().mapl_version())
+
+
+def _check(status: int):
+    if status != 0:
+        raise MaplError(status, mapl_last_error())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t, dtype=None, what="tensor"):
+    """Device pointer of a contiguous CUDA tensor (checked dtype)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what} must have dtype {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _tdtype(dt: int):
+    import torch
+    return torch.bfloat16 if dt == MAPL_BF16 else torch.float32
+
+
+class Plan:
+    """Owning handle of a ``mapl_plan``; destroyed with the object."""
+
+    def __init__(self, handle, cfg: MaplConfig):
+        self.handle = handle
+        self.cfg = cfg
+
+    @property
+    def vq(self) -> bool:
+        return self.cfg.G > 0
+
+    def payload_shape(self, N: int):
+        return (N, self.cfg.R, self.cfg.G) if self.vq else (N, self.cfg.r)
+
+    def payload_dtype(self):
+        import torch
+        return torch.uint8 if self.vq else _tdtype(self.cfg.dtype)
+
+    def destroy(self):
+        if self.handle is not None and _LIB is not None:
+            _LIB.mapl_plan_destroy(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def make_config(d, r, V, G=0, R=0, K=0, dtype=MAPL_BF16) -> MaplConfig:
+    return MaplConfig(d, r, V, G, R, K, dtype, 0)
+
+
+def mapl_payload_bytes(cfg: MaplConfig) -> int:
+    out = ctypes.c_int64(0)
+    _check(load_library().mapl_payload_bytes(ctypes.byref(cfg), ctypes.byref(out)))
+    return int(out.value)
+
+
+def mapl_plan_create(cfg: MaplConfig, A, P_send, P_recv, codebooks=None, stream=None) -> Plan:
+    lib = load_library()
+    dt = _tdtype(cfg.dtype)
+    h = ctypes.c_void_p()
+    _check(lib.mapl_plan_create(ctypes.byref(h), ctypes.byref(cfg), _ptr(A, dt, "A"),
+                                _ptr(P_send, dt, "P_send"), _ptr(P_recv, dt, "P_recv"),
+                                _ptr(codebooks, dt, "codebooks"), _stream(stream)))
+    return Plan(h, cfg)
+
+
+def mapl_plan_update_A(plan: Plan, A, stream=None):
+    _check(load_library().mapl_plan_update_A(plan.handle, _ptr(A, _tdtype(plan.cfg.dtype), "A"),
+                                             _stream(stream)))
+
+
+def mapl_compress(plan: Plan, X, tids, E_send, payload, stream=None):
+    import torch
+    dt = _tdtype(plan.cfg.dtype)
+    _check(load_library().mapl_compress(
+        plan.handle, _ptr(X, dt, "X"), _ptr(tids, torch.int32, "tids"), int(X.shape[0]),
+        _ptr(E_send, dt, "E_send"), _ptr(payload, plan.payload_dtype(), "payload"),
+        _stream(stream)))
+    return payload
+
+
+def mapl_compress_z32(plan: Plan, X, tids, E_send, Z, stream=None):
+    import torch
+    dt = _tdtype(plan.cfg.dtype)
+    _check(load_library().mapl_compress_z32(
+        plan.handle, _ptr(X, dt, "X"), _ptr(tids, torch.int32, "tids"), int(X.shape[0]),
+        _ptr(E_send, dt, "E_send"), _ptr(Z, torch.float32, "Z"), _stream(stream)))
+    return Z
+
+
+def mapl_decompress(plan: Plan, payload, tids, E_recv, X_hat, stream=None):
+    import torch
+    dt = _tdtype(plan.cfg.dtype)
+    _check(load_library().mapl_decompress(
+        plan.handle, _ptr(payload, plan.payload_dtype(), "payload"),
+        _ptr(tids, torch.int32, "tids"), int(tids.shape[0]), _ptr(E_recv, dt, "E_recv"),
+        _ptr(X_hat, dt, "X_hat"), _stream(stream)))
+    return X_hat
+
+
+def mapl_check(plan: Plan, stream=None):
+    """Synchronise and raise MaplError if a kernel flagged a data error."""
+    _check(load_library().mapl_check(plan.handle, _stream(stream)))
+
+
+def mapl_plan_destroy(plan: Plan):
+    plan.destroy()
+
+
+def mapl_spel_workspace_size(d: int, r: int, batch: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().mapl_spel_workspace_size(int(d), int(r), int(batch), ctypes.byref(out)))
+    return int(out.value)
+
+
+def mapl_spel_step(A, G, m, lr: float, beta: float, coeffs, n_lmo: int, n_retr: int,
+                   workspace, stream=None):
+    """In-place SPEL update of A (batch x d x r) and m; coeffs: (n_lmo+n_retr) x 3."""
+    import torch
+    co = np.ascontiguousarray(np.asarray(coeffs, dtype=np.float32).reshape(-1))
+    if co.size != 3 * (n_lmo + n_retr):
+        raise ValueError("coeffs must hold (n_lmo + n_retr) rows of (a, b, c)")
+    b, d, r = A.shape
+    _check(load_library().mapl_spel_step(
+        _ptr(A, torch.float32, "A"), _ptr(G, torch.float32, "G"), _ptr(m, torch.float32, "m"),
+        d, r, b, float(lr), float(beta), co.ctypes.data_as(ctypes.c_void_p), int(n_lmo),
+        int(n_retr), _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)))

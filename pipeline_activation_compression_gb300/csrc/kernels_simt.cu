@@ -1,0 +1,285 @@
+// kernels_simt.cu -- plan preparation kernels and the fp32 CUDA-core codec.
+//
+// Plan preparation (once per projector update, MAPL §3.3 "send the updated
+// A_p ... after every optimizer step"):
+//   M = P_send A (r x r) accumulated in fp64; for the bf16 tensor-core path
+//   -M is split into three bf16 terms hi + mid + lo (about 24 significant
+//   bits), stored transposed as K-major B operands; A^T and [A | P_recv^T]
+//   are laid out as K-major B operands; codebook rows are padded to 64
+//   elements and their squared norms and per-book maximum norm computed.
+//
+// fp32 path (plan dtype MAPL_F32): one warp per token.
+//   compress:   z = x A - E[t] M, then residual VQ with exact fp32 distances
+//   decompress: x_hat = z_hat A^T + E'[t] P'
+#include "mapl_internal.h"
+#include "ptx.cuh"
+
+namespace mapl {
+
+namespace {
+
+__device__ __forceinline__ double ld_f64(const void* p, size_t i, bool bf) {
+  return bf ? static_cast<double>(__bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]))
+            : static_cast<double>(reinterpret_cast<const float*>(p)[i]);
+}
+
+// ------------------------------------------------------------------ prep
+__global__ void k_prep_M(const void* Ps, const void* A, int d, int r, bool bf,
+                         __nv_bfloat16* Mts, float* M32) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= r * r) return;
+  const int i = idx / r, j = idx % r;   // M[i][j] = sum_k P_send[i][k] A[k][j]
+  double acc = 0.0;
+  for (int k = 0; k < d; ++k)
+    acc = fma(ld_f64(Ps, static_cast<size_t>(i) * d + k, bf),
+              ld_f64(A, static_cast<size_t>(k) * r + j, bf), acc);
+  if (M32) M32[idx] = static_cast<float>(acc);
+  if (Mts) {
+    double v = -acc;
+    for (int s = 0; s < kNumSplit; ++s) {
+      const __nv_bfloat16 h = __double2bfloat16(v);
+      Mts[(static_cast<size_t>(s) * r + j) * r + i] = h;
+      v -= static_cast<double>(__bfloat162float(h));
+    }
+  }
+}
+
+__global__ void k_prep_At(const __nv_bfloat16* A, int d, int r, __nv_bfloat16* At) {
+  const size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  if (idx >= static_cast<size_t>(d) * r) return;
+  const int j = static_cast<int>(idx / d), i = static_cast<int>(idx % d);
+  At[idx] = A[static_cast<size_t>(i) * r + j];
+}
+
+__global__ void k_prep_Bcat(const __nv_bfloat16* A, const __nv_bfloat16* Pr, int d, int r,
+                            __nv_bfloat16* Bcat) {
+  const size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  const int w = 2 * r;
+  if (idx >= static_cast<size_t>(d) * w) return;
+  const int n = static_cast<int>(idx / w), k = static_cast<int>(idx % w);
+  Bcat[idx] = k < r ? A[static_cast<size_t>(n) * r + k] : Pr[static_cast<size_t>(k - r) * d + n];
+}
+
+__global__ void k_copy_f32(const float* src, float* dst, size_t n) {
+  const size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  if (idx < n) dst[idx] = src[idx];
+}
+
+__global__ void k_prep_At32(const float* A, int d, int r, float* At) {
+  const size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  if (idx >= static_cast<size_t>(d) * r) return;
+  const int j = static_cast<int>(idx / d), i = static_cast<int>(idx % d);
+  At[idx] = A[static_cast<size_t>(i) * r + j];
+}
+
+__global__ void k_prep_codes(const void* C, int nbooks, int K, int gd, bool bf,
+                             __nv_bfloat16* Cpad, __nv_bfloat16* Cb, float* C32, float* cnorm) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;   // code id over all books
+  if (idx >= nbooks * K) return;
+  double s = 0.0;
+  for (int i = 0; i < gd; ++i) {
+    const double v = ld_f64(C, static_cast<size_t>(idx) * gd + i, bf);
+    s = fma(v, v, s);
+    if (Cb) Cb[static_cast<size_t>(idx) * gd + i] = reinterpret_cast<const __nv_bfloat16*>(C)[static_cast<size_t>(idx) * gd + i];
+    if (C32) C32[static_cast<size_t>(idx) * gd + i] = static_cast<float>(v);
+  }
+  if (Cpad) {
+    for (int i = 0; i < 64; ++i)
+      Cpad[static_cast<size_t>(idx) * 64 + i] =
+          i < gd ? reinterpret_cast<const __nv_bfloat16*>(C)[static_cast<size_t>(idx) * gd + i]
+                 : __float2bfloat16(0.f);
+  }
+  cnorm[idx] = static_cast<float>(s);
+}
+
+__global__ void k_prep_cmax(const float* cnorm, int nbooks, int K, float* cmax) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nbooks) return;
+  double m = 0.0;
+  for (int k = 0; k < K; ++k) m = fmax(m, static_cast<double>(cnorm[static_cast<size_t>(b) * K + k]));
+  cmax[b] = static_cast<float>(sqrt(m) * (1.0 + 1e-6));
+}
+
+inline unsigned blocks_for(size_t n, int t) { return static_cast<unsigned>((n + t - 1) / t); }
+
+// ------------------------------------------------------------ fp32 codec
+constexpr int kWarpsPerBlock = 8;
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    k_compress_f32(const float* __restrict__ X, const int32_t* __restrict__ tids,
+                   const float* __restrict__ A, const float* __restrict__ M,
+                   const float* __restrict__ E, const float* __restrict__ C, void* out, int* err,
+                   int N, int d, int r, int V, int G, int R, int K, int gd, int mode) {
+  extern __shared__ float zs_all[];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * kWarpsPerBlock + w;
+  if (n >= N) return;
+  float* zs = zs_all + w * r;
+  int t = tids[n];
+  const bool bad = t < 0 || t >= V;
+  if (bad && lane == 0) atomicOr(err, kErrBadToken);
+  const float* x = X + static_cast<size_t>(n) * d;
+  for (int j = lane; j < r; j += 32) {
+    float acc = 0.f;
+    for (int i = 0; i < d; ++i) acc = fmaf(x[i], A[static_cast<size_t>(i) * r + j], acc);
+    if (!bad) {
+      const float* e = E + static_cast<size_t>(t) * r;
+      for (int k = 0; k < r; ++k) acc = fmaf(-e[k], M[static_cast<size_t>(k) * r + j], acc);
+    }
+    zs[j] = bad ? 0.f : acc;
+  }
+  __syncwarp();
+  if (mode != kModeVQ) {
+    float* o = reinterpret_cast<float*>(out) + static_cast<size_t>(n) * r;
+    for (int j = lane; j < r; j += 32) o[j] = zs[j];
+    return;
+  }
+  uint8_t* io = reinterpret_cast<uint8_t*>(out) + static_cast<size_t>(n) * R * G;
+  for (int rho = 0; rho < R; ++rho) {
+    for (int g = 0; g < G; ++g) {
+      const float* book = C + static_cast<size_t>(rho * G + g) * K * gd;
+      const float* u = zs + g * gd;
+      float best = __int_as_float(0x7f800000);
+      int bk = 0x7fffffff;
+      for (int k = lane; k < K; k += 32) {
+        float D = 0.f;
+        for (int i = 0; i < gd; ++i) {
+          const float df = u[i] - book[static_cast<size_t>(k) * gd + i];
+          D = fmaf(df, df, D);
+        }
+        if (D < best) {
+          best = D;
+          bk = k;
+        }
+      }
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+        const int ok = __shfl_xor_sync(0xffffffffu, bk, off);
+        if (ob < best || (ob == best && ok < bk)) {
+          best = ob;
+          bk = ok;
+        }
+      }
+      if (lane == 0) io[rho * G + g] = bad ? 0 : static_cast<uint8_t>(bk);
+      __syncwarp();
+      for (int i = lane; i < gd; i += 32) zs[g * gd + i] -= book[static_cast<size_t>(bk) * gd + i];
+      __syncwarp();
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    k_decompress_f32(const void* in, const int32_t* __restrict__ tids,
+                     const float* __restrict__ At, const float* __restrict__ Pr,
+                     const float* __restrict__ E, const float* __restrict__ C, float* Xh,
+                     int* err, int N, int d, int r, int V, int G, int R, int K, int gd, int vq) {
+  extern __shared__ float zs_all[];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * kWarpsPerBlock + w;
+  if (n >= N) return;
+  float* zs = zs_all + w * r;
+  const int t = tids[n];
+  const bool bad = t < 0 || t >= V;
+  if (bad && lane == 0) atomicOr(err, kErrBadToken);
+  if (vq) {
+    const uint8_t* ip = reinterpret_cast<const uint8_t*>(in) + static_cast<size_t>(n) * R * G;
+    for (int j = lane; j < r; j += 32) {
+      const int g = j / gd, i = j % gd;
+      float acc = 0.f;
+      for (int rho = 0; rho < R; ++rho) {
+        int k = ip[rho * G + g];
+        if (k >= K) {   // not a valid code: flag it, never read past the book
+          atomicOr(err, kErrBadIndex);
+          k = K - 1;
+        }
+        acc += C[(static_cast<size_t>(rho * G + g) * K + k) * gd + i];
+      }
+      zs[j] = acc;
+    }
+  } else {
+    const float* z = reinterpret_cast<const float*>(in) + static_cast<size_t>(n) * r;
+    for (int j = lane; j < r; j += 32) zs[j] = z[j];
+  }
+  __syncwarp();
+  float* o = Xh + static_cast<size_t>(n) * d;
+  for (int j = lane; j < d; j += 32) {
+    float acc = 0.f;
+    for (int k = 0; k < r; ++k) acc = fmaf(zs[k], At[static_cast<size_t>(k) * d + j], acc);
+    if (!bad) {
+      const float* e = E + static_cast<size_t>(t) * r;
+      for (int k = 0; k < r; ++k) acc = fmaf(e[k], Pr[static_cast<size_t>(k) * d + j], acc);
+    }
+    o[j] = bad ? 0.f : acc;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps, const void* Pr,
+                             const void* C, PlanDevice& p, bool A_only, cudaStream_t s) {
+  const int d = static_cast<int>(c.d), r = static_cast<int>(c.r);
+  const int T = 256;
+  k_prep_At<<<blocks_for(static_cast<size_t>(d) * r, T), T, 0, s>>>(
+      reinterpret_cast<const __nv_bfloat16*>(A), d, r, p.At);
+  k_prep_M<<<blocks_for(static_cast<size_t>(r) * r, T), T, 0, s>>>(Ps, A, d, r, true, p.Mts,
+                                                                     nullptr);
+  k_prep_Bcat<<<blocks_for(static_cast<size_t>(d) * 2 * r, T), T, 0, s>>>(
+      reinterpret_cast<const __nv_bfloat16*>(A), reinterpret_cast<const __nv_bfloat16*>(Pr), d, r,
+      p.Bcat);
+  if (!A_only && c.G > 0) {
+    const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G);
+    k_prep_codes<<<blocks_for(static_cast<size_t>(nb) * c.K, T), T, 0, s>>>(
+        C, nb, c.K, gd, true, p.Cpad, p.Cb, nullptr, p.cnorm);
+    k_prep_cmax<<<blocks_for(nb, 64), 64, 0, s>>>(p.cnorm, nb, c.K, p.cmax);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep_f32(const mapl_config& c, const void* A, const void* Ps, const void* Pr,
+                            const void* C, PlanDevice& p, bool A_only, cudaStream_t s) {
+  const int d = static_cast<int>(c.d), r = static_cast<int>(c.r);
+  const int T = 256;
+  const size_t dr = static_cast<size_t>(d) * r;
+  k_copy_f32<<<blocks_for(dr, T), T, 0, s>>>(reinterpret_cast<const float*>(A), p.A32, dr);
+  k_prep_At32<<<blocks_for(dr, T), T, 0, s>>>(reinterpret_cast<const float*>(A), d, r, p.At32);
+  k_prep_M<<<blocks_for(static_cast<size_t>(r) * r, T), T, 0, s>>>(Ps, A, d, r, false, nullptr,
+                                                                     p.M32);
+  (void)Pr;   // the plan's P_recv copy is used in place (p.Pr32)
+  if (!A_only) {
+    if (c.G > 0) {
+      const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G);
+      k_prep_codes<<<blocks_for(static_cast<size_t>(nb) * c.K, T), T, 0, s>>>(
+          C, nb, c.K, gd, false, nullptr, nullptr, p.C32, p.cnorm);
+      k_prep_cmax<<<blocks_for(nb, 64), 64, 0, s>>>(p.cnorm, nb, c.K, p.cmax);
+    }
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compress_f32(const mapl_config& c, const PlanDevice& p, const float* X,
+                                const int32_t* tids, int64_t N, const float* E, void* out,
+                                int mode, cudaStream_t s) {
+  const int r = static_cast<int>(c.r);
+  const int gd = c.G ? r / c.G : 0;
+  const unsigned grid = static_cast<unsigned>((N + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  const size_t smem = static_cast<size_t>(kWarpsPerBlock) * r * sizeof(float);
+  k_compress_f32<<<grid, kWarpsPerBlock * 32, smem, s>>>(
+      X, tids, p.A32, p.M32, E, p.C32, out, p.err, static_cast<int>(N), static_cast<int>(c.d), r,
+      static_cast<int>(c.V), c.G, c.R, c.K, gd, mode);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decompress_f32(const mapl_config& c, const PlanDevice& p, const void* in,
+                                  const int32_t* tids, int64_t N, const float* E, float* Xh,
+                                  cudaStream_t s) {
+  const int r = static_cast<int>(c.r);
+  const int gd = c.G ? r / c.G : 0;
+  const unsigned grid = static_cast<unsigned>((N + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  const size_t smem = static_cast<size_t>(kWarpsPerBlock) * r * sizeof(float);
+  k_decompress_f32<<<grid, kWarpsPerBlock * 32, smem, s>>>(
+      in, tids, p.At32, p.Pr32, E, p.C32, Xh, p.err, static_cast<int>(N), static_cast<int>(c.d),
+      r, static_cast<int>(c.V), c.G, c.R, c.K, gd, c.G > 0 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace mapl

@@ -1,0 +1,270 @@
+// kernels_spel.cu -- SPEL projector update (MAPL §3.3 eqs. (4)-(7)), fp32.
+//
+// For each of `batch` independent boundaries (A, G, m are d x r):
+//   H   = sym(A^T G)                       r x r   (split-K over d, then sym)
+//   m   = beta m + (1 - beta)(G - A H)     eq. (4) + (5), fused epilogue
+//   Y   = m / (||m||_F + 1e-7)
+//   repeat n_lmo:  S = Y^T Y; Q = aI + bS + cS^2; Y = Y Q      eq. (6)
+//   Y   = A - lr Y
+//   repeat n_retr: same polynomial step                         eq. (7)
+//   A   = Y
+// The GEMMs are tiled 64 x 64 x 16 fp32 CUDA-core kernels with sequential
+// fp32 accumulation per output; r x r reductions over d use a fixed split-K
+// followed by an ordered sum, so results are run-to-run deterministic.
+#include "mapl_internal.h"
+
+namespace mapl {
+
+namespace {
+
+constexpr int BM = 64, BN = 64, BK = 16;
+
+enum Epi { kStore = 0, kMomentum = 1, kPoly = 2 };
+
+struct EpiArgs {
+  const float* G;     // kMomentum: gradient
+  float* m;           // kMomentum: momentum (read-modify-write)
+  const float* S;     // kPoly: S
+  float beta, a, b, c;
+  long sG, sm, sS;    // batch strides
+};
+
+// C[z] = op(A) B for z = blockIdx.z / ksplit; with ksplit > 1 each split
+// writes its partial product to C + split * M * N (per batch).
+template <bool TA, int EPI>
+__global__ void __launch_bounds__(256)
+    k_sgemm(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C,
+            int M, int N, int K, int lda, int ldb, long sA, long sB, long sC, int ksplit,
+            EpiArgs e) {
+  __shared__ float As[BK][BM + 4];
+  __shared__ float Bs[BK][BN + 4];
+  const int z = blockIdx.z / ksplit, ks = blockIdx.z % ksplit;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int kbeg = static_cast<int>(static_cast<long>(K) * ks / ksplit);
+  const int kend = static_cast<int>(static_cast<long>(K) * (ks + 1) / ksplit);
+  A += z * sA;
+  B += z * sB;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4] = {};
+  for (int k0 = kbeg; k0 < kend; k0 += BK) {
+    for (int q = threadIdx.x; q < BK * BM; q += 256) {
+      int kk, mm;
+      if (TA) { kk = q / BM; mm = q % BM; } else { mm = q / BK; kk = q % BK; }
+      const int gk = k0 + kk, gm = m0 + mm;
+      float v = 0.f;
+      if (gk < kend && gm < M) v = TA ? A[static_cast<long>(gk) * lda + gm] : A[static_cast<long>(gm) * lda + gk];
+      As[kk][mm] = v;
+    }
+    for (int q = threadIdx.x; q < BK * BN; q += 256) {
+      const int kk = q / BN, nn = q % BN;
+      const int gk = k0 + kk, gn = n0 + nn;
+      Bs[kk][nn] = (gk < kend && gn < N) ? B[static_cast<long>(gk) * ldb + gn] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int gm = m0 + ty * 4 + i;
+    if (gm >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int gn = n0 + tx * 4 + j;
+      if (gn >= N) continue;
+      const long o = static_cast<long>(gm) * N + gn;
+      if (EPI == kStore) {
+        C[z * sC + static_cast<long>(ks) * M * N + o] = acc[i][j];
+      } else if (EPI == kMomentum) {
+        float* mp = e.m + z * e.sm + o;
+        const float gR = e.G[z * e.sG + o] - acc[i][j];
+        *mp = e.beta * (*mp) + (1.f - e.beta) * gR;
+      } else {
+        const float sv = e.S[z * e.sS + o];
+        C[z * sC + o] = (gm == gn ? e.a : 0.f) + e.b * sv + e.c * acc[i][j];
+      }
+    }
+  }
+}
+
+// out = sum of `ksplit` partials (ordered); optionally symmetrised.
+__global__ void k_reduce(const float* __restrict__ part, float* __restrict__ out, int n,
+                         int ksplit, int sym, long sP, long sO) {
+  const int z = blockIdx.y;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n * n) return;
+  const float* p = part + z * sP;
+  float v = 0.f;
+  for (int s = 0; s < ksplit; ++s) v += p[static_cast<long>(s) * n * n + idx];
+  if (sym) {
+    const int i = idx / n, j = idx % n;
+    float w = 0.f;
+    for (int s = 0; s < ksplit; ++s) w += p[static_cast<long>(s) * n * n + j * n + i];
+    v = 0.5f * (v + w);
+  }
+  out[z * sO + idx] = v;
+}
+
+// per-block partial sums of squares, then an ordered final sum
+__global__ void k_sumsq_partial(const float* __restrict__ x, long n, float* part, long sX,
+                                int nblk) {
+  __shared__ float red[256];
+  const int z = blockIdx.y;
+  const float* p = x + z * sX;
+  float s = 0.f;
+  for (long i = blockIdx.x * 256L + threadIdx.x; i < n; i += 256L * nblk) s = fmaf(p[i], p[i], s);
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) part[z * nblk + blockIdx.x] = red[0];
+}
+
+__global__ void k_sumsq_final(const float* part, int nblk, float* inv) {
+  const int z = blockIdx.x;
+  if (threadIdx.x != 0) return;
+  float s = 0.f;
+  for (int i = 0; i < nblk; ++i) s += part[z * nblk + i];
+  inv[z] = 1.f / (sqrtf(s) + 1e-7f);
+}
+
+// y = alpha_z * x (alpha from a per-batch array) or y = A - lr * x
+__global__ void k_scale(const float* __restrict__ x, const float* __restrict__ inv, float* y,
+                        long n, long sX) {
+  const int z = blockIdx.y;
+  const float a = inv[z];
+  for (long i = blockIdx.x * 256L + threadIdx.x; i < n; i += 256L * gridDim.x)
+    y[z * sX + i] = a * x[z * sX + i];
+}
+
+__global__ void k_axpy(const float* __restrict__ A, const float* __restrict__ D, float lr,
+                       float* y, long n, long sX) {
+  const int z = blockIdx.y;
+  for (long i = blockIdx.x * 256L + threadIdx.x; i < n; i += 256L * gridDim.x)
+    y[z * sX + i] = A[z * sX + i] - lr * D[z * sX + i];
+}
+
+inline dim3 gemm_grid(int M, int N, int zdim) {
+  return dim3((N + BN - 1) / BN, (M + BM - 1) / BM, zdim);
+}
+
+int choose_ksplit(int d) {
+  int ks = d / 128;
+  if (ks < 1) ks = 1;
+  if (ks > 16) ks = 16;
+  return ks;
+}
+
+struct Ws {
+  float *Y0, *Y1, *S, *Q, *part, *nrm_part, *inv;
+  long dr, rr;   // packed per-boundary strides of the d x r and r x r buffers
+  int ks;
+};
+
+constexpr int kNormBlocks = 64;
+
+inline size_t al64(size_t x) { return (x + 63) & ~static_cast<size_t>(63); }
+
+Ws carve(void* ws, int d, int r, int batch) {
+  Ws w;
+  w.dr = static_cast<long>(d) * r;
+  w.rr = static_cast<long>(r) * r;
+  w.ks = choose_ksplit(d);
+  float* p = reinterpret_cast<float*>(ws);
+  w.Y0 = p; p += al64(w.dr * batch);
+  w.Y1 = p; p += al64(w.dr * batch);
+  w.S = p; p += al64(w.rr * batch);
+  w.Q = p; p += al64(w.rr * batch);
+  w.part = p; p += al64(w.rr * w.ks * batch);
+  w.nrm_part = p; p += al64(static_cast<size_t>(kNormBlocks) * batch);
+  w.inv = p;
+  return w;
+}
+
+// Y_out = Y_in (a I + b S + c S^2), S = Y_in^T Y_in
+void pe_step(const float* Yin, float* Yout, const float* co, const Ws& w, int d, int r,
+             int batch, cudaStream_t s) {
+  EpiArgs none{};
+  k_sgemm<true, kStore><<<gemm_grid(r, r, batch * w.ks), 256, 0, s>>>(
+      Yin, Yin, w.part, r, r, d, r, r, w.dr, w.dr, w.rr * w.ks, w.ks, none);
+  k_reduce<<<dim3((r * r + 255) / 256, batch), 256, 0, s>>>(w.part, w.S, r, w.ks, 0,
+                                                            w.rr * w.ks, w.rr);
+  EpiArgs pe{};
+  pe.S = w.S;
+  pe.sS = w.rr;
+  pe.a = co[0];
+  pe.b = co[1];
+  pe.c = co[2];
+  k_sgemm<false, kPoly><<<gemm_grid(r, r, batch), 256, 0, s>>>(w.S, w.S, w.Q, r, r, r, r, r,
+                                                               w.rr, w.rr, w.rr, 1, pe);
+  k_sgemm<false, kStore><<<gemm_grid(d, r, batch), 256, 0, s>>>(Yin, w.Q, Yout, d, r, r, r, r,
+                                                                w.dr, w.rr, w.dr, 1, none);
+}
+
+}  // namespace
+
+size_t spel_workspace_bytes(int64_t d, int64_t r, int32_t batch) {
+  const size_t dr = static_cast<size_t>(d) * r, rr = static_cast<size_t>(r) * r;
+  const int ks = choose_ksplit(static_cast<int>(d));
+  const size_t floats = 2 * al64(dr * batch) + 2 * al64(rr * batch) + al64(rr * ks * batch) +
+                        al64(static_cast<size_t>(kNormBlocks) * batch) + al64(batch);
+  return floats * sizeof(float);
+}
+
+cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int batch, float lr,
+                        float beta, const float* coeffs, int n_lmo, int n_retr, void* ws,
+                        cudaStream_t s) {
+  const Ws w = carve(ws, d, r, batch);
+  EpiArgs none{};
+  // H = sym(A^T G)
+  k_sgemm<true, kStore><<<gemm_grid(r, r, batch * w.ks), 256, 0, s>>>(
+      A, G, w.part, r, r, d, r, r, w.dr, w.dr, w.rr * w.ks, w.ks, none);
+  k_reduce<<<dim3((r * r + 255) / 256, batch), 256, 0, s>>>(w.part, w.S, r, w.ks, 1,
+                                                            w.rr * w.ks, w.rr);
+  // m = beta m + (1 - beta)(G - A H)
+  EpiArgs mo{};
+  mo.G = G;
+  mo.m = m;
+  mo.sG = w.dr;
+  mo.sm = w.dr;
+  mo.beta = beta;
+  k_sgemm<false, kMomentum><<<gemm_grid(d, r, batch), 256, 0, s>>>(A, w.S, nullptr, d, r, r, r,
+                                                                   r, w.dr, w.rr, 0, 1, mo);
+  // Y = m / (||m||_F + 1e-7)
+  k_sumsq_partial<<<dim3(kNormBlocks, batch), 256, 0, s>>>(m, w.dr, w.nrm_part, w.dr,
+                                                           kNormBlocks);
+  k_sumsq_final<<<batch, 32, 0, s>>>(w.nrm_part, kNormBlocks, w.inv);
+  k_scale<<<dim3(256, batch), 256, 0, s>>>(m, w.inv, w.Y0, w.dr, w.dr);
+  float* cur = w.Y0;
+  float* nxt = w.Y1;
+  for (int t = 0; t < n_lmo; ++t) {
+    pe_step(cur, nxt, coeffs + 3 * t, w, d, r, batch, s);
+    float* tmp = cur; cur = nxt; nxt = tmp;
+  }
+  // retraction input A - lr D
+  k_axpy<<<dim3(256, batch), 256, 0, s>>>(A, cur, lr, nxt, w.dr, w.dr);
+  { float* tmp = cur; cur = nxt; nxt = tmp; }
+  for (int t = 0; t < n_retr; ++t) {
+    float* out = (t == n_retr - 1) ? A : nxt;
+    pe_step(cur, out, coeffs + 3 * (n_lmo + t), w, d, r, batch, s);
+    float* tmp = cur; cur = out; nxt = tmp;
+  }
+  if (n_retr == 0)
+    cudaMemcpyAsync(A, cur, sizeof(float) * w.dr * batch, cudaMemcpyDeviceToDevice, s);
+  return cudaGetLastError();
+}
+
+}  // namespace mapl

@@ -1,0 +1,488 @@
+// mapl_api.cu -- host side of the C ABI declared in include/mapl.h: argument
+// validation, plan memory and operand layouts, TMA descriptors, launches.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "mapl_internal.h"
+
+using namespace mapl;
+
+struct mapl_plan_s {
+  mapl_config cfg{};
+  int device = 0;
+  bool vq = false;
+  bool tc = false;        // bf16 tensor-core path
+  int gd = 0;
+  PlanDevice p;
+  CUtensorMap tmAt{}, tmMt{}, tmC{}, tmB{};
+  uint64_t timeout_ns = kDefaultTimeoutNs;
+  // launch geometry
+  int c_nstage = 0;
+  uint32_t c_stage = 0, c_smem = 0;
+  int d_nstage = 0;
+  uint32_t d_stage = 0, d_smem = 0, d_abytes = 0;
+  bool d_stream = false;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+mapl_status fail(mapl_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+mapl_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MAPL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t elt_size(const mapl_config& c) { return c.dtype == MAPL_BF16 ? 2 : 4; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major (outer x inner) matrix, 128-byte
+// swizzled boxes of box_outer rows x 64 elements; out-of-range reads are zero.
+bool make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
+               uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+constexpr uint32_t kSmemMax = 232448;   // opt-in dynamic shared memory per CTA
+
+mapl_status validate(const mapl_config* c) {
+  if (!c) return fail(MAPL_ERR_INVALID_ARG, "config is NULL");
+  if (c->dtype != MAPL_F32 && c->dtype != MAPL_BF16)
+    return fail(MAPL_ERR_INVALID_ARG, "dtype must be MAPL_F32 or MAPL_BF16");
+  if (c->flags != 0) return fail(MAPL_ERR_INVALID_ARG, "flags must be 0");
+  if (c->d < 64 || c->d % 64 != 0 || c->d > (1 << 16))
+    return fail(MAPL_ERR_INVALID_ARG, "d must be a positive multiple of 64 (<= 65536)");
+  if (c->r < 16 || c->r % 16 != 0 || c->r > 512 || c->r > c->d)
+    return fail(MAPL_ERR_INVALID_ARG, "r must be a multiple of 16 in [16, min(512, d)]");
+  if (c->V < 1 || c->V > 0x7fffffff) return fail(MAPL_ERR_INVALID_ARG, "V must be in [1, 2^31)");
+  const bool vq = c->G != 0 || c->R != 0 || c->K != 0;
+  if (vq) {
+    if (c->G < 1 || c->r % c->G != 0) return fail(MAPL_ERR_INVALID_ARG, "G must divide r");
+    if (c->R < 1 || c->R > 8) return fail(MAPL_ERR_INVALID_ARG, "R must be in [1, 8]");
+    if (c->K < 1 || c->K > 256) return fail(MAPL_ERR_INVALID_ARG, "K must be in [1, 256]");
+  }
+  if (c->dtype == MAPL_BF16) {
+    if (c->r % 64 != 0)
+      return fail(MAPL_ERR_UNSUPPORTED, "bf16 tensor-core path needs r % 64 == 0");
+    if (vq) {
+      const int64_t gd = c->r / c->G;
+      if (gd != 16 && gd != 32 && gd != 64)
+        return fail(MAPL_ERR_UNSUPPORTED, "bf16 VQ needs group width r/G in {16, 32, 64}");
+      if (c->K % 16 != 0) return fail(MAPL_ERR_UNSUPPORTED, "bf16 VQ needs K % 16 == 0");
+      if (c->r > 256 || c->r + c->K > 512)
+        return fail(MAPL_ERR_UNSUPPORTED, "bf16 VQ needs r <= 256 and r + K <= 512");
+      if (static_cast<int64_t>(c->R) * c->G * c->K * 4 > 32768)
+        return fail(MAPL_ERR_UNSUPPORTED, "bf16 VQ needs R*G*K <= 8192");
+    }
+  }
+  return MAPL_OK;
+}
+
+size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+mapl_status geometry(mapl_plan_s* pl) {
+  const mapl_config& c = pl->cfg;
+  const uint32_t ctl = ctl_bytes() + 64;
+  const uint32_t slack = 1024;
+  // compress
+  {
+    uint32_t st = 16384u + static_cast<uint32_t>(c.r) * 128u;
+    if (pl->vq) st = st > static_cast<uint32_t>(c.K) * 128u ? st : static_cast<uint32_t>(c.K) * 128u;
+    st = (st + 1023u) & ~1023u;
+    uint32_t extra = ctl + slack;
+    if (pl->vq) extra += 16384u + static_cast<uint32_t>(c.R * c.G * c.K) * 4u;
+    int ns = static_cast<int>((kSmemMax - extra) / st);
+    if (ns > 8) ns = 8;
+    if (ns < 2) return fail(MAPL_ERR_UNSUPPORTED, "compress stages do not fit in shared memory");
+    pl->c_nstage = ns;
+    pl->c_stage = st;
+    pl->c_smem = ns * st + extra;
+  }
+  // decompress
+  {
+    const int64_t NC = (c.d % 256 == 0) ? 256 : ((c.d % 128 == 0) ? 128 : 64);
+    const uint32_t a_res = static_cast<uint32_t>(2 * c.r / 64) * 16384u;
+    pl->d_stream = a_res > 131072u;
+    uint32_t st = static_cast<uint32_t>(NC) * 128u + (pl->d_stream ? 16384u : 0u);
+    pl->d_abytes = pl->d_stream ? 0u : a_res;
+    const uint32_t extra = ctl + slack + pl->d_abytes;
+    int ns = static_cast<int>((kSmemMax - extra) / st);
+    if (ns > 8) ns = 8;
+    if (ns < 2) return fail(MAPL_ERR_UNSUPPORTED, "decompress stages do not fit in shared memory");
+    pl->d_nstage = ns;
+    pl->d_stage = st;
+    pl->d_smem = ns * st + extra;
+  }
+  return MAPL_OK;
+}
+
+mapl_status build_plan_maps(mapl_plan_s* pl) {
+  const mapl_config& c = pl->cfg;
+  const uint32_t nrow = c.r > 256 ? 256u : static_cast<uint32_t>(c.r);
+  const uint64_t NC = (c.d % 256 == 0) ? 256 : ((c.d % 128 == 0) ? 128 : 64);
+  if (!make_tmap(&pl->tmAt, pl->p.At, c.d, c.r, 64, nrow))
+    return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (A^T)");
+  if (!make_tmap(&pl->tmMt, pl->p.Mts, c.r, static_cast<uint64_t>(kNumSplit) * c.r, 64, nrow))
+    return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (M splits)");
+  if (!make_tmap(&pl->tmB, pl->p.Bcat, 2 * c.r, c.d, 64, static_cast<uint32_t>(NC)))
+    return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed ([A | P'^T])");
+  if (pl->vq) {
+    if (!make_tmap(&pl->tmC, pl->p.Cpad, 64, static_cast<uint64_t>(c.R) * c.G * c.K, 64,
+                   static_cast<uint32_t>(c.K)))
+      return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (codebooks)");
+  } else {
+    pl->tmC = pl->tmAt;   // unused
+  }
+  return MAPL_OK;
+}
+
+mapl_status check_device(const mapl_plan_s* pl) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != pl->device)
+    return fail(MAPL_ERR_INVALID_ARG, "current device %d differs from the plan's device %d", dev,
+                pl->device);
+  return MAPL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t mapl_version(void) { return 100; }
+
+const char* mapl_last_error(void) { return g_last_error.c_str(); }
+
+mapl_status mapl_payload_bytes(const mapl_config* cfg, int64_t* bytes_per_token) {
+  mapl_status st = validate(cfg);
+  if (st != MAPL_OK) return st;
+  if (!bytes_per_token) return fail(MAPL_ERR_INVALID_ARG, "bytes_per_token is NULL");
+  if (cfg->G > 0)
+    *bytes_per_token = static_cast<int64_t>(cfg->R) * cfg->G;
+  else
+    *bytes_per_token = cfg->r * static_cast<int64_t>(elt_size(*cfg));
+  return MAPL_OK;
+}
+
+mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void* A,
+                             const void* P_send, const void* P_recv, const void* codebooks,
+                             cudaStream_t stream) {
+  if (!out) return fail(MAPL_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  mapl_status st = validate(cfg);
+  if (st != MAPL_OK) return st;
+  const bool vq = cfg->G > 0;
+  if (!A || !P_send || !P_recv) return fail(MAPL_ERR_INVALID_ARG, "A, P_send, P_recv must be non-NULL");
+  if (vq && !codebooks) return fail(MAPL_ERR_INVALID_ARG, "codebooks must be non-NULL with VQ");
+  if (!vq && codebooks) return fail(MAPL_ERR_INVALID_ARG, "codebooks given without VQ");
+  if (!aligned16(A) || !aligned16(P_send) || !aligned16(P_recv) || (codebooks && !aligned16(codebooks)))
+    return fail(MAPL_ERR_INVALID_ARG, "parameter pointers must be 16-byte aligned");
+
+  mapl_plan_s* pl = new mapl_plan_s();
+  pl->cfg = *cfg;
+  pl->vq = vq;
+  pl->tc = cfg->dtype == MAPL_BF16;
+  pl->gd = vq ? static_cast<int>(cfg->r / cfg->G) : 0;
+  cudaError_t e = cudaGetDevice(&pl->device);
+  if (e != cudaSuccess) {
+    delete pl;
+    return cuda_fail(e, "cudaGetDevice");
+  }
+  const int64_t d = cfg->d, r = cfg->r;
+  const int64_t nb = vq ? static_cast<int64_t>(cfg->R) * cfg->G : 0;
+  const int64_t ncode = nb * (vq ? cfg->K : 0);
+  // one pool for every plan-owned buffer
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off += up256(bytes); return o; };
+  size_t oAt = 0, oMts = 0, oBcat = 0, oCpad = 0, oCb = 0, oA32 = 0, oAt32 = 0, oM32 = 0,
+         oC32 = 0;
+  const size_t oPs = take(d * r * elt_size(*cfg));
+  const size_t oPr = take(d * r * elt_size(*cfg));
+  if (pl->tc) {
+    oAt = take(d * r * 2);
+    oMts = take(static_cast<size_t>(kNumSplit) * r * r * 2);
+    oBcat = take(d * 2 * r * 2);
+    if (vq) {
+      oCpad = take(ncode * 64 * 2);
+      oCb = take(ncode * pl->gd * 2);
+    }
+  } else {
+    oA32 = take(d * r * 4);
+    oAt32 = take(d * r * 4);
+    oM32 = take(r * r * 4);
+    if (vq) oC32 = take(ncode * pl->gd * 4);
+  }
+  const size_t ocn = take((ncode > 0 ? ncode : 1) * 4);
+  const size_t ocm = take((nb > 0 ? nb : 1) * 4);
+  const size_t oerr = take(4);
+  void* pool = nullptr;
+  e = cudaMalloc(&pool, off);
+  if (e != cudaSuccess) {
+    delete pl;
+    return cuda_fail(e, "cudaMalloc(plan)");
+  }
+  char* b = reinterpret_cast<char*>(pool);
+  PlanDevice& p = pl->p;
+  p.pool = pool;
+  if (pl->tc) {
+    p.At = reinterpret_cast<__nv_bfloat16*>(b + oAt);
+    p.Mts = reinterpret_cast<__nv_bfloat16*>(b + oMts);
+    p.Bcat = reinterpret_cast<__nv_bfloat16*>(b + oBcat);
+    if (vq) {
+      p.Cpad = reinterpret_cast<__nv_bfloat16*>(b + oCpad);
+      p.Cb = reinterpret_cast<__nv_bfloat16*>(b + oCb);
+    }
+  } else {
+    p.A32 = reinterpret_cast<float*>(b + oA32);
+    p.At32 = reinterpret_cast<float*>(b + oAt32);
+    p.M32 = reinterpret_cast<float*>(b + oM32);
+    p.Pr32 = reinterpret_cast<float*>(b + oPr);
+    if (vq) p.C32 = reinterpret_cast<float*>(b + oC32);
+  }
+  p.Ps = b + oPs;
+  p.Pr = b + oPr;
+  p.cnorm = reinterpret_cast<float*>(b + ocn);
+  p.cmax = reinterpret_cast<float*>(b + ocm);
+  p.err = reinterpret_cast<int*>(b + oerr);
+
+  e = cudaMemsetAsync(p.err, 0, 4, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(p.Ps, P_send, d * r * elt_size(*cfg), cudaMemcpyDeviceToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(p.Pr, P_recv, d * r * elt_size(*cfg), cudaMemcpyDeviceToDevice, stream);
+  if (e == cudaSuccess)
+    e = pl->tc ? launch_prep_bf16(*cfg, A, p.Ps, p.Pr, codebooks, p, false, stream)
+               : launch_prep_f32(*cfg, A, p.Ps, p.Pr, codebooks, p, false, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) {
+    cudaFree(pool);
+    delete pl;
+    return cuda_fail(e, "plan preparation");
+  }
+  if (pl->tc) {
+    st = geometry(pl);
+    if (st == MAPL_OK) st = build_plan_maps(pl);
+    if (st != MAPL_OK) {
+      cudaFree(pool);
+      delete pl;
+      return st;
+    }
+  }
+  *out = pl;
+  return MAPL_OK;
+}
+
+mapl_status mapl_plan_update_A(mapl_plan pl, const void* A, cudaStream_t stream) {
+  if (!pl || !A) return fail(MAPL_ERR_INVALID_ARG, "plan and A must be non-NULL");
+  if (!aligned16(A)) return fail(MAPL_ERR_INVALID_ARG, "A must be 16-byte aligned");
+  mapl_status st = check_device(pl);
+  if (st != MAPL_OK) return st;
+  cudaError_t e = pl->tc ? launch_prep_bf16(pl->cfg, A, pl->p.Ps, pl->p.Pr, nullptr, pl->p, true, stream)
+                         : launch_prep_f32(pl->cfg, A, pl->p.Ps, pl->p.Pr, nullptr, pl->p, true, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "update_A");
+  return MAPL_OK;
+}
+
+void mapl_plan_destroy(mapl_plan pl) {
+  if (!pl) return;
+  if (pl->p.pool) cudaFree(pl->p.pool);
+  delete pl;
+}
+
+static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* tids, int64_t N,
+                                   const void* E, void* out, int mode, cudaStream_t stream) {
+  if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
+  if (!X || !tids || !E || !out) return fail(MAPL_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (N < 1 || N > 0x7fffffffLL) return fail(MAPL_ERR_INVALID_ARG, "N must be in [1, 2^31)");
+  if (!aligned16(X) || !aligned16(E) || !aligned16(out) || (reinterpret_cast<uintptr_t>(tids) & 3u))
+    return fail(MAPL_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned (tids 4-byte)");
+  mapl_status st = check_device(pl);
+  if (st != MAPL_OK) return st;
+  const mapl_config& c = pl->cfg;
+  cudaError_t e;
+  if (!pl->tc) {
+    e = launch_compress_f32(c, pl->p, reinterpret_cast<const float*>(X), tids, N,
+                            reinterpret_cast<const float*>(E), out, mode, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "compress launch");
+    return MAPL_OK;
+  }
+  CUtensorMap tmX;
+  if (!make_tmap(&tmX, X, c.d, static_cast<uint64_t>(N), 64, kTile))
+    return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (X)");
+  CompressArgs a{};
+  a.tids = tids;
+  a.E = reinterpret_cast<const __nv_bfloat16*>(E);
+  a.Cb = pl->p.Cb;
+  a.cnorm = pl->p.cnorm;
+  a.cmax = pl->p.cmax;
+  a.out = out;
+  a.err = pl->p.err;
+  a.N = static_cast<int>(N);
+  a.d = static_cast<int>(c.d);
+  a.r = static_cast<int>(c.r);
+  a.V = static_cast<int>(c.V);
+  a.G = c.G;
+  a.R = c.R;
+  a.K = c.K;
+  a.gd = pl->gd;
+  a.mode = mode;
+  a.nstage = pl->c_nstage;
+  a.stage_bytes = pl->c_stage;
+  a.timeout_ns = pl->timeout_ns;
+  const int grid = static_cast<int>((N + kTile - 1) / kTile);
+  e = launch_compress_tc(tmX, pl->tmAt, pl->tmMt, pl->tmC, a, pl->c_smem, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "compress launch");
+  return MAPL_OK;
+}
+
+mapl_status mapl_compress(mapl_plan pl, const void* X, const int32_t* tids, int64_t N,
+                          const void* E_send, void* payload, cudaStream_t stream) {
+  if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
+  const int mode = pl->vq ? kModeVQ : (pl->tc ? kModeZ16 : kModeZ32);
+  return compress_common(pl, X, tids, N, E_send, payload, mode, stream);
+}
+
+mapl_status mapl_compress_z32(mapl_plan pl, const void* X, const int32_t* tids, int64_t N,
+                              const void* E_send, float* Z, cudaStream_t stream) {
+  return compress_common(pl, X, tids, N, E_send, Z, kModeZ32, stream);
+}
+
+mapl_status mapl_decompress(mapl_plan pl, const void* payload, const int32_t* tids, int64_t N,
+                            const void* E_recv, void* X_hat, cudaStream_t stream) {
+  if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
+  if (!payload || !tids || !E_recv || !X_hat) return fail(MAPL_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (N < 1 || N > 0x7fffffffLL) return fail(MAPL_ERR_INVALID_ARG, "N must be in [1, 2^31)");
+  if (!aligned16(payload) || !aligned16(E_recv) || !aligned16(X_hat) ||
+      (reinterpret_cast<uintptr_t>(tids) & 3u))
+    return fail(MAPL_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned (tids 4-byte)");
+  mapl_status st = check_device(pl);
+  if (st != MAPL_OK) return st;
+  const mapl_config& c = pl->cfg;
+  cudaError_t e;
+  if (!pl->tc) {
+    e = launch_decompress_f32(c, pl->p, payload, tids, N, reinterpret_cast<const float*>(E_recv),
+                              reinterpret_cast<float*>(X_hat), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decompress launch");
+    return MAPL_OK;
+  }
+  CUtensorMap tmZ;
+  if (!pl->vq) {
+    if (!make_tmap(&tmZ, payload, c.r, static_cast<uint64_t>(N), 64, kTile))
+      return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (Z)");
+  } else {
+    tmZ = pl->tmB;   // unused
+  }
+  DecompressArgs a{};
+  a.tids = tids;
+  a.E = reinterpret_cast<const __nv_bfloat16*>(E_recv);
+  a.Cb = pl->p.Cb;
+  a.idx = pl->vq ? reinterpret_cast<const uint8_t*>(payload) : nullptr;
+  a.Xh = reinterpret_cast<__nv_bfloat16*>(X_hat);
+  a.err = pl->p.err;
+  a.N = static_cast<int>(N);
+  a.d = static_cast<int>(c.d);
+  a.r = static_cast<int>(c.r);
+  a.V = static_cast<int>(c.V);
+  a.G = c.G;
+  a.R = c.R;
+  a.K = c.K;
+  a.gd = pl->gd;
+  a.vq = pl->vq ? 1 : 0;
+  a.a_stream = pl->d_stream ? 1 : 0;
+  a.nstage = pl->d_nstage;
+  a.stage_bytes = pl->d_stage;
+  a.a_bytes = pl->d_abytes;
+  a.timeout_ns = pl->timeout_ns;
+  const int grid = static_cast<int>((N + kTile - 1) / kTile);
+  e = launch_decompress_tc(pl->tmB, tmZ, a, pl->d_smem, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decompress launch");
+  return MAPL_OK;
+}
+
+mapl_status mapl_check(mapl_plan pl, cudaStream_t stream) {
+  if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int w = 0;
+  e = cudaMemcpy(&w, pl->p.err, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (w) {
+    e = cudaMemset(pl->p.err, 0, 4);
+    if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  }
+  if (w & kErrTimeout) return fail(MAPL_ERR_TIMEOUT, "an in-kernel wait gave up");
+  if (w & kErrBadToken) return fail(MAPL_ERR_BAD_TOKEN, "a token id was outside [0, V)");
+  if (w & kErrBadIndex) return fail(MAPL_ERR_INVALID_ARG, "a VQ index in the payload was >= K");
+  return MAPL_OK;
+}
+
+mapl_status mapl_spel_workspace_size(int64_t d, int64_t r, int32_t batch, size_t* bytes) {
+  if (!bytes) return fail(MAPL_ERR_INVALID_ARG, "bytes is NULL");
+  if (d < 4 || r < 4 || d % 4 || r % 4 || r > d || batch < 1 || d > (1 << 20))
+    return fail(MAPL_ERR_INVALID_ARG, "need 4 | d, 4 | r, r <= d, batch >= 1");
+  *bytes = spel_workspace_bytes(d, r, batch);
+  return MAPL_OK;
+}
+
+mapl_status mapl_spel_step(float* A, const float* G, float* m, int64_t d, int64_t r,
+                           int32_t batch, float lr, float beta, const float* coeffs,
+                           int32_t n_lmo, int32_t n_retr, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  if (!A || !G || !m || !coeffs || !workspace)
+    return fail(MAPL_ERR_INVALID_ARG, "NULL pointer argument");
+  size_t need = 0;
+  mapl_status st = mapl_spel_workspace_size(d, r, batch, &need);
+  if (st != MAPL_OK) return st;
+  if (workspace_bytes < need)
+    return fail(MAPL_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+  if (n_lmo < 0 || n_retr < 0 || n_lmo + n_retr < 1 || n_lmo + n_retr > 32)
+    return fail(MAPL_ERR_INVALID_ARG, "need 1 <= n_lmo + n_retr <= 32");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || !aligned16(A) || !aligned16(G) || !aligned16(m))
+    return fail(MAPL_ERR_INVALID_ARG, "workspace must be 256-byte, tensors 16-byte aligned");
+  if (!(beta >= 0.f && beta < 1.f)) return fail(MAPL_ERR_INVALID_ARG, "beta must be in [0, 1)");
+  cudaError_t e = launch_spel(A, G, m, static_cast<int>(d), static_cast<int>(r), batch, lr, beta,
+                              coeffs, n_lmo, n_retr, workspace, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "spel launch");
+  return MAPL_OK;
+}
+
+}  // extern "C"

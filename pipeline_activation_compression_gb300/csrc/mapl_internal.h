@@ -1,0 +1,106 @@
+// mapl_internal.h -- plan layout and kernel launchers shared by the host API
+// (mapl_api.cu) and the kernel translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mapl.h"
+
+namespace mapl {
+
+constexpr int kTile = 128;          // tokens per CTA tile (MMA M)
+constexpr int kNumSplit = 3;        // bf16 terms of -M in the folded anchor product
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per bounded wait
+
+// device error word bits (mapl_check maps them to mapl_status)
+constexpr int kErrBadToken = 1;
+constexpr int kErrTimeout = 2;
+constexpr int kErrBadIndex = 4;
+
+// Compress kernel modes.
+enum CompressMode { kModeZ16 = 0, kModeVQ = 1, kModeZ32 = 2 };
+
+struct PlanDevice {
+  // bf16 tensor-core operands
+  __nv_bfloat16* At = nullptr;      // r x d     A^T (K-major B operand of X A)
+  __nv_bfloat16* Mts = nullptr;     // S x r x r -M^T split into S bf16 terms
+  __nv_bfloat16* Bcat = nullptr;    // d x 2r    [A | P_recv^T] (K-major B of decompress)
+  __nv_bfloat16* Cpad = nullptr;    // R*G*K x 64 codebook rows, zero padded to 64
+  __nv_bfloat16* Cb = nullptr;      // R x G x K x gd codebooks (decode lookups)
+  // fp32 CUDA-core path
+  float* A32 = nullptr;             // d x r
+  float* At32 = nullptr;            // r x d     A^T
+  float* M32 = nullptr;             // r x r     M = P_send A
+  float* Pr32 = nullptr;            // r x d     P_recv
+  float* C32 = nullptr;             // R x G x K x gd
+  // both
+  void* Ps = nullptr;               // r x d     copy of P_send (plan dtype)
+  void* Pr = nullptr;               // r x d     copy of P_recv (plan dtype)
+  float* cnorm = nullptr;           // R x G x K  ||c||^2 (fp32 of the exact value)
+  float* cmax = nullptr;            // R x G      max_k ||c_k|| (rounded up)
+  int* err = nullptr;               // device error word (bits kErrBadToken, kErrTimeout)
+  void* pool = nullptr;             // single allocation holding everything above
+};
+
+struct CompressArgs {
+  const int32_t* tids;
+  const __nv_bfloat16* E;           // V x r
+  const __nv_bfloat16* Cb;
+  const float* cnorm;
+  const float* cmax;
+  void* out;
+  int* err;
+  int N, d, r, V, G, R, K, gd;
+  int mode;
+  int nstage;
+  uint32_t stage_bytes;
+  uint64_t timeout_ns;
+};
+
+struct DecompressArgs {
+  const int32_t* tids;
+  const __nv_bfloat16* E;           // V x r (receiver)
+  const __nv_bfloat16* Cb;
+  const uint8_t* idx;               // VQ payload (N x R x G) or null
+  __nv_bfloat16* Xh;                // N x d
+  int* err;
+  int N, d, r, V, G, R, K, gd;
+  int vq;
+  int a_stream;                     // A operand streamed per stage (r > 256)
+  int nstage;
+  uint32_t stage_bytes;
+  uint32_t a_bytes;                 // resident A operand bytes (0 when streamed)
+  uint64_t timeout_ns;
+};
+
+uint32_t ctl_bytes();               // control block of the tensor-core kernels
+
+// ---- launchers (return cudaGetLastError() of the launch) -------------------
+cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps, const void* Pr,
+                             const void* C, PlanDevice& p, bool A_only, cudaStream_t s);
+cudaError_t launch_prep_f32(const mapl_config& c, const void* A, const void* Ps, const void* Pr,
+                            const void* C, PlanDevice& p, bool A_only, cudaStream_t s);
+
+cudaError_t launch_compress_tc(const CUtensorMap& tmX, const CUtensorMap& tmAt,
+                               const CUtensorMap& tmMt, const CUtensorMap& tmC,
+                               const CompressArgs& a, uint32_t smem_bytes, int grid,
+                               cudaStream_t s);
+cudaError_t launch_decompress_tc(const CUtensorMap& tmB, const CUtensorMap& tmZ,
+                                 const DecompressArgs& a, uint32_t smem_bytes, int grid,
+                                 cudaStream_t s);
+
+cudaError_t launch_compress_f32(const mapl_config& c, const PlanDevice& p, const float* X,
+                                const int32_t* tids, int64_t N, const float* E, void* out,
+                                int mode, cudaStream_t s);
+cudaError_t launch_decompress_f32(const mapl_config& c, const PlanDevice& p, const void* in,
+                                  const int32_t* tids, int64_t N, const float* E, float* Xh,
+                                  cudaStream_t s);
+
+size_t spel_workspace_bytes(int64_t d, int64_t r, int32_t batch);
+cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int batch, float lr,
+                        float beta, const float* coeffs, int n_lmo, int n_retr, void* ws,
+                        cudaStream_t s);
+
+}  // namespace mapl

@@ -1,0 +1,186 @@
+"""CUDA codec vs the fp64 oracle, through the C ABI (needs a GB300).
+
+Tolerances (relative Frobenius error per output tensor): 2e-2 for what the
+bf16 tensor-core path emits in bf16 (Z payload, X_hat), 1e-5 for fp32
+results (the fp32 Z that feeds VQ, and the whole fp32 CUDA-core path).  VQ
+indices must equal the oracle's except at certified near ties
+(tests/helpers.py:check_vq_indices).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import pipeline_activation_compression_gb300 as mapl
+from pipeline_activation_compression_gb300 import synth
+from tests.helpers import check_vq_indices, rel_frob, to_dev, to_host
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+TOL_F32 = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    mapl.build()
+    mapl.load_library()
+    torch.cuda.set_device(0)
+
+
+def plan_for(w, b):
+    dt = mapl.MAPL_BF16 if w.dtype == "bf16" else mapl.MAPL_F32
+    cfg = mapl.make_config(w.d, w.r, w.V, w.G, w.R, w.K, dt)
+    C = to_dev(b["C"]) if w.vq else None
+    return mapl.mapl_plan_create(cfg, to_dev(b["A"]), to_dev(b["P"]), to_dev(b["P_next"]), C)
+
+
+def run(plan, w, b, tids=None, check=True):
+    X = to_dev(b["X"])
+    t = torch.from_numpy(b["tids"] if tids is None else tids).cuda()
+    N = X.shape[0]
+    payload = torch.empty(plan.payload_shape(N), dtype=plan.payload_dtype(), device="cuda")
+    mapl.mapl_compress(plan, X, t, to_dev(b["E"]), payload)
+    Z32 = torch.empty(N, w.r, dtype=torch.float32, device="cuda")
+    mapl.mapl_compress_z32(plan, X, t, to_dev(b["E"]), Z32)
+    Xh = torch.empty(N, w.d, dtype=X.dtype, device="cuda")
+    mapl.mapl_decompress(plan, payload, t, to_dev(b["E_next"]), Xh)
+    if check:
+        mapl.mapl_check(plan)
+    torch.cuda.synchronize()
+    return to_host(payload), Z32.cpu().numpy(), to_host(Xh)
+
+
+def oracle_Z(b, rows=None):
+    sel = slice(None) if rows is None else rows
+    return oracle.compress(synth.widen(b["X"][sel]), b["tids"][sel], synth.widen(b["A"]),
+                           synth.widen(b["E"]), synth.widen(b["P"]))
+
+
+def check_outputs(w, b, payload, Z32, Xh, rows=None):
+    sel = slice(None) if rows is None else rows
+    Zo = oracle_Z(b, rows)
+    tol = TOL_BF16 if w.dtype == "bf16" else TOL_F32
+    assert rel_frob(Z32[sel], Zo) <= TOL_F32, "fp32 Z"
+    report = {"Z32": rel_frob(Z32[sel], Zo)}
+    if w.vq:
+        report.update(check_vq_indices(payload[sel], Z32[sel], Zo, b["C"]))
+        Zh = oracle.rvq_decode(payload[sel], synth.widen(b["C"]))
+    else:
+        report["Z"] = rel_frob(synth.widen(payload[sel]), Zo)
+        assert report["Z"] <= tol, "Z payload"
+        Zh = synth.widen(payload[sel])
+    Xo = oracle.reconstruct(Zh, b["tids"][sel], synth.widen(b["A"]), synth.widen(b["E_next"]),
+                            synth.widen(b["P_next"]))
+    report["Xhat"] = rel_frob(synth.widen(Xh[sel]), Xo)
+    assert report["Xhat"] <= tol, "X_hat"
+    return report
+
+
+# ---------------------------------------------------------------- oracle-size
+SMALL = [
+    ("tiny_d64_r16", None),
+    ("proj_d1024_r64", 1000),
+    ("proj_d1024_r128", 1000),
+    ("proj_d1024_r256", 1000),
+    ("proj_d1024_r512", 1000),
+    ("vq_d1024_r128", 1000),
+    ("vq_d2048_r128", 777),
+    ("vq_d2048_r256", 777),
+]
+
+
+@pytest.mark.parametrize("name,n", SMALL, ids=[s[0] for s in SMALL])
+def test_parity_small(name, n):
+    w = synth.WORKLOADS[name]
+    b = synth.make_boundary(w, n_tokens=n)
+    b["tids"][0] = 0
+    b["tids"][-1] = w.V - 1
+    plan = plan_for(w, b)
+    rep = check_outputs(w, b, *run(plan, w, b))
+    print(name, rep)
+
+
+# ------------------------------------------------------ full size, sampled rows
+@pytest.mark.parametrize("name", ["proj_d1024_r128", "vq_d1024_r128"])
+def test_parity_full_size_sampled(name):
+    w = synth.WORKLOADS[name]
+    b = synth.make_boundary(w)
+    plan = plan_for(w, b)
+    payload, Z32, Xh = run(plan, w, b)
+    rows = np.sort(np.random.default_rng(123).choice(w.N, size=1536, replace=False))
+    rows = np.unique(np.concatenate([rows, [0, w.N - 1]]))
+    rep = check_outputs(w, b, payload, Z32, Xh, rows=rows)
+    print(name, rep)
+    # every row was written (no NaN / poison left anywhere)
+    assert np.isfinite(Z32).all() and np.isfinite(synth.widen(Xh)).all()
+
+
+# ------------------------------------------------------------------ edge cases
+@pytest.mark.parametrize("n", [1, 127, 128, 129, 255])
+@pytest.mark.parametrize("name", ["vq_d1024_r128", "proj_d1024_r128", "tiny_d64_r16"])
+def test_ragged_sizes(name, n):
+    w = synth.WORKLOADS[name]
+    b = synth.make_boundary(w, n_tokens=n)
+    plan = plan_for(w, b)
+    check_outputs(w, b, *run(plan, w, b))
+
+
+@pytest.mark.parametrize("name", ["vq_d1024_r128", "proj_d1024_r256", "tiny_d64_r16"])
+def test_bad_token_ids_zero_rows_and_report(name):
+    w = synth.WORKLOADS[name]
+    b = synth.make_boundary(w, n_tokens=300)
+    t = b["tids"].copy()
+    t[5] = w.V
+    t[130] = -3
+    plan = plan_for(w, b)
+    payload, Z32, Xh = run(plan, w, b, tids=t, check=False)
+    with pytest.raises(mapl.MaplError) as ei:
+        mapl.mapl_check(plan)
+    assert ei.value.name == "MAPL_ERR_BAD_TOKEN"
+    mapl.mapl_check(plan)          # the error word was cleared
+    for rr in (5, 130):
+        assert np.all(payload[rr] == 0) and np.all(Z32[rr] == 0) and np.all(synth.widen(Xh[rr]) == 0)
+    good = np.setdiff1d(np.arange(300), [5, 130])
+    check_outputs(w, b, payload, Z32, Xh, rows=good)
+
+
+def test_update_A_matches_fresh_plan():
+    w = synth.WORKLOADS["vq_d1024_r128"]
+    b = synth.make_boundary(w, n_tokens=512)
+    b2 = synth.make_boundary(w, seed=7, n_tokens=512)
+    plan = plan_for(w, b)
+    mapl.mapl_plan_update_A(plan, to_dev(b2["A"]))
+    got = run(plan, w, b)
+    fresh = dict(b)
+    fresh["A"] = b2["A"]
+    ref = run(plan_for(w, fresh), w, fresh)
+    for g, r_ in zip(got, ref):
+        assert np.array_equal(g, r_)
+    check_outputs(w, fresh, *got)
+
+
+def test_repeatable_and_stream_ordered():
+    w = synth.WORKLOADS["vq_d1024_r128"]
+    b = synth.make_boundary(w, n_tokens=2048)
+    plan = plan_for(w, b)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        a1 = run(plan, w, b)
+    a2 = run(plan, w, b)
+    for x, y in zip(a1, a2):
+        assert np.array_equal(x, y)
+
+
+def test_exact_reconstruction_through_gpu():
+    """X = E[t] P + S A^T with E' = E, P' = P: without VQ the codec returns X
+    up to the bf16 rounding of Z and X_hat (§3.2: A^T inverts A on col(A))."""
+    w = synth.WORKLOADS["proj_d1024_r128"]
+    b = synth.make_boundary(w, n_tokens=640)
+    A = synth.widen(b["A"])
+    S = np.random.default_rng(5).standard_normal((640, w.r))
+    X = synth.widen(b["E"])[b["tids"]] @ synth.widen(b["P"]) + S @ A.T
+    b = dict(b, X=synth.bf16_bits(X), E_next=b["E"], P_next=b["P"])
+    plan = plan_for(w, b)
+    _, _, Xh = run(plan, w, b)
+    assert rel_frob(synth.widen(Xh), X) < TOL_BF16

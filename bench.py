@@ -1,0 +1,390 @@
+"""Benchmark of the MAPL boundary codec on GB300: compress (+ residual VQ) and
+reconstruct one micro-batch per step, as boundary tokens/s.
+
+Default workload: d=1024, r=128, 16 x 2048 tokens, bf16, VQ with G=4 groups,
+R=2 rounds, K=256 codes (8 bytes of indices per token).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the reference arm) on a bounded
+sample per step.  Under torchrun every rank runs its own micro-batches (the
+codec is per token, no collective on the data path) and rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "boundary tokens/s (compress+RVQ+reconstruct) and % roofline, d=1024 r=128"
+UNIT = "tokens/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="vq_d1024_r128")
+    p.add_argument("--e2e-steps", type=int, default=40)
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    return ws, rank
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, enabled=True):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        if enabled:
+            try:
+                os.makedirs(os.path.dirname(self.path), exist_ok=True)
+                self.f = open(self.path, "w")
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                     "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            except Exception:
+                self.proc = None
+
+    def stop(self, dev_index: int):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9 or not f[0].isdigit() or int(f[0]) != dev_index:
+                continue
+            try:
+                sms.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sms:
+            return None
+        return {"sm_mhz": float(np.median(sms)), "sm_max_mhz": mx, "samples": len(sms),
+                "reasons": sorted(reasons)}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("kernels_tc.cu", "ptx.cuh", "mapl_internal.h"):
+        with open(os.path.join(ROOT, "pipeline_activation_compression_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        j = json.load(f)
+    e = j.get(f"{kernel}:{workload}")
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+def algorithmic_bytes(w, tids: np.ndarray):
+    """Bytes a launch must move at minimum (HBM), per SURVEY-style accounting:
+    compress:   X (2d) + tid (4) + payload out, per token; unique anchor rows
+                (2r each) and the parameters (A^T, M splits, codebooks) once.
+    decompress: payload in + tid (4) + X_hat (2d), per token; unique anchor
+                rows of the receiver and the parameters ([A | P'^T], codebooks).
+    """
+    N = tids.size
+    payload = w.R * w.G if w.vq else 2 * w.r
+    U = np.unique(tids).size
+    books = (w.R * w.G * w.K * w.gd * 2) if w.vq else 0
+    comp = N * (2 * w.d + 4 + payload) + U * 2 * w.r + 2 * w.d * w.r + 3 * 2 * w.r * w.r + books
+    decomp = N * (payload + 4 + 2 * w.d) + U * 2 * w.r + 2 * w.d * 2 * w.r + books
+    return float(comp), float(decomp), U
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_step(b, w, rows):
+    import oracle
+    W = np.asarray
+    from pipeline_activation_compression_gb300 import synth
+    X = synth.widen(b["X"][rows])
+    t = b["tids"][rows]
+    Z = oracle.compress(X, t, synth.widen(b["A"]), synth.widen(b["E"]), synth.widen(b["P"]))
+    if w.vq:
+        C = synth.widen(b["C"])
+        idx = oracle.rvq_encode(Z, C)["idx"]
+        Zh = oracle.rvq_decode(idx, C)
+    else:
+        Zh = Z
+    return oracle.reconstruct(Zh, t, synth.widen(b["A"]), synth.widen(b["E_next"]),
+                              synth.widen(b["P_next"]))
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def time_oracle(b, w, tokens: int, budget_s: float):
+    """Oracle tokens/s on chunks of `tokens` rows until `budget_s` elapses."""
+    rng = np.random.default_rng(0)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        rows = np.sort(rng.choice(b["tids"].size, size=tokens, replace=False))
+        oracle_step(b, w, rows)
+        done += tokens
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return done / el, done, el
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(args, ws, rank):
+    import torch
+    import pipeline_activation_compression_gb300 as mapl
+    from pipeline_activation_compression_gb300 import synth
+
+    dev = torch.cuda.current_device()
+    mapl.build()
+    mapl.load_library()
+    w = synth.WORKLOADS[args.workload]
+    b = synth.make_boundary(w, seed=rank)
+    N = w.N
+
+    def to_dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(a).cuda()
+
+    dt = mapl.MAPL_BF16 if w.dtype == "bf16" else mapl.MAPL_F32
+    cfg = mapl.make_config(w.d, w.r, w.V, w.G, w.R, w.K, dt)
+    plan = mapl.mapl_plan_create(cfg, to_dev(b["A"]), to_dev(b["P"]), to_dev(b["P_next"]),
+                                 to_dev(b["C"]) if w.vq else None)
+    E, En = to_dev(b["E"]), to_dev(b["E_next"])
+    t = to_dev(b["tids"])
+    x0 = to_dev(b["X"])
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    xbytes = x0.numel() * x0.element_size()
+    nsets = max(3, int(np.ceil(2 * l2 / xbytes)) + 1)
+    Xs = [x0] + [x0.clone() for _ in range(nsets - 1)]
+    Xh = [torch.empty(N, w.d, dtype=x0.dtype, device="cuda") for _ in range(nsets)]
+    pay = [torch.empty(plan.payload_shape(N), dtype=plan.payload_dtype(), device="cuda")
+           for _ in range(nsets)]
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        k = i % nsets
+        mapl.mapl_compress(plan, Xs[k], t, E, pay[k], stream)
+        mapl.mapl_decompress(plan, pay[k], t, En, Xh[k], stream)
+
+    for i in range(args.warmup):
+        step(i)
+    mapl.mapl_check(plan)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K + 1)]
+    clocks = ClockSampler(enabled=(rank == 0 and not args.no_clocks))
+    barrier(ws)
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(K):
+        k = i % nsets
+        mapl.mapl_compress(plan, Xs[k], t, E, pay[k], stream)
+        ev[2 * i + 1].record(stream)
+        mapl.mapl_decompress(plan, pay[k], t, En, Xh[k], stream)
+        ev[2 * i + 2].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop(dev) if rank == 0 else None
+    mapl.mapl_check(plan)
+    total_ms = ev[0].elapsed_time(ev[2 * K])
+    comp_ms = np.array([ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(K)])
+    dec_ms = np.array([ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(K)])
+    total_ms = max_over_ranks(total_ms, ws)
+
+    # end to end through the public API: pinned host X in, X_hat out
+    Ke = args.e2e_steps
+    xh_host = torch.from_numpy(np.ascontiguousarray(b["X"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    t_host = torch.from_numpy(b["tids"]).pin_memory()
+    out_host = torch.empty(N, w.d, dtype=torch.bfloat16).pin_memory()
+    xd, td = torch.empty_like(x0), torch.empty_like(t)
+    for _ in range(3):
+        xd.copy_(xh_host, non_blocking=True)
+        td.copy_(t_host, non_blocking=True)
+        mapl.mapl_compress(plan, xd, td, E, pay[0], stream)
+        mapl.mapl_decompress(plan, pay[0], td, En, Xh[0], stream)
+        out_host.copy_(Xh[0], non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    e0.record(stream)
+    for _ in range(Ke):
+        xd.copy_(xh_host, non_blocking=True)
+        td.copy_(t_host, non_blocking=True)
+        mapl.mapl_compress(plan, xd, td, E, pay[0], stream)
+        mapl.mapl_decompress(plan, pay[0], td, En, Xh[0], stream)
+        out_host.copy_(Xh[0], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
+    mapl.mapl_check(plan)
+
+    if rank != 0:
+        return None
+    comp_b, dec_b, U = algorithmic_bytes(w, b["tids"])
+    comp_avg, dec_avg = float(comp_ms.mean()), float(dec_ms.mean())
+    dom = "mapl_compress" if comp_avg >= dec_avg else "mapl_decompress"
+    dom_bytes, dom_ms = (comp_b, comp_avg) if dom == "mapl_compress" else (dec_b, dec_avg)
+    peak, peak_kind = peaks()
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    step_bytes = comp_b + dec_b
+    tokens = N * K * ws
+    value = tokens / (total_ms * 1e-3)
+
+    # CPU baseline: the oracle as it stands, bounded sample
+    cps, done, el = time_oracle(b, w, 1024, 10.0)
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "d": w.d, "r": w.r, "V": w.V, "G": w.G, "R": w.R,
+                   "K": w.K, "tokens_per_step": N, "micro_batch": f"{w.B}x{w.T}",
+                   "payload_bytes_per_token": w.R * w.G if w.vq else 2 * w.r,
+                   "l2": f"{nsets} rotating input/output sets ({2 * nsets * xbytes >> 20} MiB) > L2",
+                   "step": "mapl_compress + mapl_decompress on one stream"},
+        "kernels": {"mapl_compress_us": comp_avg * 1e3, "mapl_decompress_us": dec_avg * 1e3,
+                    "step_GBps": step_bytes / (total_ms / K * 1e-3) / 1e9,
+                    "unique_token_rows": U},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "algorithmic_bytes_per_launch": dom_bytes,
+                     "traffic": profiled_traffic(dom, w.name),
+                     "step_frac": (step_bytes / (total_ms / K * 1e-3) / 1e9) / peak},
+        "e2e": {"value": N * Ke * ws / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": int(xh_host.numel() * 2 + t_host.numel() * 4),
+                "d2h_bytes_per_step": int(out_host.numel() * 2)},
+        "gpu_launches": 2 * K,
+        "cpu_baseline": {"value": cps, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                         "sample": f"{done} tokens of {w.name} in chunks of 1024 random rows, "
+                                   f"{el:.1f} s (numpy fp64; BLAS threads for the GEMMs, "
+                                   f"VQ search single-threaded)"},
+    }
+    if clk is not None:
+        res["clocks"] = clk
+    return res
+
+
+# ---------------------------------------------------------- reference arm
+def run_reference(args, ws, rank):
+    from pipeline_activation_compression_gb300 import synth
+    if rank != 0:
+        return None
+    w = synth.WORKLOADS[args.workload]
+    b = synth.make_boundary(w, n_tokens=min(w.N, 8192))
+    # per-token cost, then a per-step sample that keeps the run within minutes
+    rate, _, _ = time_oracle(b, w, 256, 2.0)
+    budget = 120.0
+    per_step = int(max(1, min(1024, rate * budget / max(1, args.steps + args.warmup))))
+    rng = np.random.default_rng(1)
+    for _ in range(args.warmup):
+        oracle_step(b, w, np.sort(rng.choice(b["tids"].size, per_step, replace=False)))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(b, w, np.sort(rng.choice(b["tids"].size, per_step, replace=False)))
+    el = time.perf_counter() - t0
+    value = per_step * args.steps / el
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "d": w.d, "r": w.r, "G": w.G, "R": w.R, "K": w.K,
+                   "tokens_per_step": per_step},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                         "sample": f"{per_step} random tokens of {w.name} per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    ws, rank = dist_setup(args) if args.impl == "ours" else (
+        int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
+    if args.gpus != ws and ws > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {ws}")
+    res = run_ours(args, ws, rank) if args.impl == "ours" else run_reference(args, ws, rank)
+    if res is not None and rank == 0:
+        print(json.dumps(res), flush=True)
+    if ws > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -40,6 +40,7 @@ struct Ctl {
   uint64_t tempty[2]; // decompress: accumulator drained
   uint32_t tmem_base;
   int abort;
+  int gate;           // anchor-gather items whose stage the producer has freed
   int32_t tids[kTile];
 };
 
@@ -172,6 +173,7 @@ __device__ __forceinline__ void vq_epilogue(const CompressArgs& a, Ctl* ctl, uin
         int kb = k1;
         for (int c0 = 0; c0 < K; c0 += 16) {
           float v[16];
+          __syncwarp();
           tmem_ld16(tdist + c0, v);
           tmem_wait_ld();
           if (need) {
@@ -257,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&ctl->uready), 1);
     mbar_init(smem_u32(&ctl->dready), 1);
     ctl->abort = 0;
+    ctl->gate = 0;
     fence_mbar_init();
     fence_async_shared();
   }
@@ -293,7 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = 0; h < nh; ++h)
             tma_load_2d(st + kBlockBytes + h * 256u * 128u, &tmMt, kb * 64, sp * r + h * nrow,
                         fb);
-          // the second arrival comes from the anchor gather
+          // the stage is free: let the anchor gather fill its A half; the
+          // gather's arrival is the second one on full[s]
+          gate_publish(smem_u32(&ctl->gate), j + 1);
         } else {
           const int j = i - nproj, g = j / a.R, rho = j % a.R;
           mbar_arrive_expect_tx(fb, a.K * 128u);
@@ -353,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar_sync(kEpiBar, kEpiThreads);
     bool alive = true;
     for (int j = 0; j < na && alive; ++j) {
-      const int i = nkx + j, s = i % nst, use = i / nst;
-      bool ok = mbar_wait(smem_u32(&ctl->empty[s]), (use & 1) ^ 1, &ctl->abort, a.timeout_ns);
+      const int i = nkx + j, s = i % nst;
+      bool ok = gate_wait(smem_u32(&ctl->gate), j, &ctl->abort, a.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
         give_up(ctl, a.err);
@@ -386,14 +391,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         for (int c0 = 0; c0 < r; c0 += 32) {
           float v[32];
+          __syncwarp();
           tmem_ld32(trow + c0, v);
           tmem_wait_ld();
-          if (!store) continue;
           if (bad) {
 #pragma unroll
             for (int q = 0; q < 32; ++q) v[q] = 0.f;
           }
-          if (a.mode == kModeZ32) {
+          if (!store) {
+          } else if (a.mode == kModeZ32) {
             float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) +
                                                     static_cast<size_t>(n) * r + c0);
 #pragma unroll
@@ -417,7 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tbase, tmem_cols);
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tbase, tmem_cols);
+  }
 }
 
 // ======================================================================
@@ -499,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
     mbar_init(smem_u32(&ctl->aready), 2);
+    ctl->gate = 0;
     for (int q = 0; q < 2; ++q) {
       mbar_init(smem_u32(&ctl->tfull[q]), 1);
       mbar_init(smem_u32(&ctl->tempty[q]), 1);
@@ -544,7 +554,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           mbar_arrive_expect_tx(fb, NC * 128u);
           tma_load_2d(st + a_slot, &tmB, kb * 64, c * NC, fb);
-          if (!stream) mbar_arrive(fb);   // streamed E' blocks: builders arrive
+          if (!stream) {
+            mbar_arrive(fb);
+          } else {
+            // streamed E' block: the stage is free for the builders, who
+            // give the second arrival; gate counts such items in order
+            gate_publish(smem_u32(&ctl->gate), c * nzb + (kb - nzb) + 1);
+          }
         }
       }
     }
@@ -606,8 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c <= nchunk && alive; ++c) {
       if (stream && c < nchunk) {
         for (int kb = nzb; kb < nka; ++kb) {
-          const int i = c * nka + kb, s = i % nst, use = i / nst;
-          bool ok = mbar_wait(smem_u32(&ctl->empty[s]), (use & 1) ^ 1, &ctl->abort,
+          const int i = c * nka + kb, s = i % nst;
+          bool ok = gate_wait(smem_u32(&ctl->gate), c * nzb + (kb - nzb), &ctl->abort,
                               a.timeout_ns);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) {
@@ -635,9 +651,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       for (int c0 = 0; c0 < NC; c0 += 32) {
         float v[32];
+        __syncwarp();
         tmem_ld32(trow + acc * NC + c0, v);
         tmem_wait_ld();
-        if (!store) continue;
+        if (!store) continue;   // no collective operation follows in this iteration
         uint4* dst = reinterpret_cast<uint4*>(a.Xh + static_cast<size_t>(n) * d + cd * NC + c0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -659,7 +676,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tbase, tmem_cols);
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tbase, tmem_cols);
+  }
 }
 
 template <typename KernelT>

@@ -69,6 +69,35 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return true;
 }
 
+// Monotonic gate counter in shared memory.  A waiter that may fall more than
+// one mbarrier phase behind cannot use a parity wait (the parity of phase k
+// and k+2 are equal); it waits for a counter that only ever grows instead.
+__device__ __forceinline__ void gate_publish(uint32_t gate, int value) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(gate), "r"(value) : "memory");
+}
+
+__device__ __forceinline__ int gate_read(uint32_t gate) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(gate) : "memory");
+  return v;
+}
+
+// Wait until the gate counter exceeds `index`; false on give-up (as mbar_wait).
+__device__ __forceinline__ bool gate_wait(uint32_t gate, int index, volatile int* abort,
+                                          uint64_t budget_ns) {
+  if (gate_read(gate) > index) return true;
+  const uint64_t t0 = global_ns();
+  uint32_t spins = 0;
+  while (gate_read(gate) <= index) {
+    __nanosleep(32);
+    if ((++spins & 63u) == 0u) {
+      if (*abort) return false;
+      if (global_ns() - t0 > budget_ns) return false;
+    }
+  }
+  return true;
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
                                             uint32_t bar) {

@@ -80,7 +80,7 @@ def check_vq_indices(idx_gpu, Z32_gpu, Z_oracle, C, rel_tie=1e-6, max_mismatch_f
                     f"g={g}: gpu {idx_gpu[n, rho, g]} (D={D[n, idx_gpu[n, rho, g]]:.9g}) vs "
                     f"{ref[n]} (D={D[n, ref[n]]:.9g})")
     # 2. oracle parity with certified near ties
-    res = oracle.rvq_encode_given(Z_oracle, C, idx_gpu, rel_tie=rel_tie)
+    res = oracle.rvq_encode_given(Z_oracle, Cd, idx_gpu, rel_tie=rel_tie)
     mism = np.argwhere(res["idx"] != idx_gpu)
     u = np.asarray(Z_oracle, dtype=np.float64).copy()
     worst = 0.0

@@ -38,6 +38,9 @@ def parse():
     p.add_argument("--workload", default="vq_d1024_r128")
     p.add_argument("--e2e-steps", type=int, default=40)
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--tokens", type=int, default=0,
+                   help="tokens per step (default: the workload's micro-batch); for profiling")
+    p.add_argument("--skip-cpu", action="store_true", help="skip the CPU-baseline timing")
     return p.parse_args()
 
 
@@ -77,11 +80,12 @@ class ClockSampler:
 
     def __init__(self, enabled=True):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = None
         if enabled:
             try:
-                os.makedirs(os.path.dirname(self.path), exist_ok=True)
-                self.f = open(self.path, "w")
+                import tempfile
+                fd, self.path = tempfile.mkstemp(prefix="mapl_clocks_", suffix=".csv")
+                self.f = os.fdopen(fd, "w")
                 self.proc = subprocess.Popen(
                     ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
                      "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
@@ -149,7 +153,7 @@ def profiled_traffic(kernel: str, workload: str):
 
 
 def algorithmic_bytes(w, tids: np.ndarray):
-    """Bytes a launch must move at minimum (HBM), per SURVEY-style accounting:
+    """Bytes a launch must move at minimum through HBM (algorithmic count):
     compress:   X (2d) + tid (4) + payload out, per token; unique anchor rows
                 (2r each) and the parameters (A^T, M splits, codebooks) once.
     decompress: payload in + tid (4) + X_hat (2d), per token; unique anchor
@@ -212,8 +216,8 @@ def run_ours(args, ws, rank):
     mapl.build()
     mapl.load_library()
     w = synth.WORKLOADS[args.workload]
-    b = synth.make_boundary(w, seed=rank)
-    N = w.N
+    N = args.tokens or w.N
+    b = synth.make_boundary(w, seed=rank, n_tokens=N)
 
     def to_dev(a):
         a = np.ascontiguousarray(a)
@@ -308,13 +312,14 @@ def run_ours(args, ws, rank):
     value = tokens / (total_ms * 1e-3)
 
     # CPU baseline: the oracle as it stands, bounded sample
-    cps, done, el = time_oracle(b, w, 1024, 10.0)
+    cps, done, el = (0.0, 0, 0.0) if args.skip_cpu else time_oracle(b, w, min(1024, N), 10.0)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "d": w.d, "r": w.r, "V": w.V, "G": w.G, "R": w.R,
-                   "K": w.K, "tokens_per_step": N, "micro_batch": f"{w.B}x{w.T}",
+                   "K": w.K, "tokens_per_step": N,
+                   "micro_batch": f"{w.B}x{w.T}" if N == w.N else f"{N} tokens",
                    "payload_bytes_per_token": w.R * w.G if w.vq else 2 * w.r,
                    "l2": f"{nsets} rotating input/output sets ({2 * nsets * xbytes >> 20} MiB) > L2",
                    "step": "mapl_compress + mapl_decompress on one stream"},

@@ -160,6 +160,34 @@ mapl_status mapl_spel_step(float* A, const float* G, float* m, int64_t d, int64_
                            int32_t n_lmo, int32_t n_retr, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * mapl_spel_step_static -- the SPEL step above without a caller workspace.
+ * The MAPL paper has no counterpart; this entry exists for callers that
+ * cannot allocate device memory when they run the update: a framework whose
+ * caching allocator has already reserved the device memory it is allowed to
+ * use, a latency-bound loop that cannot afford cudaMalloc's implicit device
+ * synchronisation, or a plugin interface whose fixed signature only passes
+ * the tensors themselves.
+ *
+ * Same arguments and results as mapl_spel_step minus the workspace.  The
+ * scratch is a fixed 16 MiB array in the library's device image, reserved on
+ * every GPU that loads the library until the process exits;
+ * mapl_spel_workspace_size(d, r, batch) must not exceed it (e.g. d = 1024,
+ * r = 256, batch = 3 fits; d = 2048, r = 256, batch = 3 does not), otherwise
+ * MAPL_ERR_UNSUPPORTED is returned and nothing runs.  The call allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array: calls whose work overlaps on the GPU
+ *    (different streams, or several threads) race on it and must be
+ *    serialised by the caller.  Nothing in the array needs to start at zero;
+ *    each call overwrites what it reads.
+ */
+mapl_status mapl_spel_step_static(float* A, const float* G, float* m, int64_t d, int64_t r,
+                                  int32_t batch, float lr, float beta, const float* coeffs,
+                                  int32_t n_lmo, int32_t n_retr, cudaStream_t stream);
+
 /* Message of the calling thread's last failed call ("" if none). */
 const char* mapl_last_error(void);
 

@@ -18,7 +18,8 @@ __all__ = [
     "MaplError", "MaplConfig", "Plan", "load_library", "library_path", "build",
     "mapl_plan_create", "mapl_plan_update_A", "mapl_payload_bytes", "mapl_compress",
     "mapl_compress_z32", "mapl_decompress", "mapl_check", "mapl_plan_destroy",
-    "mapl_spel_workspace_size", "mapl_spel_step", "mapl_last_error", "mapl_version",
+    "mapl_spel_workspace_size", "mapl_spel_step", "mapl_spel_step_static", "mapl_last_error",
+    "mapl_version",
     "MAPL_F32", "MAPL_BF16", "STATUS",
 ]
 
@@ -73,6 +74,8 @@ def load_library():
         "mapl_spel_workspace_size": [I64, I64, I32, ctypes.POINTER(SZ)],
         "mapl_spel_step": [P, P, P, I64, I64, I32, ctypes.c_float, ctypes.c_float, P, I32, I32,
                            P, SZ, P],
+        "mapl_spel_step_static": [P, P, P, I64, I64, I32, ctypes.c_float, ctypes.c_float, P,
+                                  I32, I32, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -240,3 +243,19 @@ def mapl_spel_step(A, G, m, lr: float, beta: float, coeffs, n_lmo: int, n_retr: 
         d, r, b, float(lr), float(beta), co.ctypes.data_as(ctypes.c_void_p), int(n_lmo),
         int(n_retr), _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def mapl_spel_step_static(A, G, m, lr: float, beta: float, coeffs, n_lmo: int, n_retr: int,
+                          stream=None):
+    """SPEL update without a workspace argument, for callers that cannot
+    allocate: the library's fixed 16 MiB device scratch is used instead (see
+    include/mapl.h).  Calls that overlap on the GPU race on that scratch."""
+    import torch
+    co = np.ascontiguousarray(np.asarray(coeffs, dtype=np.float32).reshape(-1))
+    if co.size != 3 * (n_lmo + n_retr):
+        raise ValueError("coeffs must hold (n_lmo + n_retr) rows of (a, b, c)")
+    b, d, r = A.shape
+    _check(load_library().mapl_spel_step_static(
+        _ptr(A, torch.float32, "A"), _ptr(G, torch.float32, "G"), _ptr(m, torch.float32, "m"),
+        d, r, b, float(lr), float(beta), co.ctypes.data_as(ctypes.c_void_p), int(n_lmo),
+        int(n_retr), _stream(stream)))

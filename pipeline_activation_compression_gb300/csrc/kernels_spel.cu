@@ -268,3 +268,44 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
 }
 
 }  // namespace mapl
+
+// ---------------------------------------------------------------------------
+// Fixed-scratch variant of the SPEL step for callers that cannot allocate.
+//
+// The scratch lives in this file-scope device array, reserved on every GPU
+// that loads the library for as long as the process runs.  Host code cannot
+// hand the array's name to a kernel (in host code it is only a stand-in, not
+// a device address); its device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current, and cached here.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace mapl {
+
+namespace {
+
+__device__ __align__(256) unsigned char g_spel_scratch[kSpelStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+}  // namespace
+
+cudaError_t spel_static_scratch(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_spel_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace mapl

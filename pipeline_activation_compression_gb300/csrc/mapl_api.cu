@@ -485,4 +485,31 @@ mapl_status mapl_spel_step(float* A, const float* G, float* m, int64_t d, int64_
   return MAPL_OK;
 }
 
+mapl_status mapl_spel_step_static(float* A, const float* G, float* m, int64_t d, int64_t r,
+                                  int32_t batch, float lr, float beta, const float* coeffs,
+                                  int32_t n_lmo, int32_t n_retr, cudaStream_t stream) {
+  if (!A || !G || !m || !coeffs) return fail(MAPL_ERR_INVALID_ARG, "NULL pointer argument");
+  size_t need = 0;
+  mapl_status st = mapl_spel_workspace_size(d, r, batch, &need);
+  if (st != MAPL_OK) return st;
+  if (need > kSpelStaticScratchBytes)
+    return fail(MAPL_ERR_UNSUPPORTED,
+                "mapl_spel_step_static: (d=%lld, r=%lld, batch=%d) needs %zu bytes of scratch, "
+                "more than the fixed %zu; use mapl_spel_step with a caller workspace",
+                static_cast<long long>(d), static_cast<long long>(r), batch, need,
+                kSpelStaticScratchBytes);
+  if (n_lmo < 0 || n_retr < 0 || n_lmo + n_retr < 1 || n_lmo + n_retr > 32)
+    return fail(MAPL_ERR_INVALID_ARG, "need 1 <= n_lmo + n_retr <= 32");
+  if (!aligned16(A) || !aligned16(G) || !aligned16(m))
+    return fail(MAPL_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if (!(beta >= 0.f && beta < 1.f)) return fail(MAPL_ERR_INVALID_ARG, "beta must be in [0, 1)");
+  void* scratch = nullptr;
+  cudaError_t e = spel_static_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static SPEL scratch)");
+  e = launch_spel(A, G, m, static_cast<int>(d), static_cast<int>(r), batch, lr, beta, coeffs,
+                  n_lmo, n_retr, scratch, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "spel launch");
+  return MAPL_OK;
+}
+
 }  // extern "C"

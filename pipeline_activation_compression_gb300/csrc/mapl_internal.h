@@ -99,6 +99,12 @@ cudaError_t launch_decompress_f32(const mapl_config& c, const PlanDevice& p, con
                                   cudaStream_t s);
 
 size_t spel_workspace_bytes(int64_t d, int64_t r, int32_t batch);
+
+// Size of the fixed device scratch behind mapl_spel_step_static (16 MiB).
+constexpr size_t kSpelStaticScratchBytes = static_cast<size_t>(16) << 20;
+// Device address of that scratch on the current device (looked up once per
+// device with cudaGetSymbolAddress and cached).
+cudaError_t spel_static_scratch(void** out);
 cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int batch, float lr,
                         float beta, const float* coeffs, int n_lmo, int n_retr, void* ws,
                         cudaStream_t s);

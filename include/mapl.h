@@ -58,7 +58,7 @@ typedef enum { MAPL_F32 = 0, MAPL_BF16 = 1 } mapl_dtype;
  *   group and round.  G = R = K = 0 disables VQ: the payload is Z itself.
  * Limits: d % 64 == 0, r % 16 == 0, r <= 512, 1 <= V.  With VQ: G divides r,
  * 1 <= R <= 8, 1 <= K <= 256 (uint8 indices).  The bf16 tensor-core path
- * additionally needs r <= 256 with VQ, gd <= 64, K % 16 == 0 and r + K <= 512.
+ * needs r % 64 == 0 and, with VQ, r <= 256, gd in {16, 32} and K % 64 == 0.
  * MAPL_F32 runs on CUDA cores in fp32 (any sizes within the limits above).
  */
 typedef struct {

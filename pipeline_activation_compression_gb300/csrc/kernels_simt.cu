@@ -83,11 +83,11 @@ __global__ void k_prep_codes(const void* C, int nbooks, int K, int gd, bool bf,
     if (Cb) Cb[static_cast<size_t>(idx) * gd + i] = reinterpret_cast<const __nv_bfloat16*>(C)[static_cast<size_t>(idx) * gd + i];
     if (C32) C32[static_cast<size_t>(idx) * gd + i] = static_cast<float>(v);
   }
-  if (Cpad) {
+  if (Cpad) {   // [c | c | 0]: the same code against the hi and the lo residual term
+    const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(C) + static_cast<size_t>(idx) * gd;
     for (int i = 0; i < 64; ++i)
       Cpad[static_cast<size_t>(idx) * 64 + i] =
-          i < gd ? reinterpret_cast<const __nv_bfloat16*>(C)[static_cast<size_t>(idx) * gd + i]
-                 : __float2bfloat16(0.f);
+          i < 2 * gd ? src[i % gd] : __float2bfloat16(0.f);
   }
   cnorm[idx] = static_cast<float>(s);
 }

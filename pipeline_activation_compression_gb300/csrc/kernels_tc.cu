@@ -1,11 +1,4 @@
-// kernels_tc.cu -- tcgen05 / TMA kernels of the MAPL boundary codec (bf16).
-//
-// compress (MAPL §3.2 eq. (1) with the anchor folded through M = P A, then the
-// multi-codebook residual VQ of §3.5):
-//   Z = X A - E[tids] M          one TMEM accumulator, K = d + S*r
-//   VQ: per group g and round rho, the distance dot products u.c for all K
-//   codes come from one tensor-core MMA (bf16 residual x bf16 codebook); the
-//   argmin, its certification and the residual update run on CUDA cores.
+// kernels_tc.cu -- tcgen05 / TMA decompress kernel of the MAPL codec (bf16).
 //
 // decompress (eq. (2)):
 //   X_hat = [Z_hat | E'[tids]] [A^T ; P']   one contraction with K = 2r
@@ -85,347 +78,6 @@ __device__ __forceinline__ void load_tids(const int32_t* __restrict__ tids, int 
       }
     }
     tids_s[q] = t;
-  }
-}
-
-// ======================================================================
-// compress
-// ======================================================================
-template <int GD>
-__device__ __forceinline__ void vq_epilogue(const CompressArgs& a, Ctl* ctl, uint32_t tz,
-                                            uint32_t tdist, uint32_t ubuf, const float* cn_s,
-                                            int row, int tid, bool store, bool bad,
-                                            int n) {
-  constexpr int kChunks = GD / 8;
-  const int G = a.G, R = a.R, K = a.K;
-  uint8_t* idx_out = reinterpret_cast<uint8_t*>(a.out) + static_cast<size_t>(n) * R * G;
-  const uint32_t fullmask = 0xffffffffu;
-  int item = 0;
-  for (int g = 0; g < G; ++g) {
-    float u[GD];
-#pragma unroll
-    for (int c = 0; c < GD; c += 16) {
-      float t16[16];
-      tmem_ld16(tz + g * GD + c, t16);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 16; ++i) u[c + i] = t16[i];
-    }
-    for (int rho = 0; rho < R; ++rho, ++item) {
-      // residual (bf16) -> A operand of the distance MMA
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        uint4 v;
-        v.x = pack_bf16x2(u[c * 8 + 0], u[c * 8 + 1]);
-        v.y = pack_bf16x2(u[c * 8 + 2], u[c * 8 + 3]);
-        v.z = pack_bf16x2(u[c * 8 + 4], u[c * 8 + 5]);
-        v.w = pack_bf16x2(u[c * 8 + 6], u[c * 8 + 7]);
-        st_shared_v4(ubuf + sw128_off(row, c), v);
-      }
-      fence_async_shared();
-      tc_fence_before();
-      named_bar_sync(kEpiBar, kEpiThreads);
-      if (tid == 0) mbar_arrive(smem_u32(&ctl->uready));
-      bool ok = mbar_wait(smem_u32(&ctl->dready), item & 1, &ctl->abort, a.timeout_ns);
-      ok = __all_sync(fullmask, ok);
-      if (!ok) {
-        give_up(ctl, a.err);
-        return;
-      }
-      tc_fence_after();
-
-      const int book = rho * G + g;
-      const float* cn = cn_s + book * K;
-      float nu2 = 0.f;
-#pragma unroll
-      for (int i = 0; i < GD; ++i) nu2 = fmaf(u[i], u[i], nu2);
-      const float nu = sqrtf(nu2);
-      const float cm = __ldg(a.cmax + book);
-
-      // coarse pass: D~_k = ||c_k||^2 - 2 u_bf16 . c_k ; keep best, its index
-      // and the second best value (exact ties keep the lowest index)
-      float b1 = __int_as_float(0x7f800000), b2 = b1;
-      int k1 = 0;
-      for (int c0 = 0; c0 < K; c0 += 16) {
-        float v[16];
-        tmem_ld16(tdist + c0, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float D = fmaf(-2.f, v[j], cn[c0 + j]);
-          const bool lt = D < b1;
-          b2 = fminf(b2, fmaxf(b1, D));
-          k1 = lt ? (c0 + j) : k1;
-          b1 = fminf(b1, D);
-        }
-      }
-      // |D~_k - D_k| <= eps for every k, D_k the same quantity computed
-      // exactly from the fp32 residual: bf16 rounding of u (2^-9 relative,
-      // doubled by the factor 2), fp32 accumulation of <= 64 exact products,
-      // fp32 rounding of ||c||^2 and of the fma.
-      const float eps = 0.0041f * nu * cm + 2.4e-7f * (cm * cm + fabsf(b1));
-      const bool need = (b2 - b1) <= 2.f * eps;
-      if (__any_sync(fullmask, need)) {
-        // refinement: every code within 2 eps of the best is re-scored with
-        // the exact squared distance in fp64; lowest index wins exact ties
-        const float thr = b1 + 2.f * eps;
-        double best = 1e300;
-        int kb = k1;
-        for (int c0 = 0; c0 < K; c0 += 16) {
-          float v[16];
-          __syncwarp();
-          tmem_ld16(tdist + c0, v);
-          tmem_wait_ld();
-          if (need) {
-            for (int j = 0; j < 16; ++j) {
-              if (fmaf(-2.f, v[j], cn[c0 + j]) <= thr) {
-                const __nv_bfloat16* cr =
-                    a.Cb + (static_cast<size_t>(book) * K + c0 + j) * GD;
-                double e = 0.0;
-#pragma unroll
-                for (int i = 0; i < GD; ++i) {
-                  const double df = static_cast<double>(u[i]) -
-                                    static_cast<double>(__bfloat162float(cr[i]));
-                  e = fma(df, df, e);
-                }
-                if (e < best) {
-                  best = e;
-                  kb = c0 + j;
-                }
-              }
-            }
-          }
-        }
-        if (need) k1 = kb;
-      }
-      if (store) idx_out[rho * G + g] = bad ? static_cast<uint8_t>(0) : static_cast<uint8_t>(k1);
-      // residual update with the chosen code
-      const uint4* cr4 =
-          reinterpret_cast<const uint4*>(a.Cb + (static_cast<size_t>(book) * K + k1) * GD);
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        const uint4 w = __ldg(cr4 + c);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
-#pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-          const float2 f = __bfloat1622float2(h[e2]);
-          u[c * 8 + 2 * e2] -= f.x;
-          u[c * 8 + 2 * e2 + 1] -= f.y;
-        }
-      }
-      tmem_wait_ld();
-    }
-  }
-}
-
-template <int GD>
-__global__ void __launch_bounds__(kThreads, 1)
-    k_compress_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmAt,
-                  const __grid_constant__ CUtensorMap tmMt, const __grid_constant__ CUtensorMap tmC,
-                  const CompressArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = align1024(smem_raw);
-  const int nst = a.nstage;
-  const uint32_t sb = a.stage_bytes;
-  const uint32_t ring = smem_u32(base);
-  const bool vq = (a.mode == kModeVQ);
-  uint32_t off = nst * sb;
-  const uint32_t ubuf = ring + off;
-  if (vq) off += kBlockBytes;
-  float* cn_s = reinterpret_cast<float*>(base + off);
-  if (vq) off += static_cast<uint32_t>(a.R * a.G * a.K) * 4u;
-  Ctl* ctl = reinterpret_cast<Ctl*>(base + ((off + 15u) & ~15u));
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x;
-  const int r = a.r;
-  const int nkx = a.d / 64;                 // K-blocks of X A
-  const int nkr = r / 64;                   // K-blocks of E M (per split)
-  const int na = kNumSplit * nkr;
-  const int nproj = nkx + na;
-  const int nvq = vq ? a.G * a.R : 0;
-  const int nitems = nproj + nvq;
-  const int nh = r > 256 ? 2 : 1;           // N halves of the projection MMA
-  const int nrow = r > 256 ? 256 : r;       // rows of one B box
-  uint32_t tmem_cols = 32;
-  while (tmem_cols < static_cast<uint32_t>(r + (vq ? a.K : 0))) tmem_cols <<= 1;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < nst; ++s) {
-      mbar_init(smem_u32(&ctl->full[s]), 2);
-      mbar_init(smem_u32(&ctl->empty[s]), 1);
-    }
-    mbar_init(smem_u32(&ctl->zfull), 1);
-    mbar_init(smem_u32(&ctl->uready), 1);
-    mbar_init(smem_u32(&ctl->dready), 1);
-    ctl->abort = 0;
-    ctl->gate = 0;
-    fence_mbar_init();
-    fence_async_shared();
-  }
-  if (warp == 1) tmem_alloc(smem_u32(&ctl->tmem_base), tmem_cols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = ctl->tmem_base;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tmap(&tmX);
-      prefetch_tmap(&tmAt);
-      prefetch_tmap(&tmMt);
-      if (vq) prefetch_tmap(&tmC);
-      for (int i = 0; i < nitems; ++i) {
-        const int s = i % nst, use = i / nst;
-        if (!mbar_wait(smem_u32(&ctl->empty[s]), (use & 1) ^ 1, &ctl->abort, a.timeout_ns)) {
-          give_up(ctl, a.err);
-          break;
-        }
-        const uint32_t st = ring + s * sb;
-        const uint32_t fb = smem_u32(&ctl->full[s]);
-        if (i < nkx) {
-          mbar_arrive_expect_tx(fb, kBlockBytes + r * 128u);
-          tma_load_2d(st, &tmX, i * 64, tile * kTile, fb);
-          for (int h = 0; h < nh; ++h)
-            tma_load_2d(st + kBlockBytes + h * 256u * 128u, &tmAt, i * 64, h * 256, fb);
-          mbar_arrive(fb);
-        } else if (i < nproj) {
-          const int j = i - nkx, sp = j / nkr, kb = j % nkr;
-          mbar_arrive_expect_tx(fb, r * 128u);
-          for (int h = 0; h < nh; ++h)
-            tma_load_2d(st + kBlockBytes + h * 256u * 128u, &tmMt, kb * 64, sp * r + h * nrow,
-                        fb);
-          // the stage is free: let the anchor gather fill its A half; the
-          // gather's arrival is the second one on full[s]
-          gate_publish(smem_u32(&ctl->gate), j + 1);
-        } else {
-          const int j = i - nproj, g = j / a.R, rho = j % a.R;
-          mbar_arrive_expect_tx(fb, a.K * 128u);
-          tma_load_2d(st, &tmC, 0, (rho * a.G + g) * a.K, fb);
-          mbar_arrive(fb);
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idz = idesc_bf16(kTile, nrow);
-      const uint32_t idd = idesc_bf16(kTile, vq ? a.K : 16);
-      for (int i = 0; i < nitems; ++i) {
-        const int s = i % nst, use = i / nst;
-        if (i >= nproj) {
-          if (!mbar_wait(smem_u32(&ctl->uready), (i - nproj) & 1, &ctl->abort, a.timeout_ns)) {
-            give_up(ctl, a.err);
-            break;
-          }
-        }
-        if (!mbar_wait(smem_u32(&ctl->full[s]), use & 1, &ctl->abort, a.timeout_ns)) {
-          give_up(ctl, a.err);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t st = ring + s * sb;
-        if (i < nproj) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = sw128_desc(st + k * 32);
-            for (int h = 0; h < nh; ++h) {
-              const uint64_t bd = sw128_desc(st + kBlockBytes + h * 256u * 128u + k * 32);
-              mma_bf16(tbase + h * 256, ad, bd, idz, (i | k) != 0 ? 1u : 0u);
-            }
-          }
-          mma_commit(smem_u32(&ctl->empty[s]));
-          if (i == nproj - 1) mma_commit(smem_u32(&ctl->zfull));
-        } else {
-          for (int k = 0; k < GD / 16; ++k)
-            mma_bf16(tbase + r, sw128_desc(ubuf + k * 32), sw128_desc(st + k * 32), idd,
-                     k != 0 ? 1u : 0u);
-          mma_commit(smem_u32(&ctl->empty[s]));
-          mma_commit(smem_u32(&ctl->dready));
-        }
-      }
-    }
-  } else {
-    // --------------------------------------------------- gather + epilogue
-    const int tid = threadIdx.x - 64;            // 0..127
-    const int row = (warp & 3) * 32 + lane;      // TMEM lane quadrant = warp % 4
-    load_tids(a.tids, a.N, a.V, tile, tid, ctl->tids, a.err);
-    if (vq) {
-      const int ncn = a.R * a.G * a.K;
-      for (int q = tid; q < ncn; q += kEpiThreads) cn_s[q] = __ldg(a.cnorm + q);
-    }
-    named_bar_sync(kEpiBar, kEpiThreads);
-    bool alive = true;
-    for (int j = 0; j < na && alive; ++j) {
-      const int i = nkx + j, s = i % nst;
-      bool ok = gate_wait(smem_u32(&ctl->gate), j, &ctl->abort, a.timeout_ns);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) {
-        give_up(ctl, a.err);
-        alive = false;
-        break;
-      }
-      gather_block(a.E, r, ctl->tids, j % nkr, ring + s * sb, tid);
-      fence_async_shared();
-      named_bar_sync(kEpiBar, kEpiThreads);
-      if (tid == 0) mbar_arrive(smem_u32(&ctl->full[s]));
-    }
-    if (alive) {
-      bool ok = mbar_wait(smem_u32(&ctl->zfull), 0, &ctl->abort, a.timeout_ns);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) {
-        give_up(ctl, a.err);
-        alive = false;
-      }
-    }
-    if (alive) {
-      tc_fence_after();
-      const uint32_t trow = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-      const int n = tile * kTile + row;
-      const bool store = n < a.N;
-      const bool bad = ctl->tids[row] == -1;
-      if (a.mode == kModeVQ) {
-        if constexpr (GD > 0)
-          vq_epilogue<GD>(a, ctl, trow, trow + r, ubuf, cn_s, row, tid, store, bad, n);
-      } else {
-        for (int c0 = 0; c0 < r; c0 += 32) {
-          float v[32];
-          __syncwarp();
-          tmem_ld32(trow + c0, v);
-          tmem_wait_ld();
-          if (bad) {
-#pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = 0.f;
-          }
-          if (!store) {
-          } else if (a.mode == kModeZ32) {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) +
-                                                    static_cast<size_t>(n) * r + c0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) +
-                                                  static_cast<size_t>(n) * r + c0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]),
-                                  pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                                  pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                                  pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-          }
-        }
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) {
-    __syncwarp();
-    tmem_dealloc(tbase, tmem_cols);
   }
 }
 
@@ -690,39 +342,7 @@ cudaError_t set_smem(KernelT k, uint32_t bytes) {
 
 }  // namespace
 
-uint32_t ctl_bytes() { return static_cast<uint32_t>(sizeof(Ctl)); }
-
-cudaError_t launch_compress_tc(const CUtensorMap& tmX, const CUtensorMap& tmAt,
-                               const CUtensorMap& tmMt, const CUtensorMap& tmC,
-                               const CompressArgs& a, uint32_t smem_bytes, int grid,
-                               cudaStream_t s) {
-  cudaError_t e;
-  switch (a.mode == kModeVQ ? a.gd : 0) {
-    case 0:
-      e = set_smem(k_compress_tc<0>, smem_bytes);
-      if (e != cudaSuccess) return e;
-      k_compress_tc<0><<<grid, kThreads, smem_bytes, s>>>(tmX, tmAt, tmMt, tmC, a);
-      break;
-    case 16:
-      e = set_smem(k_compress_tc<16>, smem_bytes);
-      if (e != cudaSuccess) return e;
-      k_compress_tc<16><<<grid, kThreads, smem_bytes, s>>>(tmX, tmAt, tmMt, tmC, a);
-      break;
-    case 32:
-      e = set_smem(k_compress_tc<32>, smem_bytes);
-      if (e != cudaSuccess) return e;
-      k_compress_tc<32><<<grid, kThreads, smem_bytes, s>>>(tmX, tmAt, tmMt, tmC, a);
-      break;
-    case 64:
-      e = set_smem(k_compress_tc<64>, smem_bytes);
-      if (e != cudaSuccess) return e;
-      k_compress_tc<64><<<grid, kThreads, smem_bytes, s>>>(tmX, tmAt, tmMt, tmC, a);
-      break;
-    default:
-      return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
-}
+uint32_t decompress_ctl_bytes() { return static_cast<uint32_t>(sizeof(Ctl)); }
 
 cudaError_t launch_decompress_tc(const CUtensorMap& tmB, const CUtensorMap& tmZ,
                                  const DecompressArgs& a, uint32_t smem_bytes, int grid,

@@ -15,6 +15,7 @@ using namespace mapl;
 struct mapl_plan_s {
   mapl_config cfg{};
   int device = 0;
+  int num_sms = 0;
   bool vq = false;
   bool tc = false;        // bf16 tensor-core path
   int gd = 0;
@@ -104,13 +105,12 @@ mapl_status validate(const mapl_config* c) {
       return fail(MAPL_ERR_UNSUPPORTED, "bf16 tensor-core path needs r % 64 == 0");
     if (vq) {
       const int64_t gd = c->r / c->G;
-      if (gd != 16 && gd != 32 && gd != 64)
-        return fail(MAPL_ERR_UNSUPPORTED, "bf16 VQ needs group width r/G in {16, 32, 64}");
-      if (c->K % 16 != 0) return fail(MAPL_ERR_UNSUPPORTED, "bf16 VQ needs K % 16 == 0");
-      if (c->r > 256 || c->r + c->K > 512)
-        return fail(MAPL_ERR_UNSUPPORTED, "bf16 VQ needs r <= 256 and r + K <= 512");
-      if (static_cast<int64_t>(c->R) * c->G * c->K * 4 > 32768)
-        return fail(MAPL_ERR_UNSUPPORTED, "bf16 VQ needs R*G*K <= 8192");
+      if (gd != 16 && gd != 32)
+        return fail(MAPL_ERR_UNSUPPORTED, "bf16 VQ needs group width r/G in {16, 32}");
+      if (c->K % 64 != 0)
+        return fail(MAPL_ERR_UNSUPPORTED, "bf16 VQ needs K a multiple of 64");
+      if (c->r > 256)
+        return fail(MAPL_ERR_UNSUPPORTED, "bf16 VQ needs r <= 256");
     }
   }
   return MAPL_OK;
@@ -120,15 +120,14 @@ size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 mapl_status geometry(mapl_plan_s* pl) {
   const mapl_config& c = pl->cfg;
-  const uint32_t ctl = ctl_bytes() + 64;
   const uint32_t slack = 1024;
-  // compress
+  // compress (persistent): ring of stages + residual operand slots + control
   {
     uint32_t st = 16384u + static_cast<uint32_t>(c.r) * 128u;
     if (pl->vq) st = st > static_cast<uint32_t>(c.K) * 128u ? st : static_cast<uint32_t>(c.K) * 128u;
     st = (st + 1023u) & ~1023u;
-    uint32_t extra = ctl + slack;
-    if (pl->vq) extra += 16384u + static_cast<uint32_t>(c.R * c.G * c.K) * 4u;
+    uint32_t extra = compress_ctl_bytes() + 64 + slack;
+    if (pl->vq) extra += static_cast<uint32_t>(c.G < 4 ? c.G : 4) * 16384u;
     int ns = static_cast<int>((kSmemMax - extra) / st);
     if (ns > 8) ns = 8;
     if (ns < 2) return fail(MAPL_ERR_UNSUPPORTED, "compress stages do not fit in shared memory");
@@ -136,6 +135,7 @@ mapl_status geometry(mapl_plan_s* pl) {
     pl->c_stage = st;
     pl->c_smem = ns * st + extra;
   }
+  const uint32_t ctl = decompress_ctl_bytes() + 64;
   // decompress
   {
     const int64_t NC = (c.d % 256 == 0) ? 256 : ((c.d % 128 == 0) ? 128 : 64);
@@ -223,6 +223,8 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   pl->tc = cfg->dtype == MAPL_BF16;
   pl->gd = vq ? static_cast<int>(cfg->r / cfg->G) : 0;
   cudaError_t e = cudaGetDevice(&pl->device);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&pl->num_sms, cudaDevAttrMultiProcessorCount, pl->device);
   if (e != cudaSuccess) {
     delete pl;
     return cuda_fail(e, "cudaGetDevice");
@@ -345,9 +347,11 @@ static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* t
     if (e != cudaSuccess) return cuda_fail(e, "compress launch");
     return MAPL_OK;
   }
-  CUtensorMap tmX;
+  CUtensorMap tmX, tmE;
   if (!make_tmap(&tmX, X, c.d, static_cast<uint64_t>(N), 64, kTile))
     return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (X)");
+  if (!make_tmap(&tmE, E, c.r, static_cast<uint64_t>(c.V), 64, 1))
+    return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (E)");
   CompressArgs a{};
   a.tids = tids;
   a.E = reinterpret_cast<const __nv_bfloat16*>(E);
@@ -368,8 +372,9 @@ static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* t
   a.nstage = pl->c_nstage;
   a.stage_bytes = pl->c_stage;
   a.timeout_ns = pl->timeout_ns;
-  const int grid = static_cast<int>((N + kTile - 1) / kTile);
-  e = launch_compress_tc(tmX, pl->tmAt, pl->tmMt, pl->tmC, a, pl->c_smem, grid, stream);
+  const int ntiles = static_cast<int>((N + kTile - 1) / kTile);
+  const int grid = ntiles < pl->num_sms ? ntiles : pl->num_sms;
+  e = launch_compress_tc(tmX, pl->tmAt, pl->tmMt, pl->tmC, tmE, a, pl->c_smem, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "compress launch");
   return MAPL_OK;
 }

@@ -27,7 +27,8 @@ struct PlanDevice {
   __nv_bfloat16* At = nullptr;      // r x d     A^T (K-major B operand of X A)
   __nv_bfloat16* Mts = nullptr;     // S x r x r -M^T split into S bf16 terms
   __nv_bfloat16* Bcat = nullptr;    // d x 2r    [A | P_recv^T] (K-major B of decompress)
-  __nv_bfloat16* Cpad = nullptr;    // R*G*K x 64 codebook rows, zero padded to 64
+  __nv_bfloat16* Cpad = nullptr;    // R*G*K x 64 codebook rows [c | c | 0] (B operand of
+                                    // the two-term distance MMA)
   __nv_bfloat16* Cb = nullptr;      // R x G x K x gd codebooks (decode lookups)
   // fp32 CUDA-core path
   float* A32 = nullptr;             // d x r
@@ -75,7 +76,8 @@ struct DecompressArgs {
   uint64_t timeout_ns;
 };
 
-uint32_t ctl_bytes();               // control block of the tensor-core kernels
+uint32_t compress_ctl_bytes();      // control block of the compress kernel
+uint32_t decompress_ctl_bytes();    // control block of the decompress kernel
 
 // ---- launchers (return cudaGetLastError() of the launch) -------------------
 cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps, const void* Pr,
@@ -85,8 +87,8 @@ cudaError_t launch_prep_f32(const mapl_config& c, const void* A, const void* Ps,
 
 cudaError_t launch_compress_tc(const CUtensorMap& tmX, const CUtensorMap& tmAt,
                                const CUtensorMap& tmMt, const CUtensorMap& tmC,
-                               const CompressArgs& a, uint32_t smem_bytes, int grid,
-                               cudaStream_t s);
+                               const CUtensorMap& tmE, const CompressArgs& a,
+                               uint32_t smem_bytes, int grid, cudaStream_t s);
 cudaError_t launch_decompress_tc(const CUtensorMap& tmB, const CUtensorMap& tmZ,
                                  const DecompressArgs& a, uint32_t smem_bytes, int grid,
                                  cudaStream_t s);

@@ -6,15 +6,15 @@
 // every group g and round rho the nearest code of the group's residual.
 //
 // One CTA per SM loops over 128-token tiles.  Warp roles (12 warps):
-//   warp 0  lane 0: TMA producer.  A ring of shared-memory stages carries, in
-//                   order, the projection items of tile k (X block + A^T block,
-//                   then -M^T split blocks with their gathered anchor rows)
-//                   and the codebook tiles of tile k-1's VQ.
+//   warp 0  lane 0: TMA producer of the main ring: per tile, X blocks with A^T
+//                   blocks, then -M^T split blocks with the tile's anchor rows
+//                   E[tids] (tile::gather4).
+//   warp 2  lane 0: TMA producer of a 2-stage codebook ring (VQ only).
 //   warp 1        : TMEM allocation; lane 0 issues every tcgen05.mma of the
 //                   CTA: the projection MMAs (into one of two Z accumulators,
 //                   double buffered across tiles) and the VQ distance MMAs,
 //                   interleaved by non-blocking barrier probes.
-//   warps 2, 3    : idle.
+//   warp 3        : idle.
 //   warps 4..11   : epilogue.  Warp w reads TMEM lanes 32*(w%4)..+31 (token
 //                   rows); warps 4..7 scan codes [0, K/2), warps 8..11 codes
 //                   [K/2, K) of the same rows.  Group g's residual is owned by
@@ -41,7 +41,8 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
 constexpr int kMaxStages = 8;
-constexpr int kNSlot = 4;                       // residual operand slots (groups in flight)
+constexpr int kNSlot = 2;                       // residual operand slots (groups in flight)
+constexpr int kCbStages = 2;                    // codebook ring
 constexpr uint32_t kBlockBytes = kTile * 128;   // 128 rows x 64 bf16, 128B swizzled
 constexpr uint32_t kFull = 0xffffffffu;
 
@@ -54,6 +55,8 @@ struct Ctl {
   uint64_t dfull[2];
   uint64_t dempty[2];
   uint64_t pair[4];                 // the two epilogue warps of a TMEM quadrant
+  uint64_t cbfull[kCbStages];       // codebook ring
+  uint64_t cbempty[kCbStages];
   uint32_t tmem_base;
   int abort;
   float xb1[2][2][kTile];           // [item parity][half][row] best of a half
@@ -72,23 +75,9 @@ __device__ __forceinline__ void give_up(Ctl* ctl, int* err) {
   atomicOr(err, kErrTimeout);
 }
 
-// Position of an item in the producer's order (P = projection items of a
-// tile, V = VQ codebook items of a tile).  With two Z accumulators the next
-// tile's projection runs ahead of this tile's VQ: P0, P1, V0, P2, V1, ...,
-// V_{L-1}.  With one accumulator the next projection must wait for this
-// tile's VQ, so its items may not block the ring: P0, V0, P1, V1, ...
-__device__ __forceinline__ int base_P(int it, int nP, int nV, int nzb) {
-  if (nzb == 1) return it * (nP + nV);
-  return it == 0 ? 0 : nP + (it - 1) * (nP + nV);
-}
-__device__ __forceinline__ int base_V(int it, int L, int nP, int nV, int nzb) {
-  if (nzb == 1) return it * (nP + nV) + nP;
-  if (it < L - 1) return base_P(it + 1, nP, nV, nzb) + nP;
-  return L == 1 ? nP : base_P(it, nP, nV, nzb) + nP + nV;
-}
-
 struct Geo {
   int r, nkx, nkr, na, nP, nV, nh, nrow, GD, B, nzb, zstride;
+  bool share;   // anchor rows gathered once per block for all -M splits
 };
 
 __device__ __forceinline__ Geo geometry(const CompressArgs& a, bool vq) {
@@ -105,6 +94,7 @@ __device__ __forceinline__ Geo geometry(const CompressArgs& a, bool vq) {
   g.B = a.G < kNSlot ? a.G : kNSlot;
   g.nzb = vq ? (a.r <= 128 ? 2 : 1) : (2 * a.r <= 512 ? 2 : 1);
   g.zstride = a.r;
+  g.share = a.nstage >= kNumSplit;
   return g;
 }
 
@@ -180,19 +170,19 @@ __device__ __forceinline__ float write_operand(uint32_t slot, int row, const flo
 }
 
 // Best / second best of D~_k = ||c_k||^2 - 2 s_k over KH columns of TMEM
-// (two interleaved trackers; exact ties keep the lowest index).
-__device__ __forceinline__ void scan_half(uint32_t tdist, const float* __restrict__ cn, int KH,
-                                          int koff, float& b1, float& b2, int& k1) {
+// (four interleaved trackers; exact ties keep the lowest index).
+__device__ __forceinline__ void scan_half(uint32_t tdist, const float* cn, int KH, int koff,
+                                          float& b1, float& b2, int& k1) {
   const float inf = __int_as_float(0x7f800000);
-  float a1 = inf, a2 = inf, c1 = inf, c2 = inf;
-  int ka = 0, kc = 0;
+  float t1[4] = {inf, inf, inf, inf}, t2[4] = {inf, inf, inf, inf};
+  int tk[4] = {0, 0, 0, 0};
   for (int c0 = 0; c0 < KH; c0 += 32) {
     float v[32];
     tmem_ld32(tdist + c0, v);
     float cv[32];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(cn + c0) + q);
+      const float4 f = reinterpret_cast<const float4*>(cn + c0)[q];
       cv[4 * q] = f.x;
       cv[4 * q + 1] = f.y;
       cv[4 * q + 2] = f.z;
@@ -200,27 +190,116 @@ __device__ __forceinline__ void scan_half(uint32_t tdist, const float* __restric
     }
     tmem_wait_ld();
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const float D0 = fmaf(-2.f, v[j], cv[j]);
-      const float D1 = fmaf(-2.f, v[j + 1], cv[j + 1]);
-      a2 = fminf(a2, fmaxf(a1, D0));
-      ka = D0 < a1 ? (koff + c0 + j) : ka;
-      a1 = fminf(a1, D0);
-      c2 = fminf(c2, fmaxf(c1, D1));
-      kc = D1 < c1 ? (koff + c0 + j + 1) : kc;
-      c1 = fminf(c1, D1);
+    for (int j = 0; j < 32; j += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float D = fmaf(-2.f, v[j + u], cv[j + u]);
+        t2[u] = fminf(t2[u], fmaxf(t1[u], D));
+        tk[u] = D < t1[u] ? (koff + c0 + j + u) : tk[u];
+        t1[u] = fminf(t1[u], D);
+      }
     }
   }
-  const bool take_c = c1 < a1 || (c1 == a1 && kc < ka);
-  b1 = take_c ? c1 : a1;
-  k1 = take_c ? kc : ka;
-  b2 = fminf(fminf(a2, c2), fmaxf(a1, c1));
+  b1 = t1[0];
+  k1 = tk[0];
+  b2 = t2[0];
+#pragma unroll
+  for (int u = 1; u < 4; ++u) {
+    b2 = fminf(fminf(b2, t2[u]), fmaxf(b1, t1[u]));
+    if (t1[u] < b1 || (t1[u] == b1 && tk[u] < k1)) {
+      b1 = t1[u];
+      k1 = tk[u];
+    }
+  }
+}
+
+// a + b = s + e exactly (Knuth's two-sum)
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// ||u - c||^2 as an unevaluated pair hi + lo (about 48 significant bits):
+// u - c is split exactly, each square is split exactly by an fma, and the
+// running sum keeps its rounding errors.  Enough to order two codes whose
+// distances differ in the 13th significant digit.
+// ||u - c||^2 as an unevaluated pair hi + lo (about 48 significant bits):
+// u - c is split exactly, each square is split exactly by an fma, and the
+// running sum keeps its rounding errors.  Enough to order two codes whose
+// distances differ in the 13th significant digit.  u stays in registers.
+template <int GD>
+__device__ __forceinline__ void exact_dist(const float (&u)[GD], const __nv_bfloat16* cr,
+                                           float& hi, float& lo) {
+  float h = 0.f, l = 0.f;
+#pragma unroll
+  for (int q = 0; q < GD / 8; ++q) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(cr) + q);
+    const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float2 f = __bfloat1622float2(hp[e >> 1]);
+      const float c = (e & 1) ? f.y : f.x;
+      float d, de;
+      two_sum(u[q * 8 + e], -c, d, de);
+      const float p = d * d;
+      float pe = fmaf(d, d, -p);
+      pe = fmaf(2.f * d, de, pe);
+      float s, se;
+      two_sum(h, p, s, se);
+      h = s;
+      l += se + pe;
+    }
+  }
+  float s, e;
+  two_sum(h, l, s, e);
+  hi = s;
+  lo = e;
+}
+
+// Rare path: exact re-scoring of every code whose coarse distance lies within
+// `thr`.  Returns the exact nearest code (lowest index on exact ties).  Per
+// 16-column chunk the in-band codes become a bit mask (registers only) that a
+// compact loop walks in increasing index order.
+template <int GD>
+__device__ __forceinline__ int refine(const float (&u)[GD], uint32_t td0, const float* cn,
+                                      const __nv_bfloat16* book, int KH, float thr, bool need,
+                                      int k_init) {
+  float bh = __int_as_float(0x7f800000), bl = 0.f;
+  int kb = k_init;
+#pragma unroll 1
+  for (int c = 0; c < 2 * KH; c += 16) {
+    const int hh = c >= KH ? 1 : 0;
+    const int c0 = c - hh * KH;
+    float v[16];
+    __syncwarp();
+    tmem_ld16(td0 + hh * 128 + c0, v);
+    tmem_wait_ld();
+    uint32_t mask = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      mask |= (fmaf(-2.f, v[j], cn[c + j]) <= thr ? 1u : 0u) << j;
+    if (!need) mask = 0;
+    while (mask) {
+      const int j = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const int kk = c + j;
+      float eh, el;
+      exact_dist<GD>(u, book + static_cast<size_t>(kk) * GD, eh, el);
+      if (eh < bh || (eh == bh && el < bl)) {
+        bh = eh;
+        bl = el;
+        kb = kk;
+      }
+    }
+  }
+  return kb;
 }
 
 template <int GD>
 __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uint32_t tbase,
-                            uint32_t ubase, int tile, int zb, int q, int h, int lane,
-                            uint32_t& dcnt, uint32_t& pcnt, bool& alive) {
+                            uint32_t ubase, const float* cn_s, int tile, int zb, int q, int h,
+                            int lane, uint32_t& dcnt, uint32_t& pcnt, bool& alive) {
   const int row = q * 32 + lane;
   const int n = tile * kTile + row;
   const bool store = n < a.N;
@@ -266,7 +345,7 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
         const uint32_t tdist = tbase + lanebase + 256 + h * 128;
         float b1, b2;
         int k1;
-        scan_half(tdist, a.cnorm + static_cast<size_t>(book) * K + h * KH, KH, h * KH, b1, b2, k1);
+        scan_half(tdist, cn_s + book * K + h * KH, KH, h * KH, b1, b2, k1);
         ctl->xb1[par][h][row] = b1;
         ctl->xb2[par][h][row] = b2;
         ctl->xk1[par][h][row] = k1;
@@ -296,35 +375,8 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
             tmem_load_group<GD>(tz + g * GD, u);
             have_u = true;
             const float thr = B1 + 2.f * eps;
-            double best = 1e300;
-            int kb = K1;
-            for (int hh = 0; hh < 2; ++hh) {
-              const uint32_t td = tbase + lanebase + 256 + hh * 128;
-              const float* cnh = a.cnorm + static_cast<size_t>(book) * K + hh * KH;
-              for (int c0 = 0; c0 < KH; c0 += 16) {
-                float v[16];
-                __syncwarp();
-                tmem_ld16(td + c0, v);
-                tmem_wait_ld();
-                if (!need) continue;
-                for (int j = 0; j < 16; ++j) {
-                  if (fmaf(-2.f, v[j], __ldg(cnh + c0 + j)) > thr) continue;
-                  const int kk = hh * KH + c0 + j;
-                  const __nv_bfloat16* cr = a.Cb + (static_cast<size_t>(book) * K + kk) * GD;
-                  double e = 0.0;
-#pragma unroll
-                  for (int i = 0; i < GD; ++i) {
-                    const double df = static_cast<double>(u[i]) -
-                                      static_cast<double>(__bfloat162float(cr[i]));
-                    e = fma(df, df, e);
-                  }
-                  if (e < best) {
-                    best = e;
-                    kb = kk;
-                  }
-                }
-              }
-            }
+            const int kb = refine<GD>(u, tbase + lanebase + 256, cn_s + book * K,
+                                      a.Cb + static_cast<size_t>(book) * K * GD, KH, thr, need, K1);
             if (need) K1 = kb;
           }
           // the partner keeps its half until the owner has re-read it
@@ -380,10 +432,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Geo geo = geometry(a, vq);
   const int nst = a.nstage;
   const uint32_t sb = a.stage_bytes;
+  const uint32_t cbsb = vq ? static_cast<uint32_t>(a.K) * 128u : 0u;   // codebook stage
+  // shared memory: main ring | codebook ring | residual slots | ||c||^2 | ids | control
   const uint32_t ring = smem_u32(base);
-  const uint32_t ubase = ring + nst * sb;
-  const uint32_t ubytes = vq ? geo.B * kBlockBytes : 0u;
-  Ctl* ctl = reinterpret_cast<Ctl*>(base + nst * sb + ubytes);
+  uint32_t off = nst * sb;
+  const uint32_t cbring = ring + off;
+  off += kCbStages * cbsb;
+  const uint32_t ubase = ring + off;
+  off += vq ? geo.B * kBlockBytes : 0u;
+  float* cn_s = reinterpret_cast<float*>(base + off);
+  off += vq ? ((static_cast<uint32_t>(a.R * a.G * a.K) * 4u + 15u) & ~15u) : 0u;
+  int* tids_s = reinterpret_cast<int*>(base + off);   // [2][kTile], producer only
+  off += 2 * kTile * 4;
+  Ctl* ctl = reinterpret_cast<Ctl*>(base + off);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ntiles = (a.N + kTile - 1) / kTile;
@@ -408,6 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kNSlot; ++s) mbar_init(smem_u32(&ctl->uready[s]), 4);
     for (int p = 0; p < 4; ++p) mbar_init(smem_u32(&ctl->pair[p]), 2);
+    for (int s = 0; s < kCbStages; ++s) {
+      mbar_init(smem_u32(&ctl->cbfull[s]), 1);
+      mbar_init(smem_u32(&ctl->cbempty[s]), 1);
+    }
     ctl->abort = 0;
     fence_mbar_init();
     fence_async_shared();
@@ -420,94 +485,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t bud = a.timeout_ns;
 
   if (warp == 0 && lane == 0) {
-    // --------------------------------------------------------------- producer
+    // --------------------------------------------- producer of the main ring
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmAt);
     prefetch_tmap(&tmMt);
     prefetch_tmap(&tmE);
-    if (vq) prefetch_tmap(&tmC);
     int i = 0;
     bool ok = true;
-    auto acquire = [&](uint32_t& st, uint32_t& fb) -> bool {
-      const int s = i % nst, use = i / nst;
-      if (!mbar_wait(smem_u32(&ctl->empty[s]), (use & 1) ^ 1, &ctl->abort, bud)) return false;
-      st = ring + s * sb;
-      fb = smem_u32(&ctl->full[s]);
-      return true;
-    };
-    for (int k = 0; k <= L && ok; ++k) {
-      // tile whose VQ codebooks follow this iteration's projection items
-      const int kv = geo.nzb == 1 ? k : k - 1;
-      if (k < L) {
-        const int tile = blockIdx.x + k * gridDim.x;
-        for (int p = 0; p < geo.nP && ok; ++p, ++i) {
-          uint32_t st, fb;
-          if (!(ok = acquire(st, fb))) break;
-          if (p < geo.nkx) {
-            mbar_arrive_expect_tx(fb, kBlockBytes + geo.r * 128u);
-            tma_load_2d(st, &tmX, p * 64, tile * kTile, fb);
-            for (int hh = 0; hh < geo.nh; ++hh)
-              tma_load_2d(st + kBlockBytes + hh * 256u * 128u, &tmAt, p * 64, hh * 256, fb);
-          } else {
-            const int j = p - geo.nkx, sp = j / geo.nkr, kb = j % geo.nkr;
-            mbar_arrive_expect_tx(fb, kBlockBytes + geo.r * 128u);
-            for (int hh = 0; hh < geo.nh; ++hh)
-              tma_load_2d(st + kBlockBytes + hh * 256u * 128u, &tmMt, kb * 64,
-                          sp * geo.r + hh * geo.nrow, fb);
-            // anchor rows E[tids] of the tile (invalid ids and rows past N
-            // read row 0; their outputs are zeroed by the epilogue)
-            for (int q4 = 0; q4 < kTile / 4; ++q4) {
-              int rr[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int n = tile * kTile + q4 * 4 + e;
-                int t = n < a.N ? __ldg(a.tids + n) : 0;
-                rr[e] = (t < 0 || t >= a.V) ? 0 : t;
-              }
-              tma_gather4(st + q4 * 512, &tmE, kb * 64, rr[0], rr[1], rr[2], rr[3], fb);
-            }
-          }
-        }
+    for (int it = 0; it < L && ok; ++it) {
+      const int tile = blockIdx.x + it * gridDim.x;
+      // the tile's anchor row ids (invalid ids and rows past N read row 0;
+      // their outputs are zeroed by the epilogue)
+      int* ts = tids_s + (it & 1) * kTile;
+      for (int q = 0; q < kTile; ++q) {
+        const int n = tile * kTile + q;
+        const int t = n < a.N ? __ldg(a.tids + n) : 0;
+        ts[q] = (t < 0 || t >= a.V) ? 0 : t;
       }
-      if (kv >= 0 && kv < L && vq && ok) {
-        // codebook tiles of tile kv, in the epilogue's item order
-        for (int b0 = 0; b0 < a.G && ok; b0 += geo.B) {
-          const int b1g = b0 + geo.B < a.G ? b0 + geo.B : a.G;
-          for (int rho = 0; rho < a.R && ok; ++rho)
-            for (int g = b0; g < b1g && ok; ++g, ++i) {
-              uint32_t st, fb;
-              if (!(ok = acquire(st, fb))) break;
-              mbar_arrive_expect_tx(fb, a.K * 128u);
-              tma_load_2d(st, &tmC, 0, (rho * a.G + g) * a.K, fb);
-            }
+      for (int p = 0; p < geo.nP; ++p, ++i) {
+        const int s = i % nst, use = i / nst;
+        if (!(ok = mbar_wait(smem_u32(&ctl->empty[s]), (use & 1) ^ 1, &ctl->abort, bud))) break;
+        const uint32_t st = ring + s * sb;
+        const uint32_t fb = smem_u32(&ctl->full[s]);
+        if (p < geo.nkx) {
+          mbar_arrive_expect_tx(fb, kBlockBytes + geo.r * 128u);
+          tma_load_2d(st, &tmX, p * 64, tile * kTile, fb);
+          for (int hh = 0; hh < geo.nh; ++hh)
+            tma_load_2d(st + kBlockBytes + hh * 256u * 128u, &tmAt, p * 64, hh * 256, fb);
+        } else {
+          // anchor item (kb, sp): -M^T split sp, block kb; the anchor rows
+          // E[tids] of block kb come with sp == 0 (or every sp when the ring
+          // is too short to keep that stage while the other splits stream)
+          const int j = p - geo.nkx, kb = j / kNumSplit, sp = j % kNumSplit;
+          const bool gather = sp == 0 || !geo.share;
+          mbar_arrive_expect_tx(fb, (gather ? kBlockBytes : 0u) + geo.r * 128u);
+          for (int hh = 0; hh < geo.nh; ++hh)
+            tma_load_2d(st + kBlockBytes + hh * 256u * 128u, &tmMt, kb * 64,
+                        sp * geo.r + hh * geo.nrow, fb);
+          if (gather)
+            for (int q4 = 0; q4 < kTile / 4; ++q4)
+              tma_gather4(st + q4 * 512, &tmE, kb * 64, ts[4 * q4], ts[4 * q4 + 1],
+                          ts[4 * q4 + 2], ts[4 * q4 + 3], fb);
         }
       }
     }
+    if (!ok) give_up(ctl, a.err);
+  } else if (warp == 2 && lane == 0 && vq) {
+    // ------------------------------------------ producer of the codebook ring
+    prefetch_tmap(&tmC);
+    int c = 0;
+    bool ok = true;
+    for (int it = 0; it < L && ok; ++it)
+      for (int b0 = 0; b0 < a.G && ok; b0 += geo.B) {
+        const int b1g = b0 + geo.B < a.G ? b0 + geo.B : a.G;
+        for (int rho = 0; rho < a.R && ok; ++rho)
+          for (int g = b0; g < b1g && ok; ++g, ++c) {
+            const int s = c % kCbStages, use = c / kCbStages;
+            if (!(ok = mbar_wait(smem_u32(&ctl->cbempty[s]), (use & 1) ^ 1, &ctl->abort, bud)))
+              break;
+            const uint32_t fb = smem_u32(&ctl->cbfull[s]);
+            mbar_arrive_expect_tx(fb, a.K * 128u);
+            tma_load_2d(cbring + s * cbsb, &tmC, 0, (rho * a.G + g) * a.K, fb);
+          }
+      }
     if (!ok) give_up(ctl, a.err);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     // One thread issues every tcgen05 operation of the CTA.  It interleaves
     // two independent streams with non-blocking probes: the VQ distance MMAs
     // of the tile in the epilogue (first, they gate the epilogue) and the
-    // projection MMAs of the next tile.
+    // projection MMAs of the next tile.  Each stream consumes its own ring in
+    // order, so no probe can see a phase two behind.
     const uint32_t idz = idesc_bf16(kTile, geo.nrow);
     const int KH = vq ? a.K / 2 : 16;
     const uint32_t idd = idesc_bf16(kTile, KH);
-    // projection stream
-    int pj_it = 0, pj_p = 0;
+    int pj_it = 0, pj_p = 0, pj_i = 0;
     bool pj_started = false;
-    // VQ stream: item (b0, rho, g) of tile vq_it, half vq_hh
-    int vq_it = 0, vq_b0 = 0, vq_rho = 0, vq_g = 0, vq_hh = 0, vq_i = 0;
-    bool vq_u = false, vq_c = false;
-    uint32_t ucnt[kNSlot] = {0u, 0u, 0u, 0u};
+    int vq_it = 0, vq_b0 = 0, vq_rho = 0, vq_g = 0, vq_hh = 0, vq_c = 0;
+    bool got_u = false, got_c = false;
+    uint32_t ucnt[kNSlot] = {0u, 0u};
     uint32_t e = 0;
-    // Ring uses of each stage observed so far.  The two streams consume
-    // interleaved items of one ring; a probe of use u of a stage is only
-    // meaningful once use u-1 was consumed (a parity probe cannot tell
-    // phase u from phase u-2), so each stream waits for its turn first.
-    int seen[kMaxStages];
-    for (int q = 0; q < kMaxStages; ++q) seen[q] = 0;
-    if (vq && L > 0) vq_i = base_V(0, L, geo.nP, geo.nV, geo.nzb);
     const int vq_end = vq ? L : 0;
     uint64_t last = global_ns();
     uint32_t idle = 0;
@@ -517,18 +574,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (vq_it < vq_end) {
         const int b1g = vq_b0 + geo.B < a.G ? vq_b0 + geo.B : a.G;
         const int slot = vq_g - vq_b0;
-        const int s = vq_i % nst, use = vq_i / nst;
-        if (!vq_u && mbar_test(smem_u32(&ctl->uready[slot]), ucnt[slot] & 1u)) {
-          vq_u = true;
+        const int cs = vq_c % kCbStages, cuse = vq_c / kCbStages;
+        if (!got_u && mbar_test(smem_u32(&ctl->uready[slot]), ucnt[slot] & 1u)) {
+          got_u = true;
           ++ucnt[slot];
         }
-        if (vq_u && !vq_c && seen[s] == use && mbar_test(smem_u32(&ctl->full[s]), use & 1)) {
-          vq_c = true;
-          ++seen[s];
-        }
-        if (vq_u && vq_c && mbar_test(smem_u32(&ctl->dempty[vq_hh]), (e & 1u) ^ 1u)) {
+        if (!got_c && mbar_test(smem_u32(&ctl->cbfull[cs]), cuse & 1)) got_c = true;
+        if (got_u && got_c && mbar_test(smem_u32(&ctl->dempty[vq_hh]), (e & 1u) ^ 1u)) {
           tc_fence_after();
-          const uint32_t st = ring + s * sb;
+          const uint32_t st = cbring + cs * cbsb;
           const uint32_t us = ubase + slot * kBlockBytes;
 #pragma unroll
           for (int k = 0; k < 2 * (GD > 0 ? GD : 16) / 16; ++k)
@@ -539,11 +593,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (vq_hh == 0) {
             vq_hh = 1;
           } else {
-            mma_commit(smem_u32(&ctl->empty[s]));
+            mma_commit(smem_u32(&ctl->cbempty[cs]));
             vq_hh = 0;
-            vq_u = vq_c = false;
+            got_u = got_c = false;
             ++e;
-            ++vq_i;
+            ++vq_c;
             if (++vq_g == b1g) {
               vq_g = vq_b0;
               if (++vq_rho == a.R) {
@@ -552,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 vq_g = vq_b0;
                 if (vq_b0 >= a.G) {
                   vq_b0 = vq_g = 0;
-                  if (++vq_it < L) vq_i = base_V(vq_it, L, geo.nP, geo.nV, geo.nzb);
+                  ++vq_it;
                 }
               }
             }
@@ -567,23 +621,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
         }
         if (pj_started) {
-          const int i = base_P(pj_it, geo.nP, geo.nV, geo.nzb) + pj_p;
-          const int s = i % nst, use = i / nst;
-          if (seen[s] == use && mbar_test(smem_u32(&ctl->full[s]), use & 1)) {
-            ++seen[s];
+          const int s = pj_i % nst, use = pj_i / nst;
+          if (mbar_test(smem_u32(&ctl->full[s]), use & 1)) {
             tc_fence_after();
             const uint32_t st = ring + s * sb;
             const uint32_t dz = tbase + zb * geo.zstride;
+            // A operand: this stage, or for a shared anchor split the stage
+            // of split 0 of the same block (still held)
+            int sp = 0;
+            if (pj_p >= geo.nkx) sp = (pj_p - geo.nkx) % kNumSplit;
+            const uint32_t sa = (geo.share && sp > 0) ? ring + ((pj_i - sp) % nst) * sb : st;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = sw128_desc(st + k * 32);
+              const uint64_t ad = sw128_desc(sa + k * 32);
               for (int hh = 0; hh < geo.nh; ++hh)
                 mma_bf16(dz + hh * 256, ad,
                          sw128_desc(st + kBlockBytes + hh * 256u * 128u + k * 32), idz,
                          (pj_p | k) != 0 ? 1u : 0u);
             }
-            mma_commit(smem_u32(&ctl->empty[s]));
+            if (pj_p < geo.nkx || !geo.share) {
+              mma_commit(smem_u32(&ctl->empty[s]));
+            } else if (sp == kNumSplit - 1) {
+              // release the block's stages together (split 0 held the rows)
+              for (int x = kNumSplit - 1; x >= 0; --x)
+                mma_commit(smem_u32(&ctl->empty[(pj_i - x) % nst]));
+            }
             progressed = true;
+            ++pj_i;
             if (++pj_p == geo.nP) {
               mma_commit(smem_u32(&ctl->zfull[zb]));
               pj_p = 0;
@@ -607,6 +671,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kEpiWarp0) {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3, h = (warp - kEpiWarp0) >> 2;
+    if (vq) {
+      const int ncn = a.R * a.G * a.K;
+      for (int x = threadIdx.x - kEpiWarp0 * 32; x < ncn; x += 8 * 32) cn_s[x] = __ldg(a.cnorm + x);
+      named_bar_sync(1, 8 * 32);
+    }
     uint32_t dcnt = 0, pcnt = 0;
     bool alive = true;
     for (int it = 0; it < L && alive; ++it) {
@@ -620,7 +689,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (vq) {
         if constexpr (GD > 0)
-          epilogue_vq<GD>(a, geo, ctl, tbase, ubase, tile, zb, q, h, lane, dcnt, pcnt, alive);
+          epilogue_vq<GD>(a, geo, ctl, tbase, ubase, cn_s, tile, zb, q, h, lane, dcnt, pcnt,
+                          alive);
+        const int n = tile * kTile + q * 32 + lane;
+        if (alive && h == 0 && n < a.N) {
+          const int t = a.tids[n];
+          if (t < 0 || t >= a.V) atomicOr(a.err, kErrBadToken);
+        }
       } else {
         const int row = q * 32 + lane;
         const int n = tile * kTile + row;
@@ -629,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (store) {
           const int t = a.tids[n];
           bad = t < 0 || t >= a.V;
-          if (bad) atomicOr(a.err, kErrBadToken);
+          if (bad && h == 0) atomicOr(a.err, kErrBadToken);
         }
         const uint32_t tz = tbase + (static_cast<uint32_t>(q * 32) << 16) + zb * geo.zstride;
         const int half = geo.r / 2;
@@ -659,14 +734,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
                                   pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
           }
-        }
-      }
-      if (vq && alive) {
-        // flag invalid token ids once per row (owner-independent)
-        const int n = tile * kTile + q * 32 + lane;
-        if (h == 0 && n < a.N) {
-          const int t = a.tids[n];
-          if (t < 0 || t >= a.V) atomicOr(a.err, kErrBadToken);
         }
       }
       if (!alive) break;

@@ -124,10 +124,13 @@ mapl_status geometry(mapl_plan_s* pl) {
   // compress (persistent): ring of stages + residual operand slots + control
   {
     uint32_t st = 16384u + static_cast<uint32_t>(c.r) * 128u;
-    if (pl->vq) st = st > static_cast<uint32_t>(c.K) * 128u ? st : static_cast<uint32_t>(c.K) * 128u;
     st = (st + 1023u) & ~1023u;
-    uint32_t extra = compress_ctl_bytes() + 64 + slack;
-    if (pl->vq) extra += static_cast<uint32_t>(c.G < 4 ? c.G : 4) * 16384u;
+    uint32_t extra = compress_ctl_bytes() + 64 + slack + 2 * 128 * 4;   // + tile ids
+    if (pl->vq) {
+      extra += 2u * static_cast<uint32_t>(c.K) * 128u;                    // codebook ring
+      extra += static_cast<uint32_t>(c.G < 2 ? c.G : 2) * 16384u;         // residual slots
+      extra += (static_cast<uint32_t>(c.R * c.G * c.K) * 4u + 15u) & ~15u; // ||c||^2
+    }
     int ns = static_cast<int>((kSmemMax - extra) / st);
     if (ns > 8) ns = 8;
     if (ns < 2) return fail(MAPL_ERR_UNSUPPORTED, "compress stages do not fit in shared memory");

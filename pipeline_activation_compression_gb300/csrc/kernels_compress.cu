@@ -223,10 +223,6 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
 // ||u - c||^2 as an unevaluated pair hi + lo (about 48 significant bits):
 // u - c is split exactly, each square is split exactly by an fma, and the
 // running sum keeps its rounding errors.  Enough to order two codes whose
-// distances differ in the 13th significant digit.
-// ||u - c||^2 as an unevaluated pair hi + lo (about 48 significant bits):
-// u - c is split exactly, each square is split exactly by an fma, and the
-// running sum keeps its rounding errors.  Enough to order two codes whose
 // distances differ in the 13th significant digit.  u stays in registers.
 template <int GD>
 __device__ __forceinline__ void exact_dist(const float (&u)[GD], const __nv_bfloat16* cr,
@@ -273,7 +269,7 @@ __device__ __forceinline__ int refine(const float (&u)[GD], uint32_t td0, const 
     const int c0 = c - hh * KH;
     float v[16];
     __syncwarp();
-    tmem_ld16(td0 + hh * 128 + c0, v);
+    tmem_ld16(td0 + hh * KH + c0, v);
     tmem_wait_ld();
     uint32_t mask = 0;
 #pragma unroll
@@ -342,7 +338,7 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
           break;
         }
         tc_fence_after();
-        const uint32_t tdist = tbase + lanebase + 256 + h * 128;
+        const uint32_t tdist = tbase + lanebase + 256 + h * KH;
         float b1, b2;
         int k1;
         scan_half(tdist, cn_s + book * K + h * KH, KH, h * KH, b1, b2, k1);
@@ -484,52 +480,83 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = ctl->tmem_base;
   const uint64_t bud = a.timeout_ns;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // --------------------------------------------- producer of the main ring
-    prefetch_tmap(&tmX);
-    prefetch_tmap(&tmAt);
-    prefetch_tmap(&tmMt);
-    prefetch_tmap(&tmE);
-    int i = 0;
+    // Lane 0 issues the TMA loads.  The whole warp stages each tile's anchor
+    // row ids in shared memory, one tile ahead (invalid ids and rows past N
+    // read row 0; their outputs are zeroed by the epilogue).
+    if (lane == 0) {
+      prefetch_tmap(&tmX);
+      prefetch_tmap(&tmAt);
+      prefetch_tmap(&tmMt);
+      prefetch_tmap(&tmE);
+    }
+    constexpr int kIdsPerLane = kTile / 32;
+    auto fetch_ids = [&](int tile, int (&v)[kIdsPerLane]) {
+#pragma unroll
+      for (int j = 0; j < kIdsPerLane; ++j) {
+        const int n = tile * kTile + lane + 32 * j;
+        const int t = n < a.N ? __ldg(a.tids + n) : 0;
+        v[j] = (t < 0 || t >= a.V) ? 0 : t;
+      }
+    };
+    auto store_ids = [&](int buf, const int (&v)[kIdsPerLane]) {
+#pragma unroll
+      for (int j = 0; j < kIdsPerLane; ++j) tids_s[buf * kTile + lane + 32 * j] = v[j];
+    };
+    if (L > 0) {
+      int v[kIdsPerLane];
+      fetch_ids(blockIdx.x, v);
+      store_ids(0, v);
+    }
+    __syncwarp();
+    int s = 0;
+    uint32_t ph = 0;   // phase parity of stage s
     bool ok = true;
     for (int it = 0; it < L && ok; ++it) {
       const int tile = blockIdx.x + it * gridDim.x;
-      // the tile's anchor row ids (invalid ids and rows past N read row 0;
-      // their outputs are zeroed by the epilogue)
-      int* ts = tids_s + (it & 1) * kTile;
-      for (int q = 0; q < kTile; ++q) {
-        const int n = tile * kTile + q;
-        const int t = n < a.N ? __ldg(a.tids + n) : 0;
-        ts[q] = (t < 0 || t >= a.V) ? 0 : t;
-      }
-      for (int p = 0; p < geo.nP; ++p, ++i) {
-        const int s = i % nst, use = i / nst;
-        if (!(ok = mbar_wait(smem_u32(&ctl->empty[s]), (use & 1) ^ 1, &ctl->abort, bud))) break;
-        const uint32_t st = ring + s * sb;
-        const uint32_t fb = smem_u32(&ctl->full[s]);
-        if (p < geo.nkx) {
-          mbar_arrive_expect_tx(fb, kBlockBytes + geo.r * 128u);
-          tma_load_2d(st, &tmX, p * 64, tile * kTile, fb);
-          for (int hh = 0; hh < geo.nh; ++hh)
-            tma_load_2d(st + kBlockBytes + hh * 256u * 128u, &tmAt, p * 64, hh * 256, fb);
-        } else {
-          // anchor item (kb, sp): -M^T split sp, block kb; the anchor rows
-          // E[tids] of block kb come with sp == 0 (or every sp when the ring
-          // is too short to keep that stage while the other splits stream)
-          const int j = p - geo.nkx, kb = j / kNumSplit, sp = j % kNumSplit;
-          const bool gather = sp == 0 || !geo.share;
-          mbar_arrive_expect_tx(fb, (gather ? kBlockBytes : 0u) + geo.r * 128u);
-          for (int hh = 0; hh < geo.nh; ++hh)
-            tma_load_2d(st + kBlockBytes + hh * 256u * 128u, &tmMt, kb * 64,
-                        sp * geo.r + hh * geo.nrow, fb);
-          if (gather)
-            for (int q4 = 0; q4 < kTile / 4; ++q4)
-              tma_gather4(st + q4 * 512, &tmE, kb * 64, ts[4 * q4], ts[4 * q4 + 1],
-                          ts[4 * q4 + 2], ts[4 * q4 + 3], fb);
+      int nv[kIdsPerLane];
+      if (it + 1 < L) fetch_ids(tile + gridDim.x, nv);
+      if (lane == 0) {
+        const int* ts = tids_s + (it & 1) * kTile;
+        for (int p = 0; p < geo.nP; ++p) {
+          if (!(ok = mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, &ctl->abort, bud))) break;
+          const uint32_t st = ring + s * sb;
+          const uint32_t fb = smem_u32(&ctl->full[s]);
+          if (p < geo.nkx) {
+            mbar_arrive_expect_tx(fb, kBlockBytes + geo.r * 128u);
+            tma_load_2d(st, &tmX, p * 64, tile * kTile, fb);
+            for (int hh = 0; hh < geo.nh; ++hh)
+              tma_load_2d(st + kBlockBytes + hh * 256u * 128u, &tmAt, p * 64, hh * 256, fb);
+          } else {
+            // anchor item (kb, sp): -M^T split sp, block kb; the anchor rows
+            // E[tids] of block kb come with sp == 0 (or every sp when the
+            // ring is too short to keep that stage while the other splits
+            // stream)
+            const int j = p - geo.nkx, kb = j / kNumSplit, sp = j - kb * kNumSplit;
+            const bool gather = sp == 0 || !geo.share;
+            mbar_arrive_expect_tx(fb, (gather ? kBlockBytes : 0u) + geo.r * 128u);
+            for (int hh = 0; hh < geo.nh; ++hh)
+              tma_load_2d(st + kBlockBytes + hh * 256u * 128u, &tmMt, kb * 64,
+                          sp * geo.r + hh * geo.nrow, fb);
+            if (gather)
+              for (int q4 = 0; q4 < kTile / 4; ++q4)
+                tma_gather4(st + q4 * 512, &tmE, kb * 64, ts[4 * q4], ts[4 * q4 + 1],
+                            ts[4 * q4 + 2], ts[4 * q4 + 3], fb);
+          }
+          if (++s == nst) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
       }
+      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+      // the gathers that read this buffer two tiles ago were issued already
+      // (their row ids travel with the instruction)
+      if (it + 1 < L) store_ids((it + 1) & 1, nv);
+      __syncwarp();
     }
-    if (!ok) give_up(ctl, a.err);
+    if (!ok && lane == 0) give_up(ctl, a.err);
   } else if (warp == 2 && lane == 0 && vq) {
     // ------------------------------------------ producer of the codebook ring
     prefetch_tmap(&tmC);
@@ -555,16 +582,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // two independent streams with non-blocking probes: the VQ distance MMAs
     // of the tile in the epilogue (first, they gate the epilogue) and the
     // projection MMAs of the next tile.  Each stream consumes its own ring in
-    // order, so no probe can see a phase two behind.
+    // order, so no probe can see a phase two behind.  The loop is kept lean
+    // (no divisions, descriptors advanced by offsets): this thread shares its
+    // scheduler with two busy epilogue warps.
     const uint32_t idz = idesc_bf16(kTile, geo.nrow);
-    const int KH = vq ? a.K / 2 : 16;
-    const uint32_t idd = idesc_bf16(kTile, KH);
-    int pj_it = 0, pj_p = 0, pj_i = 0;
+    const uint32_t idd = idesc_bf16(kTile, vq ? a.K : 16);
+    constexpr int kStepsVQ = 2 * (GD > 0 ? GD : 16) / 16;
+    const uint64_t ring_d = sw128_desc(ring);
+    const uint64_t ub_d = sw128_desc(ubase);
+    const uint64_t cb_d = sw128_desc(cbring);
+    int pj_it = 0, pj_p = 0, pj_s = 0, pj_sp = 0, blk0 = 0, blk1 = 0;
+    uint32_t pj_ph = 0;
     bool pj_started = false;
-    int vq_it = 0, vq_b0 = 0, vq_rho = 0, vq_g = 0, vq_hh = 0, vq_c = 0;
+    int vq_it = 0, vq_b0 = 0, vq_rho = 0, vq_g = 0, vq_cs = 0;
+    uint32_t vq_cph = 0, e = 0;
+    uint32_t ucnt0 = 0, ucnt1 = 0;
     bool got_u = false, got_c = false;
-    uint32_t ucnt[kNSlot] = {0u, 0u};
-    uint32_t e = 0;
     const int vq_end = vq ? L : 0;
     uint64_t last = global_ns();
     uint32_t idle = 0;
@@ -572,88 +605,91 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && (pj_it < L || vq_it < vq_end)) {
       bool progressed = false;
       if (vq_it < vq_end) {
-        const int b1g = vq_b0 + geo.B < a.G ? vq_b0 + geo.B : a.G;
         const int slot = vq_g - vq_b0;
-        const int cs = vq_c % kCbStages, cuse = vq_c / kCbStages;
-        if (!got_u && mbar_test(smem_u32(&ctl->uready[slot]), ucnt[slot] & 1u)) {
-          got_u = true;
-          ++ucnt[slot];
-        }
-        if (!got_c && mbar_test(smem_u32(&ctl->cbfull[cs]), cuse & 1)) got_c = true;
-        if (got_u && got_c && mbar_test(smem_u32(&ctl->dempty[vq_hh]), (e & 1u) ^ 1u)) {
+        if (!got_u)
+          got_u = mbar_test(smem_u32(&ctl->uready[slot]), (slot == 0 ? ucnt0 : ucnt1) & 1u);
+        if (!got_c) got_c = mbar_test(smem_u32(&ctl->cbfull[vq_cs]), vq_cph);
+        if (got_u && got_c && mbar_test(smem_u32(&ctl->dempty[0]), (e & 1u) ^ 1u) &&
+            mbar_test(smem_u32(&ctl->dempty[1]), (e & 1u) ^ 1u)) {
+          // one MMA over all K codes: both halves of the distance buffer
           tc_fence_after();
-          const uint32_t st = cbring + cs * cbsb;
-          const uint32_t us = ubase + slot * kBlockBytes;
+          const uint64_t ad = ub_d + ((static_cast<uint32_t>(slot) * kBlockBytes) >> 4);
+          const uint64_t bd = cb_d + ((static_cast<uint32_t>(vq_cs) * cbsb) >> 4);
 #pragma unroll
-          for (int k = 0; k < 2 * (GD > 0 ? GD : 16) / 16; ++k)
-            mma_bf16(tbase + 256 + vq_hh * 128, sw128_desc(us + k * 32),
-                     sw128_desc(st + vq_hh * KH * 128u + k * 32), idd, k != 0 ? 1u : 0u);
-          mma_commit(smem_u32(&ctl->dfull[vq_hh]));
+          for (int k = 0; k < kStepsVQ; ++k)
+            mma_bf16(tbase + 256, ad + 2 * k, bd + 2 * k, idd, k != 0 ? 1u : 0u);
+          mma_commit(smem_u32(&ctl->dfull[0]));
+          mma_commit(smem_u32(&ctl->dfull[1]));
+          mma_commit(smem_u32(&ctl->cbempty[vq_cs]));
           progressed = true;
-          if (vq_hh == 0) {
-            vq_hh = 1;
-          } else {
-            mma_commit(smem_u32(&ctl->cbempty[cs]));
-            vq_hh = 0;
-            got_u = got_c = false;
-            ++e;
-            ++vq_c;
-            if (++vq_g == b1g) {
+          if (slot == 0) ++ucnt0; else ++ucnt1;
+          got_u = got_c = false;
+          ++e;
+          if (++vq_cs == kCbStages) {
+            vq_cs = 0;
+            vq_cph ^= 1u;
+          }
+          const int b1g = vq_b0 + geo.B < a.G ? vq_b0 + geo.B : a.G;
+          if (++vq_g == b1g) {
+            vq_g = vq_b0;
+            if (++vq_rho == a.R) {
+              vq_rho = 0;
+              vq_b0 += geo.B;
               vq_g = vq_b0;
-              if (++vq_rho == a.R) {
-                vq_rho = 0;
-                vq_b0 += geo.B;
-                vq_g = vq_b0;
-                if (vq_b0 >= a.G) {
-                  vq_b0 = vq_g = 0;
-                  ++vq_it;
-                }
+              if (vq_b0 >= a.G) {
+                vq_b0 = vq_g = 0;
+                ++vq_it;
               }
             }
           }
         }
       }
-      if (pj_it < L) {
+      // projection MMAs only while the VQ stream waits: the tensor pipe runs
+      // in order, so a projection item queued ahead of a distance MMA would
+      // delay the epilogue, which is the critical path
+      if (pj_it < L && !progressed) {
         const int zb = geo.nzb == 2 ? (pj_it & 1) : 0;
         const int zuse = geo.nzb == 2 ? (pj_it >> 1) : pj_it;
         if (!pj_started && mbar_test(smem_u32(&ctl->zempty[zb]), (zuse & 1) ^ 1)) {
           pj_started = true;
           tc_fence_after();
         }
-        if (pj_started) {
-          const int s = pj_i % nst, use = pj_i / nst;
-          if (mbar_test(smem_u32(&ctl->full[s]), use & 1)) {
-            tc_fence_after();
-            const uint32_t st = ring + s * sb;
-            const uint32_t dz = tbase + zb * geo.zstride;
-            // A operand: this stage, or for a shared anchor split the stage
-            // of split 0 of the same block (still held)
-            int sp = 0;
-            if (pj_p >= geo.nkx) sp = (pj_p - geo.nkx) % kNumSplit;
-            const uint32_t sa = (geo.share && sp > 0) ? ring + ((pj_i - sp) % nst) * sb : st;
+        if (pj_started && mbar_test(smem_u32(&ctl->full[pj_s]), pj_ph)) {
+          tc_fence_after();
+          const uint32_t dz = tbase + zb * geo.zstride;
+          const bool anchor = pj_p >= geo.nkx;
+          if (anchor && pj_sp == 0) blk0 = pj_s;
+          if (anchor && pj_sp == 1) blk1 = pj_s;
+          // A operand: this stage, or for a shared anchor split the stage of
+          // split 0 of the same block (still held)
+          const int sa_s = (anchor && geo.share && pj_sp > 0) ? blk0 : pj_s;
+          const uint64_t ad = ring_d + ((static_cast<uint32_t>(sa_s) * sb) >> 4);
+          const uint64_t bd = ring_d + ((static_cast<uint32_t>(pj_s) * sb + kBlockBytes) >> 4);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = sw128_desc(sa + k * 32);
-              for (int hh = 0; hh < geo.nh; ++hh)
-                mma_bf16(dz + hh * 256, ad,
-                         sw128_desc(st + kBlockBytes + hh * 256u * 128u + k * 32), idz,
-                         (pj_p | k) != 0 ? 1u : 0u);
-            }
-            if (pj_p < geo.nkx || !geo.share) {
-              mma_commit(smem_u32(&ctl->empty[s]));
-            } else if (sp == kNumSplit - 1) {
-              // release the block's stages together (split 0 held the rows)
-              for (int x = kNumSplit - 1; x >= 0; --x)
-                mma_commit(smem_u32(&ctl->empty[(pj_i - x) % nst]));
-            }
-            progressed = true;
-            ++pj_i;
-            if (++pj_p == geo.nP) {
-              mma_commit(smem_u32(&ctl->zfull[zb]));
-              pj_p = 0;
-              pj_started = false;
-              ++pj_it;
-            }
+          for (int k = 0; k < 4; ++k)
+            for (int hh = 0; hh < geo.nh; ++hh)
+              mma_bf16(dz + hh * 256, ad + 2 * k, bd + hh * ((256u * 128u) >> 4) + 2 * k, idz,
+                       (pj_p | k) != 0 ? 1u : 0u);
+          if (!anchor || !geo.share) {
+            mma_commit(smem_u32(&ctl->empty[pj_s]));
+          } else if (pj_sp == kNumSplit - 1) {
+            // release the block's stages together (split 0 held the rows)
+            mma_commit(smem_u32(&ctl->empty[blk0]));
+            if (kNumSplit > 2) mma_commit(smem_u32(&ctl->empty[blk1]));
+            mma_commit(smem_u32(&ctl->empty[pj_s]));
+          }
+          progressed = true;
+          if (++pj_s == nst) {
+            pj_s = 0;
+            pj_ph ^= 1u;
+          }
+          if (anchor && ++pj_sp == kNumSplit) pj_sp = 0;
+          if (++pj_p == geo.nP) {
+            mma_commit(smem_u32(&ctl->zfull[zb]));
+            pj_p = 0;
+            pj_sp = 0;
+            pj_started = false;
+            ++pj_it;
           }
         }
       }

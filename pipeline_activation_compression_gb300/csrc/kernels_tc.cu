@@ -42,7 +42,8 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return p + ((1024u - (a & 1023u)) & 1023u);
 }
 
-__device__ __forceinline__ void give_up(Ctl* ctl, int* err) {
+template <typename C>
+__device__ __forceinline__ void give_up(C* ctl, int* err) {
   ctl->abort = 1;
   atomicOr(err, kErrTimeout);
 }
@@ -131,7 +132,7 @@ __device__ __forceinline__ void decode_rows(const DecompressArgs& a, const int32
 }
 
 template <int GD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     k_decompress_tc(const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmZ, const DecompressArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x;
   const int r = a.r, d = a.d;
-  const int NC = (d % 256 == 0) ? 256 : ((d % 128 == 0) ? 128 : 64);   // output chunk
+  const int NC = a.nc;                            // output chunk
   const int nchunk = d / NC;
   const int nzb = r / 64;                          // K-blocks holding Z_hat
   const int nka = 2 * nzb;                         // K-blocks of [Z_hat | E']
@@ -334,6 +335,347 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ======================================================================
+// decompress, persistent form (resident A operand, r <= 256)
+// ======================================================================
+// One CTA per SM walks the tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+// Warp roles (320 threads):
+//   warp 0 lane 0 : TMA producer of the [A^T | P'^T] ring (NC x 64 blocks)
+//   warp 1        : TMEM allocation; lane 0 issues every tcgen05.mma
+//   warps 2..5    : builders of the A operand [Z_hat | E'[tids]] of the next
+//                   tile (E' rows by TMA gather4, Z_hat by TMA or VQ decode)
+//   warps 6..9    : drain of the two TMEM accumulators (TMEM lane = row)
+// The A operand is double buffered when two copies fit in shared memory, so
+// the next tile is built while the current one runs on the tensor cores.
+constexpr int kPtThreads = 320;
+constexpr int kPtBuild0 = 2;      // first builder warp
+constexpr int kPtDrain0 = 6;      // first drain warp
+constexpr int kPtBuildBar = 2;    // named barrier of the builder warps
+constexpr uint32_t kPtStagingBytes = 4 * 2 * 4096;   // per drain warp: 2 x (32 rows x 128 B)
+
+struct CtlPt {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t afull[2];      // A operand built (TMA bytes + one builder arrival)
+  uint64_t aempty[2];     // MMAs of the tile that used the buffer are complete
+  uint64_t tfull[2];      // accumulator holds a finished chunk
+  uint64_t tempty[2];     // accumulator drained (one arrival per drain warp)
+  uint64_t done;          // every MMA of the CTA has completed
+  uint32_t tmem_base;
+  int abort;
+  int32_t ids[2][kTile];  // gather row ids of the tile in A buffer b
+};
+
+template <int GD>
+__device__ __forceinline__ void decode_row_pt(const DecompressArgs& a, uint32_t abuf, int row,
+                                              int n, bool live) {
+  // Z_hat[n, g-block] = sum_rho C[rho][g][idx[n][rho][g]]  (fp32, then bf16);
+  // the loads of up to four rounds are issued before they are summed
+  const int G = a.G, R = a.R, K = a.K;
+  const uint8_t* ip = a.idx + static_cast<size_t>(n) * R * G;
+  for (int g = 0; g < G; ++g) {
+    float acc[GD];
+#pragma unroll
+    for (int i = 0; i < GD; ++i) acc[i] = 0.f;
+    if (live) {
+      for (int r0 = 0; r0 < R; r0 += 4) {
+        uint4 w[4][GD / 8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (r0 + j < R) {
+            int k = ip[(r0 + j) * G + g];
+            if (k >= K) {   // not a valid code: flag it, never read past the book
+              atomicOr(a.err, kErrBadIndex);
+              k = K - 1;
+            }
+            const uint4* cr = reinterpret_cast<const uint4*>(
+                a.Cb + (static_cast<size_t>((r0 + j) * G + g) * K + k) * GD);
+#pragma unroll
+            for (int c = 0; c < GD / 8; ++c) w[j][c] = __ldg(cr + c);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (r0 + j < R) {
+#pragma unroll
+            for (int c = 0; c < GD / 8; ++c) {
+              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w[j][c]);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(h[e]);
+                acc[c * 8 + 2 * e] += f.x;
+                acc[c * 8 + 2 * e + 1] += f.y;
+              }
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < GD / 8; ++c) {
+      const int col = g * GD + c * 8;
+      uint4 v;
+      v.x = pack_bf16x2(acc[c * 8 + 0], acc[c * 8 + 1]);
+      v.y = pack_bf16x2(acc[c * 8 + 2], acc[c * 8 + 3]);
+      v.z = pack_bf16x2(acc[c * 8 + 4], acc[c * 8 + 5]);
+      v.w = pack_bf16x2(acc[c * 8 + 6], acc[c * 8 + 7]);
+      st_shared_v4(abuf + (col >> 6) * kBlockBytes + sw128_off(row, (col & 63) >> 3), v);
+    }
+  }
+}
+
+template <int GD>
+__global__ void __launch_bounds__(kPtThreads, 1)
+    k_decompress_pt(const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmZ,
+                    const __grid_constant__ CUtensorMap tmE,
+                    const __grid_constant__ CUtensorMap tmXh, const DecompressArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  const int nst = a.nstage, nab = a.nab;
+  const uint32_t sb = a.stage_bytes;
+  const uint32_t abuf0 = smem_u32(base);                     // A buffers
+  const uint32_t ring = abuf0 + nab * a.a_bytes;
+  const uint32_t stage0 = ring + nst * sb;                   // drain staging
+  CtlPt* ctl = reinterpret_cast<CtlPt*>(base + nab * a.a_bytes + nst * sb + kPtStagingBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NC = a.nc;
+  const int nchunk = a.d / NC;
+  const int nzb = a.r / 64;          // K-blocks of Z_hat (and of E')
+  const int nka = 2 * nzb;           // K-blocks of [Z_hat | E']
+  const int ntiles = (a.N + kTile - 1) / kTile;
+  const int L = blockIdx.x < ntiles ? (ntiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+  const uint32_t tmem_cols = 2u * NC < 32u ? 32u : 2u * NC;
+  const uint64_t bud = a.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nst; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctl->afull[b]), 2);
+      mbar_init(smem_u32(&ctl->aempty[b]), 1);
+      mbar_init(smem_u32(&ctl->tfull[b]), 1);
+      mbar_init(smem_u32(&ctl->tempty[b]), 4);
+    }
+    mbar_init(smem_u32(&ctl->done), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    fence_async_shared();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(&ctl->tmem_base), tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------- B operand producer
+      prefetch_tmap(&tmB);
+      int s = 0, issued = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int it = 0; it < L && ok; ++it)
+        for (int c = 0; c < nchunk && ok; ++c)
+          for (int kb = 0; kb < nka; ++kb) {
+            if (!(ok = mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, &ctl->abort, bud))) break;
+            const uint32_t fb = smem_u32(&ctl->full[s]);
+            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(NC) * 128u);
+            tma_load_2d(ring + s * sb, &tmB, kb * 64, c * NC, fb);
+            ++issued;
+            if (++s == nst) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+      if (!ok) {
+        give_up(ctl, a.err);
+        // let the copies in flight land before the CTA's memory goes away
+        for (int x = 0; x < nst && x < issued; ++x) {
+          const int i = issued - 1 - x, ss = i % nst;
+          mbar_wait(smem_u32(&ctl->full[ss]), static_cast<uint32_t>(i / nst) & 1u, &ctl->abort,
+                    bud / 16);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint32_t idc = idesc_bf16(kTile, NC);
+      const uint64_t a_d = sw128_desc(abuf0);
+      const uint64_t r_d = sw128_desc(ring);
+      int s = 0, cc = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int it = 0; it < L && ok; ++it) {
+        const int ab = nab == 2 ? (it & 1) : 0;
+        const int ause = nab == 2 ? (it >> 1) : it;
+        if (!(ok = mbar_wait(smem_u32(&ctl->afull[ab]), ause & 1, &ctl->abort, bud))) break;
+        tc_fence_after();
+        const uint64_t ad = a_d + ((static_cast<uint32_t>(ab) * a.a_bytes) >> 4);
+        for (int c = 0; c < nchunk && ok; ++c, ++cc) {
+          const int acc = cc & 1;
+          if (!(ok = mbar_wait(smem_u32(&ctl->tempty[acc]), ((cc >> 1) & 1) ^ 1, &ctl->abort,
+                               bud)))
+            break;
+          tc_fence_after();
+          for (int kb = 0; kb < nka; ++kb) {
+            if (!(ok = mbar_wait(smem_u32(&ctl->full[s]), ph, &ctl->abort, bud))) break;
+            tc_fence_after();
+            const uint64_t bd = r_d + ((static_cast<uint32_t>(s) * sb) >> 4);
+            const uint64_t akd = ad + ((static_cast<uint32_t>(kb) * kBlockBytes) >> 4);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_bf16(tbase + acc * NC, akd + 2 * k, bd + 2 * k, idc, (kb | k) != 0 ? 1u : 0u);
+            mma_commit(smem_u32(&ctl->empty[s]));
+            if (++s == nst) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+          if (ok) mma_commit(smem_u32(&ctl->tfull[acc]));
+        }
+        if (ok) mma_commit(smem_u32(&ctl->aempty[ab]));
+      }
+      if (!ok) give_up(ctl, a.err);
+      // every MMA issued above has completed once `done` flips
+      mma_commit(smem_u32(&ctl->done));
+      mbar_wait(smem_u32(&ctl->done), 0, &ctl->abort, bud);
+    }
+  } else if (warp < kPtDrain0) {
+    // ------------------------------------------------------------- builders
+    const int bt = threadIdx.x - kPtBuild0 * 32;   // row of the tile
+    if (bt == 0) {
+      prefetch_tmap(&tmE);
+      if (!a.vq) prefetch_tmap(&tmZ);
+    }
+    int last_ab = -1, last_use = 0;
+    for (int it = 0; it < L; ++it) {
+      const int tile = blockIdx.x + it * gridDim.x;
+      const int ab = nab == 2 ? (it & 1) : 0;
+      const int ause = nab == 2 ? (it >> 1) : it;
+      const bool ok = mbar_wait(smem_u32(&ctl->aempty[ab]), (ause & 1) ^ 1, &ctl->abort, bud);
+      // one decision for all builder warps (they meet at named barriers below)
+      if (named_bar_or(kPtBuildBar, 128, !ok || ctl->abort)) {
+        if (bt == 0) give_up(ctl, a.err);
+        break;
+      }
+      const uint32_t abuf = abuf0 + ab * a.a_bytes;
+      const int n = tile * kTile + bt;
+      int t = 0;
+      bool live = false;
+      if (n < a.N) {
+        t = __ldg(a.tids + n);
+        live = t >= 0 && t < a.V;
+        if (!live) {
+          atomicOr(a.err, kErrBadToken);
+          t = 0;
+        }
+      }
+      ctl->ids[ab][bt] = t;
+      named_bar_sync(kPtBuildBar, 128);
+      if (bt == 0) {
+        // Z_hat (non-VQ payload) and the anchor rows E'[tids] by TMA
+        const uint32_t fb = smem_u32(&ctl->afull[ab]);
+        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nzb) * kBlockBytes * (a.vq ? 1u : 2u));
+        if (!a.vq)
+          for (int kb = 0; kb < nzb; ++kb)
+            tma_load_2d(abuf + kb * kBlockBytes, &tmZ, kb * 64, tile * kTile, fb);
+        const int32_t* ids = ctl->ids[ab];
+        for (int kb = 0; kb < nzb; ++kb)
+          for (int q4 = 0; q4 < kTile / 4; ++q4)
+            tma_gather4(abuf + (nzb + kb) * kBlockBytes + q4 * 512, &tmE, kb * 64, ids[4 * q4],
+                        ids[4 * q4 + 1], ids[4 * q4 + 2], ids[4 * q4 + 3], fb);
+        last_ab = ab;
+        last_use = ause;
+      }
+      if (a.vq) {
+        if constexpr (GD > 0) decode_row_pt<GD>(a, abuf, bt, n, live);
+        fence_async_shared();
+        named_bar_sync(kPtBuildBar, 128);
+      }
+      if (bt == 0) mbar_arrive(smem_u32(&ctl->afull[ab]));
+    }
+    if (bt == 0 && last_ab >= 0 && ctl->abort)
+      mbar_wait(smem_u32(&ctl->afull[last_ab]), last_use & 1, &ctl->abort, bud / 16);
+  } else {
+    // ---------------------------------------------------------------- drain
+    // TMEM -> bf16 -> a swizzled 32-row x 64-column staging tile -> TMA
+    // store.  Each warp double-buffers its staging tile.
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t trow = tbase + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t stg = stage0 + (warp - kPtDrain0) * 8192u;
+    if (lane == 0) prefetch_tmap(&tmXh);
+    int cc = 0, sbuf = 0;
+    bool alive = true;
+    for (int it = 0; it < L && alive; ++it) {
+      const int tile = blockIdx.x + it * gridDim.x;
+      const int n = tile * kTile + row;
+      const int row0 = tile * kTile + q * 32;     // first row of this warp's box
+      const bool any = row0 < a.N;
+      bool bad = false;
+      if (n < a.N) {
+        const int t = __ldg(a.tids + n);
+        bad = t < 0 || t >= a.V;
+      }
+      for (int c = 0; c < nchunk; ++c, ++cc) {
+        const int acc = cc & 1;
+        bool ok = mbar_wait(smem_u32(&ctl->tfull[acc]), (cc >> 1) & 1, &ctl->abort, bud);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          give_up(ctl, a.err);
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        for (int c0 = 0; c0 < NC; c0 += 64) {
+          float v0[32], v1[32];
+          __syncwarp();
+          tmem_ld32(trow + acc * NC + c0, v0);
+          tmem_ld32(trow + acc * NC + c0 + 32, v1);
+          tmem_wait_ld();
+          if (!any) continue;   // no collective operation follows in this iteration
+          if (lane == 0) bulk_wait_read<1>();   // this buffer's previous store has read it
+          __syncwarp();
+          const uint32_t buf = stg + sbuf * 4096u;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float* vv = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);
+            if (!bad)
+              w = make_uint4(pack_bf16x2(vv[0], vv[1]), pack_bf16x2(vv[2], vv[3]),
+                             pack_bf16x2(vv[4], vv[5]), pack_bf16x2(vv[6], vv[7]));
+            st_shared_v4(buf + sw128_off(lane, j), w);
+          }
+          fence_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmXh, buf, c * NC + c0, row0);
+            bulk_commit();
+          }
+          sbuf ^= 1;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+      }
+    }
+    if (lane == 0) bulk_wait<0>();   // stores complete before the CTA exits
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tbase, tmem_cols);
+  }
+}
+
 template <typename KernelT>
 cudaError_t set_smem(KernelT k, uint32_t bytes) {
   return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -343,6 +685,7 @@ cudaError_t set_smem(KernelT k, uint32_t bytes) {
 }  // namespace
 
 uint32_t decompress_ctl_bytes() { return static_cast<uint32_t>(sizeof(Ctl)); }
+uint32_t decompress_pt_ctl_bytes() { return static_cast<uint32_t>(sizeof(CtlPt)) + kPtStagingBytes; }
 
 cudaError_t launch_decompress_tc(const CUtensorMap& tmB, const CUtensorMap& tmZ,
                                  const DecompressArgs& a, uint32_t smem_bytes, int grid,
@@ -368,6 +711,37 @@ cudaError_t launch_decompress_tc(const CUtensorMap& tmB, const CUtensorMap& tmZ,
       e = set_smem(k_decompress_tc<64>, smem_bytes);
       if (e != cudaSuccess) return e;
       k_decompress_tc<64><<<grid, kThreads, smem_bytes, s>>>(tmB, tmZ, a);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace mapl
+
+namespace mapl {
+
+cudaError_t launch_decompress_pt(const CUtensorMap& tmB, const CUtensorMap& tmZ,
+                                 const CUtensorMap& tmE, const CUtensorMap& tmXh,
+                                 const DecompressArgs& a, uint32_t smem_bytes, int grid,
+                                 cudaStream_t s) {
+  cudaError_t e;
+  switch (a.vq ? a.gd : 0) {
+    case 0:
+      e = set_smem(k_decompress_pt<0>, smem_bytes);
+      if (e != cudaSuccess) return e;
+      k_decompress_pt<0><<<grid, kPtThreads, smem_bytes, s>>>(tmB, tmZ, tmE, tmXh, a);
+      break;
+    case 16:
+      e = set_smem(k_decompress_pt<16>, smem_bytes);
+      if (e != cudaSuccess) return e;
+      k_decompress_pt<16><<<grid, kPtThreads, smem_bytes, s>>>(tmB, tmZ, tmE, tmXh, a);
+      break;
+    case 32:
+      e = set_smem(k_decompress_pt<32>, smem_bytes);
+      if (e != cudaSuccess) return e;
+      k_decompress_pt<32><<<grid, kPtThreads, smem_bytes, s>>>(tmB, tmZ, tmE, tmXh, a);
       break;
     default:
       return cudaErrorInvalidValue;

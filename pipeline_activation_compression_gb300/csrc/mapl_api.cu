@@ -26,8 +26,9 @@ struct mapl_plan_s {
   int c_nstage = 0;
   uint32_t c_stage = 0, c_smem = 0;
   int d_nstage = 0;
-  uint32_t d_stage = 0, d_smem = 0, d_abytes = 0;
+  uint32_t d_stage = 0, d_smem = 0, d_abytes = 0, d_nc = 0;
   bool d_stream = false;
+  int d_nab = 0;                      // > 0: persistent kernel with d_nab A buffers
 };
 
 namespace {
@@ -139,20 +140,49 @@ mapl_status geometry(mapl_plan_s* pl) {
     pl->c_smem = ns * st + extra;
   }
   const uint32_t ctl = decompress_ctl_bytes() + 64;
-  // decompress
+  // decompress.  r <= 256: persistent kernel, one CTA per SM, the A operand
+  // [Z_hat | E'] resident (double buffered when two copies leave room for a
+  // ring of three stages).  Larger r: one CTA per tile, A streamed per stage.
   {
-    const int64_t NC = (c.d % 256 == 0) ? 256 : ((c.d % 128 == 0) ? 128 : 64);
     const uint32_t a_res = static_cast<uint32_t>(2 * c.r / 64) * 16384u;
     pl->d_stream = a_res > 131072u;
-    uint32_t st = static_cast<uint32_t>(NC) * 128u + (pl->d_stream ? 16384u : 0u);
-    pl->d_abytes = pl->d_stream ? 0u : a_res;
-    const uint32_t extra = ctl + slack + pl->d_abytes;
-    int ns = static_cast<int>((kSmemMax - extra) / st);
-    if (ns > 8) ns = 8;
-    if (ns < 2) return fail(MAPL_ERR_UNSUPPORTED, "decompress stages do not fit in shared memory");
-    pl->d_nstage = ns;
-    pl->d_stage = st;
-    pl->d_smem = ns * st + extra;
+    const uint32_t NC = (c.d % 256 == 0) ? 256u : ((c.d % 128 == 0) ? 128u : 64u);
+    pl->d_nc = NC;
+    if (!pl->d_stream) {
+      // first of: double-buffered A with NC-column chunks, the same with
+      // 128-column chunks, single A buffer; each with at least three stages
+      const uint32_t extra = decompress_pt_ctl_bytes() + 64 + slack;
+      const uint32_t cand_nc[3] = {NC, NC > 128u ? 128u : NC, NC};
+      const int cand_nab[3] = {2, 2, 1};
+      bool found = false;
+      for (int k = 0; k < 3 && !found; ++k) {
+        const uint32_t used = extra + cand_nab[k] * a_res;
+        if (used >= kSmemMax) continue;
+        const uint32_t st = cand_nc[k] * 128u;
+        int ns = static_cast<int>((kSmemMax - used) / st);
+        if (ns > 8) ns = 8;
+        if (ns < (k < 2 ? 3 : 2)) continue;
+        pl->d_nc = cand_nc[k];
+        pl->d_nab = cand_nab[k];
+        pl->d_abytes = a_res;
+        pl->d_nstage = ns;
+        pl->d_stage = st;
+        pl->d_smem = ns * st + used;
+        found = true;
+      }
+      if (!found) return fail(MAPL_ERR_UNSUPPORTED, "decompress stages do not fit in shared memory");
+    } else {
+      const uint32_t st = NC * 128u + 16384u;
+      const uint32_t extra = ctl + slack;
+      int ns = static_cast<int>((kSmemMax - extra) / st);
+      if (ns > 8) ns = 8;
+      if (ns < 2) return fail(MAPL_ERR_UNSUPPORTED, "decompress stages do not fit in shared memory");
+      pl->d_nab = 0;
+      pl->d_abytes = 0;
+      pl->d_nstage = ns;
+      pl->d_stage = st;
+      pl->d_smem = ns * st + extra;
+    }
   }
   return MAPL_OK;
 }
@@ -160,7 +190,7 @@ mapl_status geometry(mapl_plan_s* pl) {
 mapl_status build_plan_maps(mapl_plan_s* pl) {
   const mapl_config& c = pl->cfg;
   const uint32_t nrow = c.r > 256 ? 256u : static_cast<uint32_t>(c.r);
-  const uint64_t NC = (c.d % 256 == 0) ? 256 : ((c.d % 128 == 0) ? 128 : 64);
+  const uint64_t NC = pl->d_nc;
   if (!make_tmap(&pl->tmAt, pl->p.At, c.d, c.r, 64, nrow))
     return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (A^T)");
   if (!make_tmap(&pl->tmMt, pl->p.Mts, c.r, static_cast<uint64_t>(kNumSplit) * c.r, 64, nrow))
@@ -436,12 +466,25 @@ mapl_status mapl_decompress(mapl_plan pl, const void* payload, const int32_t* ti
   a.gd = pl->gd;
   a.vq = pl->vq ? 1 : 0;
   a.a_stream = pl->d_stream ? 1 : 0;
+  a.nc = static_cast<int>(pl->d_nc);
+  a.nab = pl->d_nab;
   a.nstage = pl->d_nstage;
   a.stage_bytes = pl->d_stage;
   a.a_bytes = pl->d_abytes;
   a.timeout_ns = pl->timeout_ns;
-  const int grid = static_cast<int>((N + kTile - 1) / kTile);
-  e = launch_decompress_tc(pl->tmB, tmZ, a, pl->d_smem, grid, stream);
+  const int ntiles = static_cast<int>((N + kTile - 1) / kTile);
+  if (pl->d_nab > 0) {
+    CUtensorMap tmE;
+    if (!make_tmap(&tmE, E_recv, c.r, static_cast<uint64_t>(c.V), 64, 1))
+      return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (E')");
+    CUtensorMap tmXh;
+    if (!make_tmap(&tmXh, X_hat, c.d, static_cast<uint64_t>(N), 64, 32))
+      return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (X_hat)");
+    const int grid = ntiles < pl->num_sms ? ntiles : pl->num_sms;
+    e = launch_decompress_pt(pl->tmB, tmZ, tmE, tmXh, a, pl->d_smem, grid, stream);
+  } else {
+    e = launch_decompress_tc(pl->tmB, tmZ, a, pl->d_smem, ntiles, stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "decompress launch");
   return MAPL_OK;
 }

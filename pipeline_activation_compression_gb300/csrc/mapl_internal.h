@@ -70,6 +70,8 @@ struct DecompressArgs {
   int N, d, r, V, G, R, K, gd;
   int vq;
   int a_stream;                     // A operand streamed per stage (r > 256)
+  int nc;                           // output columns per accumulator chunk
+  int nab;                          // A operand buffers (persistent kernel)
   int nstage;
   uint32_t stage_bytes;
   uint32_t a_bytes;                 // resident A operand bytes (0 when streamed)
@@ -78,6 +80,7 @@ struct DecompressArgs {
 
 uint32_t compress_ctl_bytes();      // control block of the compress kernel
 uint32_t decompress_ctl_bytes();    // control block of the decompress kernel
+uint32_t decompress_pt_ctl_bytes(); // control block + drain staging of the persistent kernel
 
 // ---- launchers (return cudaGetLastError() of the launch) -------------------
 cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps, const void* Pr,
@@ -89,6 +92,10 @@ cudaError_t launch_compress_tc(const CUtensorMap& tmX, const CUtensorMap& tmAt,
                                const CUtensorMap& tmMt, const CUtensorMap& tmC,
                                const CUtensorMap& tmE, const CompressArgs& a,
                                uint32_t smem_bytes, int grid, cudaStream_t s);
+cudaError_t launch_decompress_pt(const CUtensorMap& tmB, const CUtensorMap& tmZ,
+                                 const CUtensorMap& tmE, const CUtensorMap& tmXh,
+                                 const DecompressArgs& a, uint32_t smem_bytes, int grid,
+                                 cudaStream_t s);
 cudaError_t launch_decompress_tc(const CUtensorMap& tmB, const CUtensorMap& tmZ,
                                  const DecompressArgs& a, uint32_t smem_bytes, int grid,
                                  cudaStream_t s);

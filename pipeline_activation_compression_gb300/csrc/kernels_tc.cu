@@ -351,7 +351,7 @@ constexpr int kPtThreads = 320;
 constexpr int kPtBuild0 = 2;      // first builder warp
 constexpr int kPtDrain0 = 6;      // first drain warp
 constexpr int kPtBuildBar = 2;    // named barrier of the builder warps
-constexpr uint32_t kPtStagingBytes = 4 * 2 * 4096;   // per drain warp: 2 x (32 rows x 128 B)
+constexpr uint32_t kPtStagingBytes = 4 * 4096;   // per drain warp: 32 rows x 128 B
 
 struct CtlPt {
   uint64_t full[kMaxStages];
@@ -604,13 +604,13 @@ __global__ void __launch_bounds__(kPtThreads, 1)
   } else {
     // ---------------------------------------------------------------- drain
     // TMEM -> bf16 -> a swizzled 32-row x 64-column staging tile -> TMA
-    // store.  Each warp double-buffers its staging tile.
+    // store.  The tile is reused once the previous store has read it.
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t trow = tbase + (static_cast<uint32_t>(q * 32) << 16);
-    const uint32_t stg = stage0 + (warp - kPtDrain0) * 8192u;
+    const uint32_t stg = stage0 + (warp - kPtDrain0) * 4096u;
     if (lane == 0) prefetch_tmap(&tmXh);
-    int cc = 0, sbuf = 0;
+    int cc = 0;
     bool alive = true;
     for (int it = 0; it < L && alive; ++it) {
       const int tile = blockIdx.x + it * gridDim.x;
@@ -639,9 +639,9 @@ __global__ void __launch_bounds__(kPtThreads, 1)
           tmem_ld32(trow + acc * NC + c0 + 32, v1);
           tmem_wait_ld();
           if (!any) continue;   // no collective operation follows in this iteration
-          if (lane == 0) bulk_wait_read<1>();   // this buffer's previous store has read it
+          if (lane == 0) bulk_wait_read<0>();   // the previous store has read the tile
           __syncwarp();
-          const uint32_t buf = stg + sbuf * 4096u;
+          const uint32_t buf = stg;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float* vv = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
@@ -657,7 +657,6 @@ __global__ void __launch_bounds__(kPtThreads, 1)
             tma_store_2d(&tmXh, buf, c * NC + c0, row0);
             bulk_commit();
           }
-          sbuf ^= 1;
         }
         tc_fence_before();
         __syncwarp();

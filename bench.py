@@ -130,9 +130,14 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {"mapl_compress": "kernels_compress.cu", "mapl_decompress": "kernels_tc.cu"}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources a kernel is built from: a profiled traffic figure
+    is reported only while it still describes the kernel that runs."""
     h = hashlib.sha256()
-    for name in ("kernels_tc.cu", "ptx.cuh", "mapl_internal.h"):
+    for name in (KERNEL_SOURCES[kernel], "ptx.cuh", "mapl_internal.h", "mapl_api.cu"):
         with open(os.path.join(ROOT, "pipeline_activation_compression_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -147,7 +152,7 @@ def profiled_traffic(kernel: str, workload: str):
     with open(path) as f:
         j = json.load(f)
     e = j.get(f"{kernel}:{workload}")
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return float(e["dram_bytes_per_launch"])
 

@@ -21,13 +21,15 @@
 //                   the half (g & 1) warp of each quadrant.
 //
 // VQ decision.  The residual u (fp32, kept in the Z accumulator's columns) is
-// split into u_hi = bf16(u), u_lo = bf16(u - u_hi) and one MMA per half gives
+// split into u_hi = bf16(u), u_lo = bf16(u - u_hi) and one N = K MMA gives
 // s_k = u_hi.c_k + u_lo.c_k for all codes (|s_k - u.c_k| <= ~2^-18 |u||c_k|
 // plus fp32 accumulation).  D~_k = ||c_k||^2 - 2 s_k is scanned for the best
 // and second best; when the two are within twice the certified error bound
-// every code inside that band is re-scored with the exact squared distance in
-// fp64.  The chosen index is therefore the exact nearest code of the fp32
-// residual (lowest index on exact ties).  The residual update is fp32.
+// every code inside that band is re-scored with the squared distance in
+// double-float arithmetic (about 48 significant bits).  The chosen index is
+// therefore the exact nearest code of the fp32 residual (lowest index on
+// exact ties) unless two distances agree to ~13 significant digits.  The
+// residual update is fp32.
 //
 // Every wait is time bounded (mbar_wait); a CTA that gives up sets the device
 // error word and unwinds through its common exit.

@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Geo geo = geometry(a, vq);
   const int nst = a.nstage;
   const uint32_t sb = a.stage_bytes;
-  const uint32_t cbsb = vq ? static_cast<uint32_t>(a.K) * 128u : 0u;   // codebook stage
+  const uint32_t cbsb = vq ? static_cast<uint32_t>(a.K * a.gd) * 2u : 0u;   // codebook stage
   // shared memory: main ring | codebook ring | residual slots | ||c||^2 | ids | control
   const uint32_t ring = smem_u32(base);
   uint32_t off = nst * sb;
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = mbar_wait(smem_u32(&ctl->cbempty[s]), (use & 1) ^ 1, &ctl->abort, bud)))
               break;
             const uint32_t fb = smem_u32(&ctl->cbfull[s]);
-            mbar_arrive_expect_tx(fb, a.K * 128u);
+            mbar_arrive_expect_tx(fb, cbsb);
             tma_load_2d(cbring + s * cbsb, &tmC, 0, (rho * a.G + g) * a.K, fb);
           }
       }
@@ -589,10 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // scheduler with two busy epilogue warps.
     const uint32_t idz = idesc_bf16(kTile, geo.nrow);
     const uint32_t idd = idesc_bf16(kTile, vq ? a.K : 16);
-    constexpr int kStepsVQ = 2 * (GD > 0 ? GD : 16) / 16;
+    // distance MMA: K-steps over [u_hi | u_lo]; both halves read the same
+    // code rows (one copy of each code in the codebook ring)
+    constexpr int kStepsC = (GD > 0 ? GD : 16) / 16;
     const uint64_t ring_d = sw128_desc(ring);
     const uint64_t ub_d = sw128_desc(ubase);
-    const uint64_t cb_d = sw128_desc(cbring);
+    const uint64_t cb_d = narrow_desc<(GD == 32 ? 64 : 32)>(cbring);
     int pj_it = 0, pj_p = 0, pj_s = 0, pj_sp = 0, blk0 = 0, blk1 = 0;
     uint32_t pj_ph = 0;
     bool pj_started = false;
@@ -618,8 +620,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t ad = ub_d + ((static_cast<uint32_t>(slot) * kBlockBytes) >> 4);
           const uint64_t bd = cb_d + ((static_cast<uint32_t>(vq_cs) * cbsb) >> 4);
 #pragma unroll
-          for (int k = 0; k < kStepsVQ; ++k)
-            mma_bf16(tbase + 256, ad + 2 * k, bd + 2 * k, idd, k != 0 ? 1u : 0u);
+          for (int k = 0; k < 2 * kStepsC; ++k)
+            mma_bf16(tbase + 256, ad + 2 * k, bd + 2 * (k % kStepsC), idd, k != 0 ? 1u : 0u);
           mma_commit(smem_u32(&ctl->dfull[0]));
           mma_commit(smem_u32(&ctl->dfull[1]));
           mma_commit(smem_u32(&ctl->cbempty[vq_cs]));

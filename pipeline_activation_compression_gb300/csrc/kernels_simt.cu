@@ -73,7 +73,7 @@ __global__ void k_prep_At32(const float* A, int d, int r, float* At) {
 }
 
 __global__ void k_prep_codes(const void* C, int nbooks, int K, int gd, bool bf,
-                             __nv_bfloat16* Cpad, __nv_bfloat16* Cb, float* C32, float* cnorm) {
+                             __nv_bfloat16* Cb, float* C32, float* cnorm) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;   // code id over all books
   if (idx >= nbooks * K) return;
   double s = 0.0;
@@ -82,12 +82,6 @@ __global__ void k_prep_codes(const void* C, int nbooks, int K, int gd, bool bf,
     s = fma(v, v, s);
     if (Cb) Cb[static_cast<size_t>(idx) * gd + i] = reinterpret_cast<const __nv_bfloat16*>(C)[static_cast<size_t>(idx) * gd + i];
     if (C32) C32[static_cast<size_t>(idx) * gd + i] = static_cast<float>(v);
-  }
-  if (Cpad) {   // [c | c | 0]: the same code against the hi and the lo residual term
-    const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(C) + static_cast<size_t>(idx) * gd;
-    for (int i = 0; i < 64; ++i)
-      Cpad[static_cast<size_t>(idx) * 64 + i] =
-          i < 2 * gd ? src[i % gd] : __float2bfloat16(0.f);
   }
   cnorm[idx] = static_cast<float>(s);
 }
@@ -229,7 +223,7 @@ cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps
   if (!A_only && c.G > 0) {
     const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G);
     k_prep_codes<<<blocks_for(static_cast<size_t>(nb) * c.K, T), T, 0, s>>>(
-        C, nb, c.K, gd, true, p.Cpad, p.Cb, nullptr, p.cnorm);
+        C, nb, c.K, gd, true, p.Cb, nullptr, p.cnorm);
     k_prep_cmax<<<blocks_for(nb, 64), 64, 0, s>>>(p.cnorm, nb, c.K, p.cmax);
   }
   return cudaGetLastError();
@@ -249,7 +243,7 @@ cudaError_t launch_prep_f32(const mapl_config& c, const void* A, const void* Ps,
     if (c.G > 0) {
       const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G);
       k_prep_codes<<<blocks_for(static_cast<size_t>(nb) * c.K, T), T, 0, s>>>(
-          C, nb, c.K, gd, false, nullptr, nullptr, p.C32, p.cnorm);
+          C, nb, c.K, gd, false, nullptr, p.C32, p.cnorm);
       k_prep_cmax<<<blocks_for(nb, 64), 64, 0, s>>>(p.cnorm, nb, c.K, p.cmax);
     }
   }

@@ -70,7 +70,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 2-D bf16 tensor map over a row-major (outer x inner) matrix, 128-byte
 // swizzled boxes of box_outer rows x 64 elements; out-of-range reads are zero.
 bool make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
-               uint32_t box_inner, uint32_t box_outer) {
+               uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -78,7 +79,7 @@ bool make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -128,7 +129,7 @@ mapl_status geometry(mapl_plan_s* pl) {
     st = (st + 1023u) & ~1023u;
     uint32_t extra = compress_ctl_bytes() + 64 + slack + 2 * 128 * 4;   // + tile ids
     if (pl->vq) {
-      extra += 2u * static_cast<uint32_t>(c.K) * 128u;                    // codebook ring
+      extra += 2u * static_cast<uint32_t>(c.K * (c.r / c.G)) * 2u;         // codebook ring
       extra += static_cast<uint32_t>(c.G < 2 ? c.G : 2) * 16384u;         // residual slots
       extra += (static_cast<uint32_t>(c.R * c.G * c.K) * 4u + 15u) & ~15u; // ||c||^2
     }
@@ -198,8 +199,13 @@ mapl_status build_plan_maps(mapl_plan_s* pl) {
   if (!make_tmap(&pl->tmB, pl->p.Bcat, 2 * c.r, c.d, 64, static_cast<uint32_t>(NC)))
     return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed ([A | P'^T])");
   if (pl->vq) {
-    if (!make_tmap(&pl->tmC, pl->p.Cpad, 64, static_cast<uint64_t>(c.R) * c.G * c.K, 64,
-                   static_cast<uint32_t>(c.K)))
+    // one book per load, rows of gd bf16 in the swizzle that matches the row
+    // width (64 B: SWIZZLE_64B, 32 B: SWIZZLE_32B)
+    const CUtensorMapSwizzle swz =
+        pl->gd == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    if (!make_tmap(&pl->tmC, pl->p.Cb, static_cast<uint64_t>(pl->gd),
+                   static_cast<uint64_t>(c.R) * c.G * c.K, static_cast<uint32_t>(pl->gd),
+                   static_cast<uint32_t>(c.K), swz))
       return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (codebooks)");
   } else {
     pl->tmC = pl->tmAt;   // unused
@@ -268,7 +274,7 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   // one pool for every plan-owned buffer
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off += up256(bytes); return o; };
-  size_t oAt = 0, oMts = 0, oBcat = 0, oCpad = 0, oCb = 0, oA32 = 0, oAt32 = 0, oM32 = 0,
+  size_t oAt = 0, oMts = 0, oBcat = 0, oCb = 0, oA32 = 0, oAt32 = 0, oM32 = 0,
          oC32 = 0;
   const size_t oPs = take(d * r * elt_size(*cfg));
   const size_t oPr = take(d * r * elt_size(*cfg));
@@ -276,10 +282,7 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
     oAt = take(d * r * 2);
     oMts = take(static_cast<size_t>(kNumSplit) * r * r * 2);
     oBcat = take(d * 2 * r * 2);
-    if (vq) {
-      oCpad = take(ncode * 64 * 2);
-      oCb = take(ncode * pl->gd * 2);
-    }
+    if (vq) oCb = take(ncode * pl->gd * 2);
   } else {
     oA32 = take(d * r * 4);
     oAt32 = take(d * r * 4);
@@ -302,10 +305,7 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
     p.At = reinterpret_cast<__nv_bfloat16*>(b + oAt);
     p.Mts = reinterpret_cast<__nv_bfloat16*>(b + oMts);
     p.Bcat = reinterpret_cast<__nv_bfloat16*>(b + oBcat);
-    if (vq) {
-      p.Cpad = reinterpret_cast<__nv_bfloat16*>(b + oCpad);
-      p.Cb = reinterpret_cast<__nv_bfloat16*>(b + oCb);
-    }
+    if (vq) p.Cb = reinterpret_cast<__nv_bfloat16*>(b + oCb);
   } else {
     p.A32 = reinterpret_cast<float*>(b + oA32);
     p.At32 = reinterpret_cast<float*>(b + oAt32);

@@ -27,9 +27,8 @@ struct PlanDevice {
   __nv_bfloat16* At = nullptr;      // r x d     A^T (K-major B operand of X A)
   __nv_bfloat16* Mts = nullptr;     // S x r x r -M^T split into S bf16 terms
   __nv_bfloat16* Bcat = nullptr;    // d x 2r    [A | P_recv^T] (K-major B of decompress)
-  __nv_bfloat16* Cpad = nullptr;    // R*G*K x 64 codebook rows [c | c | 0] (B operand of
-                                    // the two-term distance MMA)
-  __nv_bfloat16* Cb = nullptr;      // R x G x K x gd codebooks (decode lookups)
+  __nv_bfloat16* Cb = nullptr;      // R x G x K x gd codebooks (B operand of the distance
+                                    // MMA, decode lookups)
   // fp32 CUDA-core path
   float* A32 = nullptr;             // d x r
   float* At32 = nullptr;            // r x d     A^T

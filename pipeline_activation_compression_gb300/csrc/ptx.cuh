@@ -262,6 +262,22 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
   return d;
 }
 
+// Shared-memory descriptor of a K-major operand whose rows are only 64 bytes
+// (ROWB = 64: SWIZZLE_64B, layout code 4) or 32 bytes (ROWB = 32:
+// SWIZZLE_32B, code 6) wide, as TMA writes them; 8-row groups are 8 * ROWB
+// bytes apart.  Used for codebooks of 32 or 16 bf16 per code.
+template <int ROWB>
+__device__ __forceinline__ uint64_t narrow_desc(uint32_t addr) {
+  static_assert(ROWB == 64 || ROWB == 32, "64- or 32-byte rows");
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);         // start address
+  d |= static_cast<uint64_t>(1) << 16;                         // LBO (unused, K within a row)
+  d |= static_cast<uint64_t>((8 * ROWB) >> 4) << 32;           // SBO: 8 rows
+  d |= static_cast<uint64_t>(1) << 46;                         // descriptor version (sm_100+)
+  d |= static_cast<uint64_t>(ROWB == 64 ? 4 : 6) << 61;        // swizzle: 64 B / 32 B
+  return d;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B, fp32 D, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4)                                   // D format: f32

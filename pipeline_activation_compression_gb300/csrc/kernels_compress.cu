@@ -65,6 +65,7 @@ struct Ctl {
   float xb2[2][2][kTile];           // second best of a half
   int xk1[2][2][kTile];             // index of the best
   float nu[kNSlot][2][kTile];       // ||u|| of the residual in a slot [round parity]
+  float uscr[8][32];                // per epilogue warp: the residual being refined
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -222,72 +223,101 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = (a - (s - bb)) + (b - bb);
 }
 
-// ||u - c||^2 as an unevaluated pair hi + lo (about 48 significant bits):
-// u - c is split exactly, each square is split exactly by an fma, and the
-// running sum keeps its rounding errors.  Enough to order two codes whose
-// distances differ in the 13th significant digit.  u stays in registers.
+// 16-byte chunk c of code k in a codebook stage as TMA wrote it (rows of
+// 2*GD bytes, 64- or 32-byte swizzle: the chunk index is XORed with address
+// bits 7.. of the row).
 template <int GD>
-__device__ __forceinline__ void exact_dist(const float (&u)[GD], const __nv_bfloat16* cr,
-                                           float& hi, float& lo) {
+__device__ __forceinline__ uint4 code_chunk(const uint8_t* stage, int k, int c) {
+  constexpr int kRowB = 2 * GD, kNch = kRowB / 16;
+  const int sw = c ^ (((k * kRowB) >> 7) & (kNch - 1));
+  return *reinterpret_cast<const uint4*>(stage + k * kRowB + sw * 16);
+}
+
+// Element `lane` (< GD) of code k in a codebook stage, as a float.
+template <int GD>
+__device__ __forceinline__ float code_elem(const uint8_t* stage, int k, int lane) {
+  constexpr int kRowB = 2 * GD, kNch = kRowB / 16;
+  const int c = lane >> 3;
+  const int sw = c ^ (((k * kRowB) >> 7) & (kNch - 1));
+  const __nv_bfloat16 v =
+      *reinterpret_cast<const __nv_bfloat16*>(stage + k * kRowB + sw * 16 + (lane & 7) * 2);
+  return __bfloat162float(v);
+}
+
+// ||u - c_k||^2 as an unevaluated pair hi + lo (about 48 significant bits),
+// computed by the whole warp: lane j forms (u_j - c_j)^2 exactly (two-sum of
+// the difference, fma split of the square) and a five-level shuffle tree
+// adds the 32 pairs with two-sums.  `uj` is u_j on lane j (0 past GD).
+// Enough to order two codes whose distances differ in the 13th digit.
+template <int GD>
+__device__ __forceinline__ void coop_exact_dist(float uj, const uint8_t* stage, int k, int lane,
+                                                float& hi, float& lo) {
   float h = 0.f, l = 0.f;
-#pragma unroll
-  for (int q = 0; q < GD / 8; ++q) {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(cr) + q);
-    const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&w);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float2 f = __bfloat1622float2(hp[e >> 1]);
-      const float c = (e & 1) ? f.y : f.x;
-      float d, de;
-      two_sum(u[q * 8 + e], -c, d, de);
-      const float p = d * d;
-      float pe = fmaf(d, d, -p);
-      pe = fmaf(2.f * d, de, pe);
-      float s, se;
-      two_sum(h, p, s, se);
-      h = s;
-      l += se + pe;
-    }
+  if (lane < GD) {
+    float d, de;
+    two_sum(uj, -code_elem<GD>(stage, k, lane), d, de);
+    h = d * d;
+    l = fmaf(2.f * d, de, fmaf(d, d, -h));
   }
-  float s, e;
-  two_sum(h, l, s, e);
-  hi = s;
-  lo = e;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float oh = __shfl_xor_sync(kFull, h, o);
+    const float ol = __shfl_xor_sync(kFull, l, o);
+    float s, e;
+    two_sum(h, oh, s, e);
+    h = s;
+    l = (l + ol) + e;
+  }
+  two_sum(h, l, hi, lo);
 }
 
 // Rare path: exact re-scoring of every code whose coarse distance lies within
-// `thr`.  Returns the exact nearest code (lowest index on exact ties).  Per
-// 16-column chunk the in-band codes become a bit mask (registers only) that a
-// compact loop walks in increasing index order.
+// `thr` (lanes with `need`).  Returns the exact nearest code (lowest index on
+// exact ties).  Per 32-column chunk the in-band codes of each lane become a
+// bit mask; the warp then scores each candidate of each lane together.
 template <int GD>
 __device__ __forceinline__ int refine(const float (&u)[GD], uint32_t td0, const float* cn,
-                                      const __nv_bfloat16* book, int KH, float thr, bool need,
-                                      int k_init) {
+                                      const uint8_t* stage, float* uscr, int KH, float thr,
+                                      bool need, int k_init, int lane) {
   float bh = __int_as_float(0x7f800000), bl = 0.f;
   int kb = k_init;
+  int staged = -1;   // lane whose residual is in uscr
 #pragma unroll 1
-  for (int c = 0; c < 2 * KH; c += 16) {
-    const int hh = c >= KH ? 1 : 0;
-    const int c0 = c - hh * KH;
-    float v[16];
+  for (int c = 0; c < 2 * KH; c += 32) {
+    float v[32];
     __syncwarp();
-    tmem_ld16(td0 + hh * KH + c0, v);
+    tmem_ld32(td0 + c, v);
     tmem_wait_ld();
     uint32_t mask = 0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
+    for (int j = 0; j < 32; ++j)
       mask |= (fmaf(-2.f, v[j], cn[c + j]) <= thr ? 1u : 0u) << j;
     if (!need) mask = 0;
-    while (mask) {
-      const int j = __ffs(mask) - 1;
-      mask &= mask - 1;
-      const int kk = c + j;
-      float eh, el;
-      exact_dist<GD>(u, book + static_cast<size_t>(kk) * GD, eh, el);
-      if (eh < bh || (eh == bh && el < bl)) {
-        bh = eh;
-        bl = el;
-        kb = kk;
+    uint32_t lanes = __ballot_sync(kFull, mask != 0);
+    while (lanes) {
+      const int L = __ffs(lanes) - 1;
+      lanes &= lanes - 1;
+      if (L != staged) {
+        __syncwarp();
+        if (lane == L) {
+#pragma unroll
+          for (int i = 0; i < GD; ++i) uscr[i] = u[i];
+        }
+        __syncwarp();
+        staged = L;
+      }
+      const float uj = lane < GD ? uscr[lane] : 0.f;
+      uint32_t mL = __shfl_sync(kFull, mask, L);
+      while (mL) {
+        const int kk = c + __ffs(mL) - 1;
+        mL &= mL - 1;
+        float eh, el;
+        coop_exact_dist<GD>(uj, stage, kk, lane, eh, el);
+        if (lane == L && (eh < bh || (eh == bh && el < bl))) {
+          bh = eh;
+          bl = el;
+          kb = kk;
+        }
       }
     }
   }
@@ -296,8 +326,9 @@ __device__ __forceinline__ int refine(const float (&u)[GD], uint32_t td0, const 
 
 template <int GD>
 __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uint32_t tbase,
-                            uint32_t ubase, const float* cn_s, int tile, int zb, int q, int h,
-                            int lane, uint32_t& dcnt, uint32_t& pcnt, bool& alive) {
+                            uint32_t ubase, const float* cn_s, const uint8_t* cbring_p,
+                            uint32_t cbsb, int tile, int zb, int q, int h, int lane,
+                            uint32_t& dcnt, uint32_t& pcnt, bool& alive) {
   const int row = q * 32 + lane;
   const int n = tile * kTile + row;
   const bool store = n < a.N;
@@ -333,6 +364,11 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
         const int book = rho * G + g;
         const bool owner = (G == 1) ? (h == 0) : ((g & 1) == h);
         const int par = static_cast<int>(dcnt & 1u);
+        // this step's codebook stage (read by the owner's refinement and
+        // residual update; the owners release it at the end of the step)
+        const int cs = static_cast<int>(dcnt % kCbStages);
+        const uint32_t cph = (dcnt / kCbStages) & 1u;
+        const uint8_t* stage = cbring_p + cs * cbsb;
         // 1. distances of this half are in TMEM
         if (!warp_wait(smem_u32(&ctl->dfull[h]), dcnt & 1u, ctl, bud)) {
           give_up(ctl, a.err);
@@ -340,6 +376,11 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
           break;
         }
         tc_fence_after();
+        if (owner && !warp_wait(smem_u32(&ctl->cbfull[cs]), cph, ctl, bud)) {
+          give_up(ctl, a.err);
+          alive = false;
+          break;
+        }
         const uint32_t tdist = tbase + lanebase + 256 + h * KH;
         float b1, b2;
         int k1;
@@ -373,8 +414,8 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
             tmem_load_group<GD>(tz + g * GD, u);
             have_u = true;
             const float thr = B1 + 2.f * eps;
-            const int kb = refine<GD>(u, tbase + lanebase + 256, cn_s + book * K,
-                                      a.Cb + static_cast<size_t>(book) * K * GD, KH, thr, need, K1);
+            const int kb = refine<GD>(u, tbase + lanebase + 256, cn_s + book * K, stage,
+                                      ctl->uscr[q + 4 * h], KH, thr, need, K1, lane);
             if (need) K1 = kb;
           }
           // the partner keeps its half until the owner has re-read it
@@ -394,11 +435,9 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
         if (store) idx_out[rho * G + g] = bad ? static_cast<uint8_t>(0) : static_cast<uint8_t>(K1);
         if (rho + 1 < R) {
           if (!have_u) tmem_load_group<GD>(tz + g * GD, u);
-          const uint4* cr4 =
-              reinterpret_cast<const uint4*>(a.Cb + (static_cast<size_t>(book) * K + K1) * GD);
 #pragma unroll
           for (int c = 0; c < GD / 8; ++c) {
-            const uint4 w = __ldg(cr4 + c);
+            const uint4 w = code_chunk<GD>(stage, K1, c);
             const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&w);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -414,6 +453,8 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&ctl->uready[slot]));
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->cbempty[cs]));
       }
     }
   }
@@ -469,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int p = 0; p < 4; ++p) mbar_init(smem_u32(&ctl->pair[p]), 2);
     for (int s = 0; s < kCbStages; ++s) {
       mbar_init(smem_u32(&ctl->cbfull[s]), 1);
-      mbar_init(smem_u32(&ctl->cbempty[s]), 1);
+      mbar_init(smem_u32(&ctl->cbempty[s]), 4);   // the four owner warps of the step
     }
     ctl->abort = 0;
     fence_mbar_init();
@@ -624,7 +665,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16(tbase + 256, ad + 2 * k, bd + 2 * (k % kStepsC), idd, k != 0 ? 1u : 0u);
           mma_commit(smem_u32(&ctl->dfull[0]));
           mma_commit(smem_u32(&ctl->dfull[1]));
-          mma_commit(smem_u32(&ctl->cbempty[vq_cs]));
           progressed = true;
           if (slot == 0) ++ucnt0; else ++ucnt1;
           got_u = got_c = false;
@@ -729,7 +769,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (vq) {
         if constexpr (GD > 0)
-          epilogue_vq<GD>(a, geo, ctl, tbase, ubase, cn_s, tile, zb, q, h, lane, dcnt, pcnt,
+          epilogue_vq<GD>(a, geo, ctl, tbase, ubase, cn_s, base + nst * sb, cbsb, tile, zb, q,
+                          h, lane, dcnt, pcnt,
                           alive);
         const int n = tile * kTile + q * 32 + lane;
         if (alive && h == 0 && n < a.N) {

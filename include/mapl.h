@@ -126,6 +126,33 @@ mapl_status mapl_decompress(mapl_plan plan, const void* payload, const int32_t* 
                             int64_t N, const void* E_recv, void* X_hat, cudaStream_t stream);
 
 /*
+ * Host-buffer forms of mapl_compress / mapl_decompress, for callers whose
+ * boundary activations live in host memory.  They are not part of the MAPL
+ * method; they stage the host data through a caller-owned device workspace
+ * on `stream`:
+ *   mapl_compress_host:   X (N x d) and tids (N) are copied host -> device,
+ *                         compressed, and the payload copied device -> host.
+ *   mapl_decompress_host: payload and tids are copied host -> device,
+ *                         decompressed, and X_hat (N x d) copied back.
+ * X, tids, payload and X_hat are HOST pointers (pinned memory gives
+ * asynchronous copies; pageable memory makes the copies synchronous);
+ * E_send / E_recv stay DEVICE pointers (plan-lifetime tables).  workspace is
+ * device memory of at least mapl_host_workspace_size(plan, N) bytes,
+ * 256-byte aligned, owned by the caller and not shared by calls that may
+ * overlap.  The output host buffer is written when the stream reaches the
+ * end of the call.  Async; same errors as the device forms.
+ */
+mapl_status mapl_host_workspace_size(mapl_plan plan, int64_t N, size_t* bytes);
+
+mapl_status mapl_compress_host(mapl_plan plan, const void* X, const int32_t* tids, int64_t N,
+                               const void* E_send, void* payload, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+
+mapl_status mapl_decompress_host(mapl_plan plan, const void* payload, const int32_t* tids,
+                                 int64_t N, const void* E_recv, void* X_hat, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the plan's device error word.
  * Returns MAPL_OK, MAPL_ERR_BAD_TOKEN, MAPL_ERR_TIMEOUT, MAPL_ERR_CUDA, or
  * MAPL_ERR_INVALID_ARG when a decompressed payload held an index >= K (that

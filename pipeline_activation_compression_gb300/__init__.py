@@ -18,6 +18,7 @@ __all__ = [
     "MaplError", "MaplConfig", "Plan", "load_library", "library_path", "build",
     "mapl_plan_create", "mapl_plan_update_A", "mapl_payload_bytes", "mapl_compress",
     "mapl_compress_z32", "mapl_decompress", "mapl_check", "mapl_plan_destroy",
+    "mapl_host_workspace_size", "mapl_compress_host", "mapl_decompress_host",
     "mapl_spel_workspace_size", "mapl_spel_step", "mapl_spel_step_static", "mapl_last_error",
     "mapl_version",
     "MAPL_F32", "MAPL_BF16", "STATUS",
@@ -71,6 +72,9 @@ def load_library():
         "mapl_compress_z32": [P, P, P, I64, P, P, P],
         "mapl_decompress": [P, P, P, I64, P, P, P],
         "mapl_check": [P, P],
+        "mapl_host_workspace_size": [P, I64, ctypes.POINTER(SZ)],
+        "mapl_compress_host": [P, P, P, I64, P, P, P, SZ, P],
+        "mapl_decompress_host": [P, P, P, I64, P, P, P, SZ, P],
         "mapl_spel_workspace_size": [I64, I64, I32, ctypes.POINTER(SZ)],
         "mapl_spel_step": [P, P, P, I64, I64, I32, ctypes.c_float, ctypes.c_float, P, I32, I32,
                            P, SZ, P],
@@ -212,6 +216,47 @@ def mapl_decompress(plan: Plan, payload, tids, E_recv, X_hat, stream=None):
         plan.handle, _ptr(payload, plan.payload_dtype(), "payload"),
         _ptr(tids, torch.int32, "tids"), int(tids.shape[0]), _ptr(E_recv, dt, "E_recv"),
         _ptr(X_hat, dt, "X_hat"), _stream(stream)))
+    return X_hat
+
+
+def _host_ptr(t, dtype, what):
+    """Address of a contiguous CPU tensor (pinned for asynchronous copies)."""
+    if t.is_cuda:
+        raise ValueError(f"{what} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what} must have dtype {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def mapl_host_workspace_size(plan: Plan, N: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().mapl_host_workspace_size(plan.handle, int(N), ctypes.byref(out)))
+    return int(out.value)
+
+
+def mapl_compress_host(plan: Plan, X, tids, E_send, payload, workspace, stream=None):
+    """X, tids, payload: host tensors; E_send, workspace: device tensors."""
+    import torch
+    dt = _tdtype(plan.cfg.dtype)
+    _check(load_library().mapl_compress_host(
+        plan.handle, _host_ptr(X, dt, "X"), _host_ptr(tids, torch.int32, "tids"),
+        int(X.shape[0]), _ptr(E_send, dt, "E_send"),
+        _host_ptr(payload, plan.payload_dtype(), "payload"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return payload
+
+
+def mapl_decompress_host(plan: Plan, payload, tids, E_recv, X_hat, workspace, stream=None):
+    """payload, tids, X_hat: host tensors; E_recv, workspace: device tensors."""
+    import torch
+    dt = _tdtype(plan.cfg.dtype)
+    _check(load_library().mapl_decompress_host(
+        plan.handle, _host_ptr(payload, plan.payload_dtype(), "payload"),
+        _host_ptr(tids, torch.int32, "tids"), int(tids.shape[0]), _ptr(E_recv, dt, "E_recv"),
+        _host_ptr(X_hat, dt, "X_hat"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
     return X_hat
 
 

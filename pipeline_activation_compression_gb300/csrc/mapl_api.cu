@@ -489,6 +489,101 @@ mapl_status mapl_decompress(mapl_plan pl, const void* payload, const int32_t* ti
   return MAPL_OK;
 }
 
+// ---------------------------------------------------------- host buffers
+namespace {
+
+struct HostLayout {
+  size_t x, tids, payload, total;
+};
+
+void payload_bytes_of(const mapl_config& c, int64_t* bytes) {
+  *bytes = c.G > 0 ? static_cast<int64_t>(c.R) * c.G : c.r * static_cast<int64_t>(elt_size(c));
+}
+
+HostLayout host_layout(const mapl_plan_s* pl, int64_t N) {
+  const mapl_config& c = pl->cfg;
+  int64_t pbytes = 0;
+  payload_bytes_of(c, &pbytes);
+  HostLayout h;
+  h.x = 0;
+  h.tids = h.x + up256(static_cast<size_t>(N) * c.d * elt_size(c));
+  h.payload = h.tids + up256(static_cast<size_t>(N) * 4);
+  h.total = h.payload + up256(static_cast<size_t>(N) * pbytes);
+  return h;
+}
+
+mapl_status host_args(const mapl_plan_s* pl, int64_t N, const void* a, const void* b,
+                      const void* c, void* ws, size_t ws_bytes, HostLayout* h) {
+  if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
+  if (!a || !b || !c || !ws) return fail(MAPL_ERR_INVALID_ARG, "NULL pointer");
+  if (N < 1 || N > 0x7fffffffLL) return fail(MAPL_ERR_INVALID_ARG, "N must be in [1, 2^31)");
+  if (reinterpret_cast<uintptr_t>(ws) & 255u)
+    return fail(MAPL_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  *h = host_layout(pl, N);
+  if (ws_bytes < h->total)
+    return fail(MAPL_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", ws_bytes, h->total);
+  return MAPL_OK;
+}
+
+}  // namespace
+
+mapl_status mapl_host_workspace_size(mapl_plan pl, int64_t N, size_t* bytes) {
+  if (!pl || !bytes) return fail(MAPL_ERR_INVALID_ARG, "NULL argument");
+  if (N < 1 || N > 0x7fffffffLL) return fail(MAPL_ERR_INVALID_ARG, "N must be in [1, 2^31)");
+  *bytes = host_layout(pl, N).total;
+  return MAPL_OK;
+}
+
+mapl_status mapl_compress_host(mapl_plan pl, const void* X, const int32_t* tids, int64_t N,
+                               const void* E_send, void* payload, void* ws, size_t ws_bytes,
+                               cudaStream_t stream) {
+  HostLayout h;
+  mapl_status st = host_args(pl, N, X, tids, payload, ws, ws_bytes, &h);
+  if (st != MAPL_OK) return st;
+  const mapl_config& c = pl->cfg;
+  int64_t pbytes = 0;
+  payload_bytes_of(c, &pbytes);
+  char* w = reinterpret_cast<char*>(ws);
+  cudaError_t e = cudaMemcpyAsync(w + h.x, X, static_cast<size_t>(N) * c.d * elt_size(c),
+                                  cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(w + h.tids, tids, static_cast<size_t>(N) * 4, cudaMemcpyHostToDevice,
+                        stream);
+  if (e != cudaSuccess) return cuda_fail(e, "host -> device copy");
+  st = mapl_compress(pl, w + h.x, reinterpret_cast<const int32_t*>(w + h.tids), N, E_send,
+                     w + h.payload, stream);
+  if (st != MAPL_OK) return st;
+  e = cudaMemcpyAsync(payload, w + h.payload, static_cast<size_t>(N) * pbytes,
+                      cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "device -> host copy");
+  return MAPL_OK;
+}
+
+mapl_status mapl_decompress_host(mapl_plan pl, const void* payload, const int32_t* tids,
+                                 int64_t N, const void* E_recv, void* X_hat, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
+  HostLayout h;
+  mapl_status st = host_args(pl, N, payload, tids, X_hat, ws, ws_bytes, &h);
+  if (st != MAPL_OK) return st;
+  const mapl_config& c = pl->cfg;
+  int64_t pbytes = 0;
+  payload_bytes_of(c, &pbytes);
+  char* w = reinterpret_cast<char*>(ws);
+  cudaError_t e = cudaMemcpyAsync(w + h.payload, payload, static_cast<size_t>(N) * pbytes,
+                                  cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(w + h.tids, tids, static_cast<size_t>(N) * 4, cudaMemcpyHostToDevice,
+                        stream);
+  if (e != cudaSuccess) return cuda_fail(e, "host -> device copy");
+  st = mapl_decompress(pl, w + h.payload, reinterpret_cast<const int32_t*>(w + h.tids), N, E_recv,
+                       w + h.x, stream);
+  if (st != MAPL_OK) return st;
+  e = cudaMemcpyAsync(X_hat, w + h.x, static_cast<size_t>(N) * c.d * elt_size(c),
+                      cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "device -> host copy");
+  return MAPL_OK;
+}
+
 mapl_status mapl_check(mapl_plan pl, cudaStream_t stream) {
   if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
   cudaError_t e = cudaStreamSynchronize(stream);

@@ -271,46 +271,57 @@ __device__ __forceinline__ void coop_exact_dist(float uj, const uint8_t* stage, 
   two_sum(h, l, hi, lo);
 }
 
-// Rare path: exact re-scoring of every code whose coarse distance lies within
-// `thr` (lanes with `need`).  Returns the exact nearest code (lowest index on
-// exact ties).  Per 32-column chunk the in-band codes of each lane become a
-// bit mask; the warp then scores each candidate of each lane together.
+// Rare path, on CUDA cores (the distance buffer is already released): for
+// every lane with `need`, the warp recomputes coarse distances
+// ||c_k||^2 - 2 u.c_k in fp32 for all K codes from the codebook stage (lane j
+// takes codes j, j + 32, ...), keeps the codes within that lane's `thr`, and
+// re-scores each of them exactly with the whole warp.  Returns the exact
+// nearest code (lowest index on exact ties); other lanes keep k_init.
 template <int GD>
-__device__ __forceinline__ int refine(const float (&u)[GD], uint32_t td0, const float* cn,
-                                      const uint8_t* stage, float* uscr, int KH, float thr,
+__device__ __forceinline__ int refine(const float (&u)[GD], const float* cn,
+                                      const uint8_t* stage, float* uscr, int K, float thr,
                                       bool need, int k_init, int lane) {
   float bh = __int_as_float(0x7f800000), bl = 0.f;
   int kb = k_init;
-  int staged = -1;   // lane whose residual is in uscr
-#pragma unroll 1
-  for (int c = 0; c < 2 * KH; c += 32) {
-    float v[32];
+  uint32_t lanes = __ballot_sync(kFull, need);
+  while (lanes) {
+    const int L = __ffs(lanes) - 1;
+    lanes &= lanes - 1;
     __syncwarp();
-    tmem_ld32(td0 + c, v);
-    tmem_wait_ld();
-    uint32_t mask = 0;
+    if (lane == L) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      mask |= (fmaf(-2.f, v[j], cn[c + j]) <= thr ? 1u : 0u) << j;
-    if (!need) mask = 0;
-    uint32_t lanes = __ballot_sync(kFull, mask != 0);
-    while (lanes) {
-      const int L = __ffs(lanes) - 1;
-      lanes &= lanes - 1;
-      if (L != staged) {
-        __syncwarp();
-        if (lane == L) {
+      for (int i = 0; i < GD; ++i) uscr[i] = u[i];
+    }
+    __syncwarp();
+    const float thrL = __shfl_sync(kFull, thr, L);
+    float uu[GD];
 #pragma unroll
-          for (int i = 0; i < GD; ++i) uscr[i] = u[i];
+    for (int i = 0; i < GD; ++i) uu[i] = uscr[i];
+    uint32_t cmask = 0;   // bit i: code lane + 32 i is a candidate
+#pragma unroll 1
+    for (int i = 0; i < K / 32; ++i) {
+      const int k = lane + 32 * i;
+      float dot = 0.f;
+#pragma unroll
+      for (int q = 0; q < GD / 8; ++q) {
+        const uint4 w = code_chunk<GD>(stage, k, q);
+        const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(hp[e]);
+          dot = fmaf(uu[q * 8 + 2 * e], f.x, dot);
+          dot = fmaf(uu[q * 8 + 2 * e + 1], f.y, dot);
         }
-        __syncwarp();
-        staged = L;
       }
-      const float uj = lane < GD ? uscr[lane] : 0.f;
-      uint32_t mL = __shfl_sync(kFull, mask, L);
-      while (mL) {
-        const int kk = c + __ffs(mL) - 1;
-        mL &= mL - 1;
+      cmask |= (fmaf(-2.f, dot, cn[k]) <= thrL ? 1u : 0u) << i;
+    }
+    const float uj = lane < GD ? uscr[lane] : 0.f;
+#pragma unroll 1
+    for (int i = 0; i < K / 32; ++i) {
+      uint32_t cl = __ballot_sync(kFull, (cmask >> i) & 1u);
+      while (cl) {
+        const int kk = 32 * i + __ffs(cl) - 1;
+        cl &= cl - 1;
         float eh, el;
         coop_exact_dist<GD>(uj, stage, kk, lane, eh, el);
         if (lane == L && (eh < bh || (eh == bh && el < bl))) {
@@ -385,6 +396,12 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
         float b1, b2;
         int k1;
         scan_half(tdist, cn_s + book * K + h * KH, KH, h * KH, b1, b2, k1);
+        // release this half of the distance buffer at once: the next step's
+        // MMA overlaps the merge and the update below (the rare refinement
+        // recomputes what it needs on CUDA cores)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->dempty[h]));
         ctl->xb1[par][h][row] = b1;
         ctl->xb2[par][h][row] = b2;
         ctl->xk1[par][h][row] = k1;
@@ -409,26 +426,19 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
         const bool need = (B2 - B1) <= 2.f * eps;
         float u[GD];
         bool have_u = false;
-        if (__any_sync(kFull, need)) {
-          if (owner) {
+        if (owner && __any_sync(kFull, need)) {
+          {
             tmem_load_group<GD>(tz + g * GD, u);
             have_u = true;
-            const float thr = B1 + 2.f * eps;
-            const int kb = refine<GD>(u, tbase + lanebase + 256, cn_s + book * K, stage,
-                                      ctl->uscr[q + 4 * h], KH, thr, need, K1, lane);
+            // band of the candidates: the MMA-coarse band plus the error of
+            // the fp32 CUDA-core dot products (32 exact products, fp32 sums)
+            const float thr =
+                B1 + 2.f * eps + 4e-6f * nu * cm + 2.4e-7f * (cm * cm + fabsf(B1));
+            const int kb = refine<GD>(u, cn_s + book * K, stage, ctl->uscr[q + 4 * h], K, thr,
+                                      need, K1, lane);
             if (need) K1 = kb;
           }
-          // the partner keeps its half until the owner has re-read it
-          if (!pair_sync(ctl, q, lane, pcnt, bud)) {
-            give_up(ctl, a.err);
-            alive = false;
-            break;
-          }
         }
-        // 3. release this half's distance buffer
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctl->dempty[h]));
         ++dcnt;
         if (!owner) continue;
         // 4. owner: record the index, update the residual, next operand

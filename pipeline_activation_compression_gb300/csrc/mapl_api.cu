@@ -504,7 +504,7 @@ HostLayout host_layout(const mapl_plan_s* pl, int64_t N) {
   const mapl_config& c = pl->cfg;
   int64_t pbytes = 0;
   payload_bytes_of(c, &pbytes);
-  HostLayout h;
+  HostLayout h{};
   h.x = 0;
   h.tids = h.x + up256(static_cast<size_t>(N) * c.d * elt_size(c));
   h.payload = h.tids + up256(static_cast<size_t>(N) * 4);
@@ -537,7 +537,7 @@ mapl_status mapl_host_workspace_size(mapl_plan pl, int64_t N, size_t* bytes) {
 mapl_status mapl_compress_host(mapl_plan pl, const void* X, const int32_t* tids, int64_t N,
                                const void* E_send, void* payload, void* ws, size_t ws_bytes,
                                cudaStream_t stream) {
-  HostLayout h;
+  HostLayout h{};
   mapl_status st = host_args(pl, N, X, tids, payload, ws, ws_bytes, &h);
   if (st != MAPL_OK) return st;
   const mapl_config& c = pl->cfg;
@@ -562,7 +562,7 @@ mapl_status mapl_compress_host(mapl_plan pl, const void* X, const int32_t* tids,
 mapl_status mapl_decompress_host(mapl_plan pl, const void* payload, const int32_t* tids,
                                  int64_t N, const void* E_recv, void* X_hat, void* ws,
                                  size_t ws_bytes, cudaStream_t stream) {
-  HostLayout h;
+  HostLayout h{};
   mapl_status st = host_args(pl, N, payload, tids, X_hat, ws, ws_bytes, &h);
   if (st != MAPL_OK) return st;
   const mapl_config& c = pl->cfg;

@@ -64,7 +64,7 @@ struct Ctl {
   float xb1[2][2][kTile];           // [item parity][half][row] best of a half
   float xb2[2][2][kTile];           // second best of a half
   int xk1[2][2][kTile];             // index of the best
-  float nu[kNSlot][2][kTile];       // ||u|| of the residual in a slot [round parity]
+  float nu[kNSlot][2][kTile];       // ||u|| of the residual in a slot [use parity]
   float uscr[8][32];                // per epilogue warp: the residual being refined
 };
 
@@ -339,7 +339,8 @@ template <int GD>
 __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uint32_t tbase,
                             uint32_t ubase, const float* cn_s, const uint8_t* cbring_p,
                             uint32_t cbsb, int tile, int zb, int q, int h, int lane,
-                            uint32_t& dcnt, uint32_t& pcnt, bool& alive) {
+                            uint32_t& dcnt, uint32_t& pcnt, uint32_t (&suse)[kNSlot],
+                            bool& alive) {
   const int row = q * 32 + lane;
   const int n = tile * kTile + row;
   const bool store = n < a.N;
@@ -364,7 +365,9 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
       tmem_load_group<GD>(tz + g * GD, u);
       const int slot = g - b0;
       const float nu = write_operand<GD>(ubase + slot * kBlockBytes, row, u);
-      ctl->nu[slot][0][row] = nu;
+      // ||u|| slots alternate with the slot's uses, so a writer never
+      // touches the one its partner warp may still be reading
+      ctl->nu[slot][suse[slot] & 1u][row] = nu;
       fence_async_shared();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl->uready[slot]));
@@ -375,6 +378,8 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
         const int book = rho * G + g;
         const bool owner = (G == 1) ? (h == 0) : ((g & 1) == h);
         const int par = static_cast<int>(dcnt & 1u);
+        const uint32_t npar = suse[slot] & 1u;   // parity of this use of the slot
+        ++suse[slot];
         // this step's codebook stage (read by the owner's refinement and
         // residual update; the owners release it at the end of the step)
         const int cs = static_cast<int>(dcnt % kCbStages);
@@ -418,7 +423,7 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
         const float B1 = take_o ? ob1 : b1;
         int K1 = take_o ? ok1 : k1;
         const float B2 = fminf(fminf(b2, ob2), fmaxf(b1, ob1));
-        const float nu = ctl->nu[slot][rho & 1][row];
+        const float nu = ctl->nu[slot][npar][row];
         const float cm = __ldg(a.cmax + book);
         // certified bound on |D~_k - D_k| (two-term split, fp32 accumulation
         // of 2*GD exact products, fp32 rounding of ||c||^2 and the fma)
@@ -458,7 +463,7 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
           }
           tmem_store_group<GD>(tz + g * GD, u);
           const float nn = write_operand<GD>(ubase + slot * kBlockBytes, row, u);
-          ctl->nu[slot][(rho + 1) & 1][row] = nn;
+          ctl->nu[slot][suse[slot] & 1u][row] = nn;
           fence_async_shared();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&ctl->uready[slot]));
@@ -767,6 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1, 8 * 32);
     }
     uint32_t dcnt = 0, pcnt = 0;
+    uint32_t suse[kNSlot] = {0u, 0u};   // uses of each residual slot so far
     bool alive = true;
     for (int it = 0; it < L && alive; ++it) {
       const int tile = blockIdx.x + it * gridDim.x;
@@ -780,8 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (vq) {
         if constexpr (GD > 0)
           epilogue_vq<GD>(a, geo, ctl, tbase, ubase, cn_s, base + nst * sb, cbsb, tile, zb, q,
-                          h, lane, dcnt, pcnt,
-                          alive);
+                          h, lane, dcnt, pcnt, suse, alive);
         const int n = tile * kTile + q * 32 + lane;
         if (alive && h == 0 && n < a.N) {
           const int t = a.tids[n];

@@ -101,6 +101,26 @@ def test_parity_small(name, n):
     print(name, rep)
 
 
+# Round counts and codebook sizes the standard workloads do not use: odd R
+# (the residual-norm slots alternate across a block boundary), one round,
+# K = 128 and K = 64 codes, 16-wide groups.  Codebook stds are synthetic.
+VARIANTS = [
+    ("vq_d1024_r128", dict(R=3, K=256, code_sigma=(0.99, 0.6, 0.35))),
+    ("vq_d1024_r128", dict(R=1, K=128, code_sigma=(0.99,))),
+    ("vq_d2048_r128", dict(R=3, K=64, code_sigma=(1.0, 0.7, 0.5))),
+]
+
+
+@pytest.mark.parametrize("name,kw", VARIANTS, ids=["R3K256", "R1K128", "G8R3K64"])
+def test_parity_vq_variants(name, kw):
+    import dataclasses
+    w = dataclasses.replace(synth.WORKLOADS[name], name=f"{name}_v", **kw)
+    b = synth.make_boundary(w, n_tokens=700)
+    plan = plan_for(w, b)
+    rep = check_outputs(w, b, *run(plan, w, b))
+    print(w, rep)
+
+
 # ------------------------------------------------------ full size, sampled rows
 @pytest.mark.parametrize("name", ["proj_d1024_r128", "vq_d1024_r128"])
 def test_parity_full_size_sampled(name):

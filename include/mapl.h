@@ -126,6 +126,37 @@ mapl_status mapl_decompress(mapl_plan plan, const void* payload, const int32_t* 
                             int64_t N, const void* E_recv, void* X_hat, cudaStream_t stream);
 
 /*
+ * Backward pass (MAPL §3.2: the gradient of the boundary activation is
+ * routed through the same orthogonal projector A; §3.5: it is what the
+ * gradient exchange compresses).  bf16 tensor-core plans only
+ * (MAPL_ERR_UNSUPPORTED otherwise).  All pointers are device pointers.
+ *
+ * mapl_grad_compress   receiver side:  gZ = gX_hat A
+ *   gX_hat  N x d  dL/dX_hat (bf16);  gZ  N x r  out (bf16, round to nearest
+ *   even).  No anchor term: the anchor does not depend on X.
+ * mapl_grad_decompress sender side:    gX = gZ A^T
+ *   gZ  N x r (bf16);  gX  N x d out (bf16) = dL/dX through the codec.
+ * mapl_grad_A          Euclidean gradient of A for SPEL:
+ *   dA = X_res^T gZ + gX_hat^T Z,  X_res = X - E_send[tids] P_send
+ *   X, gX_hat N x d; gZ, Z N x r (bf16; Z as the pipeline has it, e.g. the
+ *   decoded payload); tids N; E_send V x r;  dA  d x r fp32 out.
+ *   Computed as X^T gZ + gX_hat^T Z (two cuBLAS GEMMs, fp32 accumulation)
+ *   minus P_send^T (E_send[tids]^T gZ) (library kernels, fp32 atomics: the
+ *   last bits depend on the order of the additions).  The first call on a
+ *   plan creates its cuBLAS handle (not capturable in a CUDA graph).
+ * Async on `stream`.
+ */
+mapl_status mapl_grad_compress(mapl_plan plan, const void* gX_hat, int64_t N, void* gZ,
+                               cudaStream_t stream);
+
+mapl_status mapl_grad_decompress(mapl_plan plan, const void* gZ, int64_t N, void* gX,
+                                 cudaStream_t stream);
+
+mapl_status mapl_grad_A(mapl_plan plan, const void* X, const int32_t* tids, const void* E_send,
+                        const void* gZ, const void* gX_hat, const void* Z, int64_t N,
+                        float* dA, cudaStream_t stream);
+
+/*
  * Host-buffer forms of mapl_compress / mapl_decompress, for callers whose
  * boundary activations live in host memory.  They are not part of the MAPL
  * method; they stage the host data through a caller-owned device workspace

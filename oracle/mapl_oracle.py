@@ -12,6 +12,11 @@ Parallelism* (MAPL).  Every function names the passage it writes out:
 * anchor            -- §3.2, eq. (3): E_small[ids] P
 * compress          -- §3.2, eq. (1): Z = (X - E_small[ids] P) A
 * reconstruct       -- §3.2, eq. (2): X_hat = Z A^T + E_small_next[ids] P_next
+* grad_compress     -- §3.2 (backward pass): the boundary gradient dL/dX_hat
+                       routed through the same projector, gZ = dL/dX_hat A
+* grad_decompress   -- §3.2 (backward pass): dL/dX = gZ A^T
+* grad_A            -- Euclidean gradient of A that §3.3 feeds to SPEL, for the
+                       composed codec X_hat = (X - E[ids] P) A A^T + E'[ids] P'
 * rvq_encode/decode -- §3.5 "Composing with vector quantization" and App. E.4:
                        G groups, R rounds of residual quantisation, K codes
 * tangent_project   -- §3.3, eq. (4): g - A sym(A^T g), sym(M) = (M + M^T)/2
@@ -44,7 +49,8 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "anchor", "compress", "compress_folded", "reconstruct", "rvq_encode",
+    "anchor", "compress", "compress_folded", "reconstruct", "grad_compress",
+    "grad_decompress", "grad_A", "grad_A_given", "rvq_encode",
     "rvq_encode_given", "rvq_decode", "tangent_project", "sym", "momentum",
     "polar_express", "spel_step", "payload_bytes_per_token",
 ]
@@ -87,6 +93,39 @@ def reconstruct(Zhat, tids, A, E_next, P_next) -> np.ndarray:
     """Receiver side, eq. (2): X_hat = Z A^T + E_small_{p+1}[tids] P_{p+1}."""
     Zhat, A = _f64(Zhat), _f64(A)
     return Zhat @ A.T + anchor(E_next, P_next, tids)
+
+
+# ---------------------------------------------------------------------------
+# backward pass, §3.2 ("we symmetrically route the gradient through the same
+# orthogonal projector")
+# ---------------------------------------------------------------------------
+def grad_compress(gXhat, A) -> np.ndarray:
+    """Receiver side of the backward pass: gZ = dL/dX_hat A (N x r).  Since
+    X_hat = Z A^T + (anchor, independent of Z), dL/dZ = dL/dX_hat A."""
+    return _f64(gXhat) @ _f64(A)
+
+
+def grad_decompress(gZ, A) -> np.ndarray:
+    """Sender side: dL/dX = gZ A^T (N x d).  Z = (X - anchor) A, so
+    dL/dX = dL/dZ A^T."""
+    return _f64(gZ) @ _f64(A).T
+
+
+def grad_A_given(X, tids, E, P, gZ, gXhat, Z) -> np.ndarray:
+    """dL/dA = X_res^T gZ + gX_hat^T Z with X_res = X - E[tids] P, for given
+    gZ (the gradient of Z) and Z (d x r): the two places A appears in
+    X_hat = X_res A A^T + E'[tids] P'."""
+    Xres = _f64(X) - anchor(E, P, tids)
+    return Xres.T @ _f64(gZ) + _f64(gXhat).T @ _f64(Z)
+
+
+def grad_A(X, tids, A, E, P, gXhat) -> np.ndarray:
+    """Euclidean gradient of L = <dL/dX_hat, X_hat(A)> with respect to A for
+    X_hat = (X - E[tids] P) A A^T + E'[tids] P' (the anchor' term does not
+    involve A): X_res^T (gX_hat A) + gX_hat^T (X_res A)."""
+    Xres = _f64(X) - anchor(E, P, tids)
+    A, g = _f64(A), _f64(gXhat)
+    return Xres.T @ (g @ A) + g.T @ (Xres @ A)
 
 
 # ---------------------------------------------------------------------------

@@ -19,6 +19,7 @@ __all__ = [
     "mapl_plan_create", "mapl_plan_update_A", "mapl_payload_bytes", "mapl_compress",
     "mapl_compress_z32", "mapl_decompress", "mapl_check", "mapl_plan_destroy",
     "mapl_host_workspace_size", "mapl_compress_host", "mapl_decompress_host",
+    "mapl_grad_compress", "mapl_grad_decompress", "mapl_grad_A",
     "mapl_spel_workspace_size", "mapl_spel_step", "mapl_spel_step_static", "mapl_last_error",
     "mapl_version",
     "MAPL_F32", "MAPL_BF16", "STATUS",
@@ -73,6 +74,9 @@ def load_library():
         "mapl_decompress": [P, P, P, I64, P, P, P],
         "mapl_check": [P, P],
         "mapl_host_workspace_size": [P, I64, ctypes.POINTER(SZ)],
+        "mapl_grad_compress": [P, P, I64, P, P],
+        "mapl_grad_decompress": [P, P, I64, P, P],
+        "mapl_grad_A": [P, P, P, P, P, P, P, I64, P, P],
         "mapl_compress_host": [P, P, P, I64, P, P, P, SZ, P],
         "mapl_decompress_host": [P, P, P, I64, P, P, P, SZ, P],
         "mapl_spel_workspace_size": [I64, I64, I32, ctypes.POINTER(SZ)],
@@ -258,6 +262,35 @@ def mapl_decompress_host(plan: Plan, payload, tids, E_recv, X_hat, workspace, st
         _host_ptr(X_hat, dt, "X_hat"), _ptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return X_hat
+
+
+def mapl_grad_compress(plan: Plan, gX_hat, gZ, stream=None):
+    """gZ = gX_hat A (receiver side of the backward pass); bf16 device tensors."""
+    import torch
+    _check(load_library().mapl_grad_compress(
+        plan.handle, _ptr(gX_hat, torch.bfloat16, "gX_hat"), int(gX_hat.shape[0]),
+        _ptr(gZ, torch.bfloat16, "gZ"), _stream(stream)))
+    return gZ
+
+
+def mapl_grad_decompress(plan: Plan, gZ, gX, stream=None):
+    """gX = gZ A^T (sender side of the backward pass); bf16 device tensors."""
+    import torch
+    _check(load_library().mapl_grad_decompress(
+        plan.handle, _ptr(gZ, torch.bfloat16, "gZ"), int(gZ.shape[0]),
+        _ptr(gX, torch.bfloat16, "gX"), _stream(stream)))
+    return gX
+
+
+def mapl_grad_A(plan: Plan, X, tids, E_send, gZ, gX_hat, Z, dA, stream=None):
+    """dA = (X - E_send[tids] P_send)^T gZ + gX_hat^T Z, fp32 d x r."""
+    import torch
+    _check(load_library().mapl_grad_A(
+        plan.handle, _ptr(X, torch.bfloat16, "X"), _ptr(tids, torch.int32, "tids"),
+        _ptr(E_send, torch.bfloat16, "E_send"), _ptr(gZ, torch.bfloat16, "gZ"),
+        _ptr(gX_hat, torch.bfloat16, "gX_hat"), _ptr(Z, torch.bfloat16, "Z"),
+        int(X.shape[0]), _ptr(dA, torch.float32, "dA"), _stream(stream)))
+    return dA
 
 
 def mapl_check(plan: Plan, stream=None):

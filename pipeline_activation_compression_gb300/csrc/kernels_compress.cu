@@ -89,7 +89,7 @@ __device__ __forceinline__ Geo geometry(const CompressArgs& a, bool vq) {
   g.nkx = a.d / 64;
   g.nkr = a.r / 64;
   g.na = kNumSplit * g.nkr;
-  g.nP = g.nkx + g.na;
+  g.nP = g.nkx + (a.anchor ? g.na : 0);
   g.nV = vq ? a.G * a.R : 0;
   g.nh = a.r > 256 ? 2 : 1;
   g.nrow = a.r > 256 ? 256 : a.r;
@@ -345,7 +345,7 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
   const int n = tile * kTile + row;
   const bool store = n < a.N;
   bool bad = false;
-  if (store) {
+  if (store && a.anchor) {
     const int t = a.tids[n];
     bad = t < 0 || t >= a.V;
   }
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < kIdsPerLane; ++j) {
         const int n = tile * kTile + lane + 32 * j;
-        const int t = n < a.N ? __ldg(a.tids + n) : 0;
+        const int t = (a.anchor && n < a.N) ? __ldg(a.tids + n) : 0;
         v[j] = (t < 0 || t >= a.V) ? 0 : t;
       }
     };
@@ -797,7 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = tile * kTile + row;
         const bool store = n < a.N;
         bool bad = false;
-        if (store) {
+        if (store && a.anchor) {
           const int t = a.tids[n];
           bad = t < 0 || t >= a.V;
           if (bad && h == 0) atomicOr(a.err, kErrBadToken);

@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int NC = a.nc;                            // output chunk
   const int nchunk = d / NC;
   const int nzb = r / 64;                          // K-blocks holding Z_hat
-  const int nka = 2 * nzb;                         // K-blocks of [Z_hat | E']
+  const int nka = a.anchor ? 2 * nzb : nzb;        // K-blocks of [Z_hat | E'] (or Z_hat)
   const int nitems = nchunk * nka;
   const bool stream = a.a_stream != 0;
   const uint32_t a_slot = stream ? kBlockBytes : 0u;   // A block at stage start
@@ -255,15 +255,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int tid = threadIdx.x - 64;
     const int row = (warp & 3) * 32 + lane;
     const int n = tile * kTile + row;
-    load_tids(a.tids, a.N, a.V, tile, tid, ctl->tids, a.err);
+    if (a.anchor) {
+      load_tids(a.tids, a.N, a.V, tile, tid, ctl->tids, a.err);
+    } else {
+      for (int q = tid; q < kTile; q += kEpiThreads) ctl->tids[q] = tile * kTile + q < a.N ? 0 : -2;
+    }
     named_bar_sync(kEpiBar, kEpiThreads);
     bool alive = true;
     if (!stream) {
       if (a.vq) {
         if constexpr (GD > 0) decode_rows<GD>(a, ctl->tids, aop, row, n);
       }
-      for (int kb = 0; kb < nzb; ++kb)
-        gather_block(a.E, r, ctl->tids, kb, aop + (nzb + kb) * kBlockBytes, tid);
+      if (a.anchor)
+        for (int kb = 0; kb < nzb; ++kb)
+          gather_block(a.E, r, ctl->tids, kb, aop + (nzb + kb) * kBlockBytes, tid);
       fence_async_shared();
       named_bar_sync(kEpiBar, kEpiThreads);
       if (tid == 0) mbar_arrive(smem_u32(&ctl->aready));
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(kPtThreads, 1)
   const int NC = a.nc;
   const int nchunk = a.d / NC;
   const int nzb = a.r / 64;          // K-blocks of Z_hat (and of E')
-  const int nka = 2 * nzb;           // K-blocks of [Z_hat | E']
+  const int nka = a.anchor ? 2 * nzb : nzb;   // K-blocks of [Z_hat | E'] (or Z_hat alone)
   const int ntiles = (a.N + kTile - 1) / kTile;
   const int L = blockIdx.x < ntiles ? (ntiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
   const uint32_t tmem_cols = 2u * NC < 32u ? 32u : 2u * NC;
@@ -568,11 +573,14 @@ __global__ void __launch_bounds__(kPtThreads, 1)
       int t = 0;
       bool live = false;
       if (n < a.N) {
-        t = __ldg(a.tids + n);
-        live = t >= 0 && t < a.V;
-        if (!live) {
-          atomicOr(a.err, kErrBadToken);
-          t = 0;
+        live = true;
+        if (a.anchor) {
+          t = __ldg(a.tids + n);
+          live = t >= 0 && t < a.V;
+          if (!live) {
+            atomicOr(a.err, kErrBadToken);
+            t = 0;
+          }
         }
       }
       ctl->ids[ab][bt] = t;
@@ -580,15 +588,17 @@ __global__ void __launch_bounds__(kPtThreads, 1)
       if (bt == 0) {
         // Z_hat (non-VQ payload) and the anchor rows E'[tids] by TMA
         const uint32_t fb = smem_u32(&ctl->afull[ab]);
-        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nzb) * kBlockBytes * (a.vq ? 1u : 2u));
+        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nzb) * kBlockBytes *
+                                      ((a.vq ? 0u : 1u) + (a.anchor ? 1u : 0u)));
         if (!a.vq)
           for (int kb = 0; kb < nzb; ++kb)
             tma_load_2d(abuf + kb * kBlockBytes, &tmZ, kb * 64, tile * kTile, fb);
         const int32_t* ids = ctl->ids[ab];
-        for (int kb = 0; kb < nzb; ++kb)
-          for (int q4 = 0; q4 < kTile / 4; ++q4)
-            tma_gather4(abuf + (nzb + kb) * kBlockBytes + q4 * 512, &tmE, kb * 64, ids[4 * q4],
-                        ids[4 * q4 + 1], ids[4 * q4 + 2], ids[4 * q4 + 3], fb);
+        if (a.anchor)
+          for (int kb = 0; kb < nzb; ++kb)
+            for (int q4 = 0; q4 < kTile / 4; ++q4)
+              tma_gather4(abuf + (nzb + kb) * kBlockBytes + q4 * 512, &tmE, kb * 64, ids[4 * q4],
+                          ids[4 * q4 + 1], ids[4 * q4 + 2], ids[4 * q4 + 3], fb);
         last_ab = ab;
         last_use = ause;
       }
@@ -618,7 +628,7 @@ __global__ void __launch_bounds__(kPtThreads, 1)
       const int row0 = tile * kTile + q * 32;     // first row of this warp's box
       const bool any = row0 < a.N;
       bool bad = false;
-      if (n < a.N) {
+      if (n < a.N && a.anchor) {
         const int t = __ldg(a.tids + n);
         bad = t < 0 || t >= a.V;
       }

@@ -1,5 +1,6 @@
 // mapl_api.cu -- host side of the C ABI declared in include/mapl.h: argument
 // validation, plan memory and operand layouts, TMA descriptors, launches.
+#include <cublas_v2.h>
 #include <cudaTypedefs.h>
 
 #include <cstdarg>
@@ -29,6 +30,9 @@ struct mapl_plan_s {
   uint32_t d_stage = 0, d_smem = 0, d_abytes = 0, d_nc = 0;
   bool d_stream = false;
   int d_nab = 0;                      // > 0: persistent kernel with d_nab A buffers
+  // projector gradient: cuBLAS handle (made on first use) and r x r scratch
+  cublasHandle_t blas = nullptr;
+  float* gS = nullptr;
 };
 
 namespace {
@@ -292,6 +296,7 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   const size_t ocn = take((ncode > 0 ? ncode : 1) * 4);
   const size_t ocm = take((nb > 0 ? nb : 1) * 4);
   const size_t oerr = take(4);
+  const size_t ogS = pl->tc ? take(static_cast<size_t>(r) * r * 4) : 0;
   void* pool = nullptr;
   e = cudaMalloc(&pool, off);
   if (e != cudaSuccess) {
@@ -318,6 +323,7 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   p.cnorm = reinterpret_cast<float*>(b + ocn);
   p.cmax = reinterpret_cast<float*>(b + ocm);
   p.err = reinterpret_cast<int*>(b + oerr);
+  if (pl->tc) pl->gS = reinterpret_cast<float*>(b + ogS);
 
   e = cudaMemsetAsync(p.err, 0, 4, stream);
   if (e == cudaSuccess)
@@ -359,21 +365,27 @@ mapl_status mapl_plan_update_A(mapl_plan pl, const void* A, cudaStream_t stream)
 
 void mapl_plan_destroy(mapl_plan pl) {
   if (!pl) return;
+  if (pl->blas) cublasDestroy(pl->blas);
   if (pl->p.pool) cudaFree(pl->p.pool);
   delete pl;
 }
 
 static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* tids, int64_t N,
-                                   const void* E, void* out, int mode, cudaStream_t stream) {
+                                   const void* E, void* out, int mode, cudaStream_t stream,
+                                   bool anchor = true) {
   if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
-  if (!X || !tids || !E || !out) return fail(MAPL_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!X || !out || (anchor && (!tids || !E)))
+    return fail(MAPL_ERR_INVALID_ARG, "NULL tensor pointer");
   if (N < 1 || N > 0x7fffffffLL) return fail(MAPL_ERR_INVALID_ARG, "N must be in [1, 2^31)");
-  if (!aligned16(X) || !aligned16(E) || !aligned16(out) || (reinterpret_cast<uintptr_t>(tids) & 3u))
+  if (!aligned16(X) || !aligned16(out) ||
+      (anchor && (!aligned16(E) || (reinterpret_cast<uintptr_t>(tids) & 3u))))
     return fail(MAPL_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned (tids 4-byte)");
   mapl_status st = check_device(pl);
   if (st != MAPL_OK) return st;
   const mapl_config& c = pl->cfg;
   cudaError_t e;
+  if (!anchor && !pl->tc)
+    return fail(MAPL_ERR_UNSUPPORTED, "gradient calls need a bf16 (tensor-core) plan");
   if (!pl->tc) {
     e = launch_compress_f32(c, pl->p, reinterpret_cast<const float*>(X), tids, N,
                             reinterpret_cast<const float*>(E), out, mode, stream);
@@ -383,8 +395,12 @@ static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* t
   CUtensorMap tmX, tmE;
   if (!make_tmap(&tmX, X, c.d, static_cast<uint64_t>(N), 64, kTile))
     return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (X)");
-  if (!make_tmap(&tmE, E, c.r, static_cast<uint64_t>(c.V), 64, 1))
-    return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (E)");
+  if (anchor) {
+    if (!make_tmap(&tmE, E, c.r, static_cast<uint64_t>(c.V), 64, 1))
+      return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (E)");
+  } else {
+    tmE = tmX;   // unused
+  }
   CompressArgs a{};
   a.tids = tids;
   a.E = reinterpret_cast<const __nv_bfloat16*>(E);
@@ -402,6 +418,7 @@ static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* t
   a.K = c.K;
   a.gd = pl->gd;
   a.mode = mode;
+  a.anchor = anchor ? 1 : 0;
   a.nstage = pl->c_nstage;
   a.stage_bytes = pl->c_stage;
   a.timeout_ns = pl->timeout_ns;
@@ -424,18 +441,25 @@ mapl_status mapl_compress_z32(mapl_plan pl, const void* X, const int32_t* tids, 
   return compress_common(pl, X, tids, N, E_send, Z, kModeZ32, stream);
 }
 
-mapl_status mapl_decompress(mapl_plan pl, const void* payload, const int32_t* tids, int64_t N,
-                            const void* E_recv, void* X_hat, cudaStream_t stream) {
+// anchor == false: the payload is a bf16 N x r tensor (never VQ indices) and
+// the E' term is left out (backward pass, dX = gZ A^T).
+static mapl_status decompress_common(mapl_plan pl, const void* payload, const int32_t* tids,
+                                     int64_t N, const void* E_recv, void* X_hat,
+                                     cudaStream_t stream, bool anchor) {
   if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
-  if (!payload || !tids || !E_recv || !X_hat) return fail(MAPL_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!payload || !X_hat || (anchor && (!tids || !E_recv)))
+    return fail(MAPL_ERR_INVALID_ARG, "NULL tensor pointer");
   if (N < 1 || N > 0x7fffffffLL) return fail(MAPL_ERR_INVALID_ARG, "N must be in [1, 2^31)");
-  if (!aligned16(payload) || !aligned16(E_recv) || !aligned16(X_hat) ||
-      (reinterpret_cast<uintptr_t>(tids) & 3u))
+  if (!aligned16(payload) || !aligned16(X_hat) ||
+      (anchor && (!aligned16(E_recv) || (reinterpret_cast<uintptr_t>(tids) & 3u))))
     return fail(MAPL_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned (tids 4-byte)");
   mapl_status st = check_device(pl);
   if (st != MAPL_OK) return st;
   const mapl_config& c = pl->cfg;
   cudaError_t e;
+  if (!anchor && !pl->tc)
+    return fail(MAPL_ERR_UNSUPPORTED, "gradient calls need a bf16 (tensor-core) plan");
+  const bool vq = anchor && pl->vq;
   if (!pl->tc) {
     e = launch_decompress_f32(c, pl->p, payload, tids, N, reinterpret_cast<const float*>(E_recv),
                               reinterpret_cast<float*>(X_hat), stream);
@@ -443,7 +467,7 @@ mapl_status mapl_decompress(mapl_plan pl, const void* payload, const int32_t* ti
     return MAPL_OK;
   }
   CUtensorMap tmZ;
-  if (!pl->vq) {
+  if (!vq) {
     if (!make_tmap(&tmZ, payload, c.r, static_cast<uint64_t>(N), 64, kTile))
       return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (Z)");
   } else {
@@ -453,7 +477,7 @@ mapl_status mapl_decompress(mapl_plan pl, const void* payload, const int32_t* ti
   a.tids = tids;
   a.E = reinterpret_cast<const __nv_bfloat16*>(E_recv);
   a.Cb = pl->p.Cb;
-  a.idx = pl->vq ? reinterpret_cast<const uint8_t*>(payload) : nullptr;
+  a.idx = vq ? reinterpret_cast<const uint8_t*>(payload) : nullptr;
   a.Xh = reinterpret_cast<__nv_bfloat16*>(X_hat);
   a.err = pl->p.err;
   a.N = static_cast<int>(N);
@@ -464,7 +488,8 @@ mapl_status mapl_decompress(mapl_plan pl, const void* payload, const int32_t* ti
   a.R = c.R;
   a.K = c.K;
   a.gd = pl->gd;
-  a.vq = pl->vq ? 1 : 0;
+  a.vq = vq ? 1 : 0;
+  a.anchor = anchor ? 1 : 0;
   a.a_stream = pl->d_stream ? 1 : 0;
   a.nc = static_cast<int>(pl->d_nc);
   a.nab = pl->d_nab;
@@ -474,8 +499,8 @@ mapl_status mapl_decompress(mapl_plan pl, const void* payload, const int32_t* ti
   a.timeout_ns = pl->timeout_ns;
   const int ntiles = static_cast<int>((N + kTile - 1) / kTile);
   if (pl->d_nab > 0) {
-    CUtensorMap tmE;
-    if (!make_tmap(&tmE, E_recv, c.r, static_cast<uint64_t>(c.V), 64, 1))
+    CUtensorMap tmE = tmZ;   // unused without the anchor
+    if (anchor && !make_tmap(&tmE, E_recv, c.r, static_cast<uint64_t>(c.V), 64, 1))
       return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (E')");
     CUtensorMap tmXh;
     if (!make_tmap(&tmXh, X_hat, c.d, static_cast<uint64_t>(N), 64, 32))
@@ -486,6 +511,63 @@ mapl_status mapl_decompress(mapl_plan pl, const void* payload, const int32_t* ti
     e = launch_decompress_tc(pl->tmB, tmZ, a, pl->d_smem, ntiles, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "decompress launch");
+  return MAPL_OK;
+}
+
+mapl_status mapl_decompress(mapl_plan pl, const void* payload, const int32_t* tids, int64_t N,
+                            const void* E_recv, void* X_hat, cudaStream_t stream) {
+  return decompress_common(pl, payload, tids, N, E_recv, X_hat, stream, true);
+}
+
+// ------------------------------------------------------------ backward pass
+mapl_status mapl_grad_compress(mapl_plan pl, const void* gX_hat, int64_t N, void* gZ,
+                               cudaStream_t stream) {
+  return compress_common(pl, gX_hat, nullptr, N, nullptr, gZ, kModeZ16, stream, false);
+}
+
+mapl_status mapl_grad_decompress(mapl_plan pl, const void* gZ, int64_t N, void* gX,
+                                 cudaStream_t stream) {
+  return decompress_common(pl, gZ, nullptr, N, nullptr, gX, stream, false);
+}
+
+mapl_status mapl_grad_A(mapl_plan pl, const void* X, const int32_t* tids, const void* E_send,
+                        const void* gZ, const void* gX_hat, const void* Z, int64_t N, float* dA,
+                        cudaStream_t stream) {
+  if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
+  if (!X || !tids || !E_send || !gZ || !gX_hat || !Z || !dA)
+    return fail(MAPL_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (N < 1 || N > 0x7fffffffLL) return fail(MAPL_ERR_INVALID_ARG, "N must be in [1, 2^31)");
+  if (!pl->tc) return fail(MAPL_ERR_UNSUPPORTED, "gradient calls need a bf16 (tensor-core) plan");
+  mapl_status st = check_device(pl);
+  if (st != MAPL_OK) return st;
+  const mapl_config& c = pl->cfg;
+  if (!pl->blas) {
+    if (cublasCreate(&pl->blas) != CUBLAS_STATUS_SUCCESS) {
+      pl->blas = nullptr;
+      return fail(MAPL_ERR_CUDA, "cublasCreate failed");
+    }
+  }
+  if (cublasSetStream(pl->blas, stream) != CUBLAS_STATUS_SUCCESS)
+    return fail(MAPL_ERR_CUDA, "cublasSetStream failed");
+  // Row-major dA (d x r) is column-major r x d:  dA^T = gZ^T X + Z^T gX_hat,
+  // i.e. C(r x d) = gZ_cm (r x N) * X_cm^T (N x d) with the row-major
+  // tensors read as column-major r x N and d x N.
+  const int m = static_cast<int>(c.r), n = static_cast<int>(c.d), k = static_cast<int>(N);
+  const float one = 1.f, zero = 0.f;
+  cublasStatus_t bs = cublasGemmEx(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, n, k, &one, gZ,
+                                   CUDA_R_16BF, m, X, CUDA_R_16BF, n, &zero, dA, CUDA_R_32F, m,
+                                   CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+  if (bs == CUBLAS_STATUS_SUCCESS)
+    bs = cublasGemmEx(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, n, k, &one, Z, CUDA_R_16BF, m,
+                      gX_hat, CUDA_R_16BF, n, &one, dA, CUDA_R_32F, m, CUBLAS_COMPUTE_32F,
+                      CUBLAS_GEMM_DEFAULT);
+  if (bs != CUBLAS_STATUS_SUCCESS) return fail(MAPL_ERR_CUDA, "cublasGemmEx failed (%d)", (int)bs);
+  cudaError_t e = launch_anchor_grad(tids, reinterpret_cast<const __nv_bfloat16*>(E_send),
+                                     reinterpret_cast<const __nv_bfloat16*>(gZ),
+                                     reinterpret_cast<const __nv_bfloat16*>(pl->p.Ps),
+                                     static_cast<int>(N), n, m, static_cast<int>(c.V),
+                                     pl->num_sms, pl->gS, dA, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "projector gradient launch");
   return MAPL_OK;
 }
 

@@ -54,6 +54,7 @@ struct CompressArgs {
   int* err;
   int N, d, r, V, G, R, K, gd;
   int mode;
+  int anchor;                       // 0: no anchor term (backward pass: gZ = dX_hat A)
   int nstage;
   uint32_t stage_bytes;
   uint64_t timeout_ns;
@@ -71,6 +72,7 @@ struct DecompressArgs {
   int a_stream;                     // A operand streamed per stage (r > 256)
   int nc;                           // output columns per accumulator chunk
   int nab;                          // A operand buffers (persistent kernel)
+  int anchor;                       // 0: no E' term (backward pass: dX = gZ A^T)
   int nstage;
   uint32_t stage_bytes;
   uint32_t a_bytes;                 // resident A operand bytes (0 when streamed)
@@ -95,6 +97,11 @@ cudaError_t launch_decompress_pt(const CUtensorMap& tmB, const CUtensorMap& tmZ,
                                  const CUtensorMap& tmE, const CUtensorMap& tmXh,
                                  const DecompressArgs& a, uint32_t smem_bytes, int grid,
                                  cudaStream_t s);
+// Anchor correction of the projector gradient: dA -= P^T (E[tids]^T gZ);
+// S is r x r fp32 scratch.
+cudaError_t launch_anchor_grad(const int32_t* tids, const __nv_bfloat16* E,
+                               const __nv_bfloat16* gZ, const __nv_bfloat16* P, int N, int d,
+                               int r, int V, int num_sms, float* S, float* dA, cudaStream_t s);
 cudaError_t launch_decompress_tc(const CUtensorMap& tmB, const CUtensorMap& tmZ,
                                  const DecompressArgs& a, uint32_t smem_bytes, int grid,
                                  cudaStream_t s);

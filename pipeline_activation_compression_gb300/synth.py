@@ -227,6 +227,18 @@ def make_boundary(w: Workload | str, seed: int = 0, n_tokens: int | None = None)
     return out
 
 
+def make_boundary_grad(w: Workload | str, seed: int = 0, n_tokens: int | None = None,
+                       scale: float = 0.01) -> np.ndarray:
+    """Gradient arriving at the boundary in the backward pass, dL/dX_hat
+    (N x d, storage dtype): scale * N(0, 1), from its own seeded stream
+    (independent of make_boundary's tensors for the same seed)."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    n = w.N if n_tokens is None else int(n_tokens)
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 7, 1]).spawn(1)[0]))
+    return _store(scale * rng.standard_normal((n, w.d)), w.dtype)
+
+
 def make_spel(w: SpelWorkload | str, seed: int = 0) -> dict:
     """Initial projectors (batch x d x r, on St(d,r)) and zero momentum, fp32."""
     if isinstance(w, str):

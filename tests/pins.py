@@ -327,6 +327,51 @@ def pin_spel_drift(o, steps=200):
     assert np.max(np.abs(A.T @ A - np.eye(r))) < 1e-10
 
 
+# ------------------------------------------------------------ §3.2 backward
+def _codec_loss(o, X, t, A, E, P, E2, P2, W):
+    """L = <W, X_hat> for the composed codec, a scalar function of X and A."""
+    Xh = o.reconstruct(o.compress(X, t, A, E, P), t, A, E2, P2)
+    return float(np.sum(W * Xh))
+
+
+def pin_grad_finite_differences(o):
+    """The backward pass is the derivative of the forward codec: central
+    differences of L = <W, X_hat(X, A)> (quadratic in A, linear in X, so
+    the central difference is exact up to rounding) must equal
+    dL/dX = grad_decompress(grad_compress(W)) and dL/dA = grad_A; and
+    grad_A_given with gZ = W A, Z = compress(...) must agree with grad_A."""
+    rng = np.random.default_rng(31)
+    d, r, V, n = 7, 3, 5, 6
+    A = _orth(rng, d, r)
+    P, P2 = _orth(rng, d, r).T, _orth(rng, d, r).T
+    E, E2 = rng.standard_normal((V, r)), rng.standard_normal((V, r))
+    X, W = rng.standard_normal((n, d)), rng.standard_normal((n, d))
+    t = rng.integers(0, V, n)
+    h = 1e-4
+    gX = np.zeros_like(X)
+    for i in range(n):
+        for j in range(d):
+            Xp, Xm = X.copy(), X.copy()
+            Xp[i, j] += h
+            Xm[i, j] -= h
+            gX[i, j] = (_codec_loss(o, Xp, t, A, E, P, E2, P2, W) -
+                        _codec_loss(o, Xm, t, A, E, P, E2, P2, W)) / (2 * h)
+    got = o.grad_decompress(o.grad_compress(W, A), A)
+    assert np.max(np.abs(got - gX)) < 1e-8 * max(1.0, np.max(np.abs(gX)))
+    gA = np.zeros_like(A)
+    for i in range(d):
+        for j in range(r):
+            Ap, Am = A.copy(), A.copy()
+            Ap[i, j] += h
+            Am[i, j] -= h
+            gA[i, j] = (_codec_loss(o, X, t, Ap, E, P, E2, P2, W) -
+                        _codec_loss(o, X, t, Am, E, P, E2, P2, W)) / (2 * h)
+    got = o.grad_A(X, t, A, E, P, W)
+    assert np.max(np.abs(got - gA)) < 1e-7 * max(1.0, np.max(np.abs(gA)))
+    given = o.grad_A_given(X, t, E, P, W @ A, W, o.compress(X, t, A, E, P))
+    assert np.max(np.abs(given - gA)) < 1e-7 * max(1.0, np.max(np.abs(gA)))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

@@ -34,6 +34,10 @@ MUTANTS = {
     "spel_step_sign": ("A_new = polar_express(_f64(A) - lr * d, coeffs_retr)", "A_new = polar_express(_f64(A) + lr * d, coeffs_retr)"),
     "spel_no_retraction": ("A_new = polar_express(_f64(A) - lr * d, coeffs_retr)", "A_new = _f64(A) - lr * d"),
     "spel_raw_gradient": ("m_new = momentum(m, gR, beta)", "m_new = momentum(m, g, beta)"),
+    "gradA_term_dropped": ("return Xres.T @ (g @ A) + g.T @ (Xres @ A)", "return Xres.T @ (g @ A)"),
+    "gradA_no_anchor": ("    Xres = _f64(X) - anchor(E, P, tids)\n    A, g = _f64(A), _f64(gXhat)", "    Xres = _f64(X)\n    A, g = _f64(A), _f64(gXhat)"),
+    "gradA_given_raw_X": ("    return Xres.T @ _f64(gZ) + _f64(gXhat).T @ _f64(Z)", "    return _f64(X).T @ _f64(gZ) + _f64(gXhat).T @ _f64(Z)"),
+    "grad_decompress_no_T": ("return _f64(gZ) @ _f64(A).T", "return _f64(gZ) @ _f64(A).T * 2.0"),
 }
 
 

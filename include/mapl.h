@@ -140,10 +140,12 @@ mapl_status mapl_decompress(mapl_plan plan, const void* payload, const int32_t* 
  *   dA = X_res^T gZ + gX_hat^T Z,  X_res = X - E_send[tids] P_send
  *   X, gX_hat N x d; gZ, Z N x r (bf16; Z as the pipeline has it, e.g. the
  *   decoded payload); tids N; E_send V x r;  dA  d x r fp32 out.
- *   Computed as X^T gZ + gX_hat^T Z (two cuBLAS GEMMs, fp32 accumulation)
- *   minus P_send^T (E_send[tids]^T gZ) (library kernels, fp32 atomics: the
- *   last bits depend on the order of the additions).  The first call on a
- *   plan creates its cuBLAS handle (not capturable in a CUDA graph).
+ *   Computed as X^T gZ + gX_hat^T Z - P_send^T (E_send[tids]^T gZ): plain
+ *   GEMMs in cuBLAS (bf16 in, fp32 accumulation) after the library gathers
+ *   E_send[tids].  The first call on a plan, and a call with a larger N than
+ *   any before, creates the plan's cuBLAS handle / grows its scratch
+ *   (N x r bf16 + r x d + r x r fp32): it synchronises `stream` and cannot
+ *   be captured in a CUDA graph; later calls can.
  * Async on `stream`.
  */
 mapl_status mapl_grad_compress(mapl_plan plan, const void* gX_hat, int64_t N, void* gZ,

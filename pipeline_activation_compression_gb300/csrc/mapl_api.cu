@@ -30,9 +30,11 @@ struct mapl_plan_s {
   uint32_t d_stage = 0, d_smem = 0, d_abytes = 0, d_nc = 0;
   bool d_stream = false;
   int d_nab = 0;                      // > 0: persistent kernel with d_nab A buffers
-  // projector gradient: cuBLAS handle (made on first use) and r x r scratch
+  // projector gradient: cuBLAS handle and scratch, made on first use:
+  // [P_send as fp32, r x d | S^T, r x r fp32 | E[tids], g_rows x r bf16]
   cublasHandle_t blas = nullptr;
-  float* gS = nullptr;
+  void* gws = nullptr;
+  int64_t g_rows = 0;
 };
 
 namespace {
@@ -296,7 +298,6 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   const size_t ocn = take((ncode > 0 ? ncode : 1) * 4);
   const size_t ocm = take((nb > 0 ? nb : 1) * 4);
   const size_t oerr = take(4);
-  const size_t ogS = pl->tc ? take(static_cast<size_t>(r) * r * 4) : 0;
   void* pool = nullptr;
   e = cudaMalloc(&pool, off);
   if (e != cudaSuccess) {
@@ -323,7 +324,6 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   p.cnorm = reinterpret_cast<float*>(b + ocn);
   p.cmax = reinterpret_cast<float*>(b + ocm);
   p.err = reinterpret_cast<int*>(b + oerr);
-  if (pl->tc) pl->gS = reinterpret_cast<float*>(b + ogS);
 
   e = cudaMemsetAsync(p.err, 0, 4, stream);
   if (e == cudaSuccess)
@@ -366,6 +366,7 @@ mapl_status mapl_plan_update_A(mapl_plan pl, const void* A, cudaStream_t stream)
 void mapl_plan_destroy(mapl_plan pl) {
   if (!pl) return;
   if (pl->blas) cublasDestroy(pl->blas);
+  if (pl->gws) cudaFree(pl->gws);
   if (pl->p.pool) cudaFree(pl->p.pool);
   delete pl;
 }
@@ -538,22 +539,48 @@ mapl_status mapl_grad_A(mapl_plan pl, const void* X, const int32_t* tids, const 
     return fail(MAPL_ERR_INVALID_ARG, "NULL tensor pointer");
   if (N < 1 || N > 0x7fffffffLL) return fail(MAPL_ERR_INVALID_ARG, "N must be in [1, 2^31)");
   if (!pl->tc) return fail(MAPL_ERR_UNSUPPORTED, "gradient calls need a bf16 (tensor-core) plan");
+  if (!aligned16(E_send)) return fail(MAPL_ERR_INVALID_ARG, "E_send must be 16-byte aligned");
   mapl_status st = check_device(pl);
   if (st != MAPL_OK) return st;
   const mapl_config& c = pl->cfg;
+  const size_t r = static_cast<size_t>(c.r), d = static_cast<size_t>(c.d);
+  const size_t oP = 0, oT = up256(r * d * 4), oEg = oT + up256(r * r * 4);
+  cudaError_t e;
   if (!pl->blas) {
     if (cublasCreate(&pl->blas) != CUBLAS_STATUS_SUCCESS) {
       pl->blas = nullptr;
       return fail(MAPL_ERR_CUDA, "cublasCreate failed");
     }
   }
+  if (!pl->gws || pl->g_rows < N) {
+    // scratch sized for N rows of E[tids]; P_send is widened once per buffer
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    if (pl->gws) cudaFree(pl->gws);
+    pl->gws = nullptr;
+    pl->g_rows = 0;
+    e = cudaMalloc(&pl->gws, oEg + up256(static_cast<size_t>(N) * r * 2));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(gradient scratch)");
+    pl->g_rows = N;
+    e = launch_widen(reinterpret_cast<const __nv_bfloat16*>(pl->p.Ps), r * d,
+                     reinterpret_cast<float*>(static_cast<char*>(pl->gws) + oP), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "widen P_send");
+  }
+  char* ws = static_cast<char*>(pl->gws);
+  float* P32 = reinterpret_cast<float*>(ws + oP);
+  float* T = reinterpret_cast<float*>(ws + oT);
+  __nv_bfloat16* Eg = reinterpret_cast<__nv_bfloat16*>(ws + oEg);
+  e = launch_gather_rows(tids, reinterpret_cast<const __nv_bfloat16*>(E_send),
+                         static_cast<int>(N), static_cast<int>(c.V), static_cast<int>(r), Eg,
+                         stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gather E[tids]");
   if (cublasSetStream(pl->blas, stream) != CUBLAS_STATUS_SUCCESS)
     return fail(MAPL_ERR_CUDA, "cublasSetStream failed");
-  // Row-major dA (d x r) is column-major r x d:  dA^T = gZ^T X + Z^T gX_hat,
-  // i.e. C(r x d) = gZ_cm (r x N) * X_cm^T (N x d) with the row-major
-  // tensors read as column-major r x N and d x N.
-  const int m = static_cast<int>(c.r), n = static_cast<int>(c.d), k = static_cast<int>(N);
-  const float one = 1.f, zero = 0.f;
+  // Everything column-major (the row-major tensors read transposed):
+  //   dA^T (r x d)  = gZ^T X + Z^T gX_hat - (E[tids]^T gZ)^T P
+  //   T = S^T (r x r) = gZ^T E[tids]
+  const int m = static_cast<int>(r), n = static_cast<int>(d), k = static_cast<int>(N);
+  const float one = 1.f, zero = 0.f, minus = -1.f;
   cublasStatus_t bs = cublasGemmEx(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, n, k, &one, gZ,
                                    CUDA_R_16BF, m, X, CUDA_R_16BF, n, &zero, dA, CUDA_R_32F, m,
                                    CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
@@ -561,13 +588,15 @@ mapl_status mapl_grad_A(mapl_plan pl, const void* X, const int32_t* tids, const 
     bs = cublasGemmEx(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, n, k, &one, Z, CUDA_R_16BF, m,
                       gX_hat, CUDA_R_16BF, n, &one, dA, CUDA_R_32F, m, CUBLAS_COMPUTE_32F,
                       CUBLAS_GEMM_DEFAULT);
-  if (bs != CUBLAS_STATUS_SUCCESS) return fail(MAPL_ERR_CUDA, "cublasGemmEx failed (%d)", (int)bs);
-  cudaError_t e = launch_anchor_grad(tids, reinterpret_cast<const __nv_bfloat16*>(E_send),
-                                     reinterpret_cast<const __nv_bfloat16*>(gZ),
-                                     reinterpret_cast<const __nv_bfloat16*>(pl->p.Ps),
-                                     static_cast<int>(N), n, m, static_cast<int>(c.V),
-                                     pl->num_sms, pl->gS, dA, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "projector gradient launch");
+  if (bs == CUBLAS_STATUS_SUCCESS)
+    bs = cublasGemmEx(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, m, k, &one, gZ, CUDA_R_16BF, m, Eg,
+                      CUDA_R_16BF, m, &zero, T, CUDA_R_32F, m, CUBLAS_COMPUTE_32F,
+                      CUBLAS_GEMM_DEFAULT);
+  // dA^T -= T P, with P (r x d row-major) read as the column-major d x r P^T
+  if (bs == CUBLAS_STATUS_SUCCESS)
+    bs = cublasSgemm(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, n, m, &minus, T, m, P32, n, &one, dA,
+                     m);
+  if (bs != CUBLAS_STATUS_SUCCESS) return fail(MAPL_ERR_CUDA, "cuBLAS GEMM failed (%d)", (int)bs);
   return MAPL_OK;
 }
 

@@ -97,11 +97,11 @@ cudaError_t launch_decompress_pt(const CUtensorMap& tmB, const CUtensorMap& tmZ,
                                  const CUtensorMap& tmE, const CUtensorMap& tmXh,
                                  const DecompressArgs& a, uint32_t smem_bytes, int grid,
                                  cudaStream_t s);
-// Anchor correction of the projector gradient: dA -= P^T (E[tids]^T gZ);
-// S is r x r fp32 scratch.
-cudaError_t launch_anchor_grad(const int32_t* tids, const __nv_bfloat16* E,
-                               const __nv_bfloat16* gZ, const __nv_bfloat16* P, int N, int d,
-                               int r, int V, int num_sms, float* S, float* dA, cudaStream_t s);
+// Projector-gradient helpers: Eg[n] = E[tids[n]] (N x r), and a bf16 -> fp32
+// copy.
+cudaError_t launch_gather_rows(const int32_t* tids, const __nv_bfloat16* E, int N, int V, int r,
+                               __nv_bfloat16* Eg, cudaStream_t s);
+cudaError_t launch_widen(const __nv_bfloat16* a, size_t n, float* b, cudaStream_t s);
 cudaError_t launch_decompress_tc(const CUtensorMap& tmB, const CUtensorMap& tmZ,
                                  const DecompressArgs& a, uint32_t smem_bytes, int grid,
                                  cudaStream_t s);

@@ -353,6 +353,72 @@ def run_ours(args, ws, rank):
     tokens = N * K * ws
     value = tokens / (total_ms * 1e-3)
 
+    # backward pass (gradient through the same projector, and dL/dA), timed
+    # apart from the forward step: one call each per iteration, CUDA events
+    gxh = to_dev(synth.make_boundary_grad(w, n_tokens=N))
+    gZ = torch.empty(N, w.r, dtype=torch.bfloat16, device="cuda")
+    gX = torch.empty(N, w.d, dtype=torch.bfloat16, device="cuda")
+    Zb = torch.empty(N, w.r, dtype=torch.bfloat16, device="cuda")
+    dA = torch.empty(w.d, w.r, dtype=torch.float32, device="cuda")
+    bw_calls = [
+        ("grad_compress_us", lambda: mapl.mapl_grad_compress(plan, gxh, gZ, stream)),
+        ("grad_decompress_us", lambda: mapl.mapl_grad_decompress(plan, gZ, gX, stream)),
+        ("grad_A_us", lambda: mapl.mapl_grad_A(plan, x0, t, E, gZ, gxh, Zb, dA, stream)),
+    ]
+    backward = {}
+    for key, fn in bw_calls:
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nb = 200
+        b0.record(stream)
+        for _ in range(nb):
+            fn()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        backward[key] = b0.elapsed_time(b1) / nb * 1e3
+    mapl.mapl_check(plan)
+
+    # SPEL projector update (batch of 3 boundaries, St(1024, 256) and
+    # St(2048, 256), fp32) and the plan refresh after an A update
+    from pipeline_activation_compression_gb300 import polar
+    spel = {}
+    co = polar.default_coeffs(5, 5)
+    for sname in ("spel_d1024_r256", "spel_d2048_r256"):
+        sw = synth.SPEL_WORKLOADS[sname]
+        sp = synth.make_spel(sw)
+        As = torch.from_numpy(sp["A"]).cuda()
+        ms = torch.zeros_like(As)
+        Gs = torch.from_numpy(next(synth.spel_gradients(sw))).cuda()
+        wsp_s = torch.empty(mapl.mapl_spel_workspace_size(sw.d, sw.r, sw.batch) // 4 + 64,
+                            dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            mapl.mapl_spel_step(As, Gs, ms, sw.lr, sw.beta, co, 5, 5, wsp_s, stream)
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ns = 50
+        s0.record(stream)
+        for _ in range(ns):
+            mapl.mapl_spel_step(As, Gs, ms, sw.lr, sw.beta, co, 5, 5, wsp_s, stream)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        spel[sname + "_us"] = s0.elapsed_time(s1) / ns * 1e3
+    A_dev = to_dev(b["A"])
+    for _ in range(3):
+        mapl.mapl_plan_update_A(plan, A_dev, stream)
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(20):
+        mapl.mapl_plan_update_A(plan, A_dev, stream)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    spel["plan_update_A_us"] = s0.elapsed_time(s1) / 20 * 1e3
+    spel["note"] = ("one SPEL step for a batch of 3 boundaries (5 LMO + 5 retraction "
+                    "PolarExpress iterations, fp32); plan refresh after an A update")
+    mapl.mapl_check(plan)
+
     # CPU baseline: the oracle as it stands, bounded sample
     cps, done, el = (0.0, 0, 0.0) if args.skip_cpu else time_oracle(b, w, min(1024, N), 10.0)
     res = {
@@ -380,6 +446,9 @@ def run_ours(args, ws, rank):
                                           + pay_h[0].numel() * pay_h[0].element_size()),
                 "api": "mapl_compress_host + mapl_decompress_host, steps rotating "
                        "over four streams"},
+        "backward": dict(backward, note="gZ = dL/dX_hat A, dL/dX = gZ A^T, dL/dA; same "
+                         "workload, 200 calls each, inputs L2-warm"),
+        "spel": spel,
         "cuda_graph": {"value": N * ws / (graph_ms * 1e-3), "unit": UNIT,
                        "ms_per_step": graph_ms, "steps": reps * nsets,
                        "note": "compress + decompress captured once per buffer set, replayed"},

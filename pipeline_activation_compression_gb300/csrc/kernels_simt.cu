@@ -2,11 +2,12 @@
 //
 // Plan preparation (once per projector update, MAPL §3.3 "send the updated
 // A_p ... after every optimizer step"):
-//   M = P_send A (r x r) accumulated in fp64; for the bf16 tensor-core path
-//   -M is split into three bf16 terms hi + mid + lo (about 24 significant
-//   bits), stored transposed as K-major B operands; A^T and [A | P_recv^T]
-//   are laid out as K-major B operands; codebook rows are padded to 64
-//   elements and their squared norms and per-book maximum norm computed.
+//   M = P_send A (r x r) in compensated fp32 (exact products by fma split,
+//   sums kept as unevaluated pairs, about 48 significant bits); for the bf16
+//   tensor-core path -M is split into three bf16 terms hi + mid + lo (about
+//   24 significant bits), stored transposed as K-major B operands; A^T and
+//   [A | P_recv^T] are laid out as K-major B operands; codebook squared norms
+//   and per-book maximum norm are computed.
 //
 // fp32 path (plan dtype MAPL_F32): one warp per token.
 //   compress:   z = x A - E[t] M, then residual VQ with exact fp32 distances
@@ -24,22 +25,77 @@ __device__ __forceinline__ double ld_f64(const void* p, size_t i, bool bf) {
 }
 
 // ------------------------------------------------------------------ prep
-__global__ void k_prep_M(const void* Ps, const void* A, int d, int r, bool bf,
-                         __nv_bfloat16* Mts, float* M32) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= r * r) return;
-  const int i = idx / r, j = idx % r;   // M[i][j] = sum_k P_send[i][k] A[k][j]
-  double acc = 0.0;
-  for (int k = 0; k < d; ++k)
-    acc = fma(ld_f64(Ps, static_cast<size_t>(i) * d + k, bf),
-              ld_f64(A, static_cast<size_t>(k) * r + j, bf), acc);
-  if (M32) M32[idx] = static_cast<float>(acc);
+__device__ __forceinline__ float ld_f32(const void* p, size_t i, bool bf) {
+  return bf ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i])
+            : reinterpret_cast<const float*>(p)[i];
+}
+
+__device__ __forceinline__ void two_sum_f(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// M[i][j] = sum_k P_send[i][k] A[k][j].  One block (8 warps) per row i and
+// 32 columns (lane = column, reads of A coalesced, P broadcast); warp w sums
+// k in its eighth of [0, d) with four independent compensated sums (k mod 4),
+// each term an exact product split by fma; the pairs are combined in shared
+// memory.
+__global__ void __launch_bounds__(256) k_prep_M(const void* Ps, const void* A, int d, int r,
+                                                bool bf, __nv_bfloat16* Mts, float* M32) {
+  __shared__ float ph[8][32], pl[8][32];
+  const int nj = (r + 31) / 32;
+  const int i = blockIdx.x / nj, j = (blockIdx.x % nj) * 32 + (threadIdx.x & 31);
+  const int w = threadIdx.x >> 5;
+  const int kc = (d + 7) / 8, kb = w * kc, ke = min(d, kb + kc);
+  float h[4] = {0.f, 0.f, 0.f, 0.f}, l[4] = {0.f, 0.f, 0.f, 0.f};
+  if (j < r) {
+    for (int k0 = kb; k0 < ke; k0 += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = k0 + u;
+        if (k < ke) {
+          const float a = ld_f32(Ps, static_cast<size_t>(i) * d + k, bf);
+          const float b = ld_f32(A, static_cast<size_t>(k) * r + j, bf);
+          const float p = a * b, pe = fmaf(a, b, -p);
+          float t, te;
+          two_sum_f(h[u], p, t, te);
+          h[u] = t;
+          l[u] += te + pe;
+        }
+      }
+    }
+  }
+  float s01, e01, s23, e23, hi, e;
+  two_sum_f(h[0], h[1], s01, e01);
+  two_sum_f(h[2], h[3], s23, e23);
+  two_sum_f(s01, s23, hi, e);
+  ph[w][threadIdx.x & 31] = hi;
+  pl[w][threadIdx.x & 31] = (l[0] + l[1]) + (l[2] + l[3]) + (e01 + e23) + e;
+  __syncthreads();
+  if (w != 0 || j >= r) return;
+  const int c = threadIdx.x & 31;
+  hi = ph[0][c];
+  float lo = pl[0][c];
+  for (int x = 1; x < 8; ++x) {
+    float t, te;
+    two_sum_f(hi, ph[x][c], t, te);
+    hi = t;
+    lo += pl[x][c] + te;
+  }
+  two_sum_f(hi, lo, hi, lo);
+  const int idx = i * r + j;
+  if (M32) M32[idx] = hi + lo;
   if (Mts) {
-    double v = -acc;
+    // -M as hi + mid + lo bf16 terms; the remainder stays a pair
+    float vh = -hi, vl = -lo;
     for (int s = 0; s < kNumSplit; ++s) {
-      const __nv_bfloat16 h = __double2bfloat16(v);
-      Mts[(static_cast<size_t>(s) * r + j) * r + i] = h;
-      v -= static_cast<double>(__bfloat162float(h));
+      const __nv_bfloat16 b = __float2bfloat16_rn(vh);
+      Mts[(static_cast<size_t>(s) * r + j) * r + i] = b;
+      float t, te;
+      two_sum_f(vh - __bfloat162float(b), vl, t, te);
+      vh = t;
+      vl = te;
     }
   }
 }
@@ -215,8 +271,7 @@ cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps
   const int T = 256;
   k_prep_At<<<blocks_for(static_cast<size_t>(d) * r, T), T, 0, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(A), d, r, p.At);
-  k_prep_M<<<blocks_for(static_cast<size_t>(r) * r, T), T, 0, s>>>(Ps, A, d, r, true, p.Mts,
-                                                                     nullptr);
+  k_prep_M<<<r * ((r + 31) / 32), 256, 0, s>>>(Ps, A, d, r, true, p.Mts, nullptr);
   k_prep_Bcat<<<blocks_for(static_cast<size_t>(d) * 2 * r, T), T, 0, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(A), reinterpret_cast<const __nv_bfloat16*>(Pr), d, r,
       p.Bcat);
@@ -236,8 +291,7 @@ cudaError_t launch_prep_f32(const mapl_config& c, const void* A, const void* Ps,
   const size_t dr = static_cast<size_t>(d) * r;
   k_copy_f32<<<blocks_for(dr, T), T, 0, s>>>(reinterpret_cast<const float*>(A), p.A32, dr);
   k_prep_At32<<<blocks_for(dr, T), T, 0, s>>>(reinterpret_cast<const float*>(A), d, r, p.At32);
-  k_prep_M<<<blocks_for(static_cast<size_t>(r) * r, T), T, 0, s>>>(Ps, A, d, r, false, nullptr,
-                                                                     p.M32);
+  k_prep_M<<<r * ((r + 31) / 32), 256, 0, s>>>(Ps, A, d, r, false, nullptr, p.M32);
   (void)Pr;   // the plan's P_recv copy is used in place (p.Pr32)
   if (!A_only) {
     if (c.G > 0) {

@@ -8,8 +8,8 @@
 //   Y   = A - lr Y
 //   repeat n_retr: same polynomial step                         eq. (7)
 //   A   = Y
-// The GEMMs are tiled 64 x 64 x 16 fp32 CUDA-core kernels with sequential
-// fp32 accumulation per output; r x r reductions over d use a fixed split-K
+// The GEMMs are tiled 64 x 64 x 16 fp32 CUDA-core kernels (8 x 8 outputs
+// per thread) with sequential fp32 accumulation per output; r x r reductions over d use a fixed split-K
 // followed by an ordered sum, so results are run-to-run deterministic.
 #include "mapl_internal.h"
 
@@ -17,7 +17,7 @@ namespace mapl {
 
 namespace {
 
-constexpr int BM = 64, BN = 64, BK = 16;
+constexpr int BK = 16;
 
 enum Epi { kStore = 0, kMomentum = 1, kPoly = 2 };
 
@@ -30,58 +30,121 @@ struct EpiArgs {
 };
 
 // C[z] = op(A) B for z = blockIdx.z / ksplit; with ksplit > 1 each split
-// writes its partial product to C + split * M * N (per batch).
-template <bool TA, int EPI>
-__global__ void __launch_bounds__(256)
+// writes its partial product to C + split * M * N (per batch).  TM x TM
+// output tile per block of 64 threads (an 8 x 8 thread grid), each thread a
+// (TM/8) x (TM/8) micro-tile read from shared memory as float4s.  TM = 32
+// keeps the GEMMs of SPEL (r x r outputs, d x r with K = r) in enough blocks
+// to fill the GPU.  Requires lda, ldb, N multiples of 4 (d, r are) and, for
+// the non-transposed A, a split start that is a multiple of 4 (ksplit 1).
+template <bool TA, int EPI, int TM>
+__global__ void __launch_bounds__(64)
     k_sgemm(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C,
             int M, int N, int K, int lda, int ldb, long sA, long sB, long sC, int ksplit,
             EpiArgs e) {
-  __shared__ float As[BK][BM + 4];
-  __shared__ float Bs[BK][BN + 4];
+  constexpr int MT = TM / 8;          // outputs per thread per dimension
+  constexpr int V4 = TM / 16;         // float4 loads per thread per operand tile
+  constexpr int R4 = TM / 4;          // float4s in a TM-wide row
+  __shared__ __align__(16) float As[2][BK][TM + 4];
+  __shared__ __align__(16) float Bs[2][BK][TM + 4];
   const int z = blockIdx.z / ksplit, ks = blockIdx.z % ksplit;
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int m0 = blockIdx.y * TM, n0 = blockIdx.x * TM;
   const int kbeg = static_cast<int>(static_cast<long>(K) * ks / ksplit);
   const int kend = static_cast<int>(static_cast<long>(K) * (ks + 1) / ksplit);
   A += z * sA;
   B += z * sB;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float acc[4][4] = {};
-  for (int k0 = kbeg; k0 < kend; k0 += BK) {
-    for (int q = threadIdx.x; q < BK * BM; q += 256) {
-      int kk, mm;
-      if (TA) { kk = q / BM; mm = q % BM; } else { mm = q / BK; kk = q % BK; }
-      const int gk = k0 + kk, gm = m0 + mm;
-      float v = 0.f;
-      if (gk < kend && gm < M) v = TA ? A[static_cast<long>(gk) * lda + gm] : A[static_cast<long>(gm) * lda + gk];
-      As[kk][mm] = v;
+  const int t = threadIdx.x;
+  const int ty = t >> 3, tx = t & 7;
+  float acc[MT][MT];
+#pragma unroll
+  for (int i = 0; i < MT; ++i)
+#pragma unroll
+    for (int j = 0; j < MT; ++j) acc[i][j] = 0.f;
+  auto load4 = [](const float* src, int valid) {
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (valid >= 4) {
+      x = *reinterpret_cast<const float4*>(src);
+    } else {
+      if (valid > 0) x.x = src[0];
+      if (valid > 1) x.y = src[1];
+      if (valid > 2) x.z = src[2];
     }
-    for (int q = threadIdx.x; q < BK * BN; q += 256) {
-      const int kk = q / BN, nn = q % BN;
+    return x;
+  };
+  // the next K-tile is fetched into registers while the current one is
+  // multiplied out of the other shared-memory buffer
+  float4 ra[V4], rb[V4];
+  auto fetch = [&](int k0) {
+#pragma unroll
+    for (int v = 0; v < V4; ++v) {
+      if (TA) {   // A is K x M (row-major, ld lda): rows k, m contiguous
+        const int kk = t / R4 + (64 / R4) * v, mm = (t % R4) * 4;
+        const int gk = k0 + kk, gm = m0 + mm;
+        ra[v] = gk < kend ? load4(A + static_cast<long>(gk) * lda + gm, M - gm)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {    // A is M x K: rows m, k contiguous
+        const int mm = t % TM, kk = 4 * (t / TM + (64 / TM) * v);
+        const int gm = m0 + mm, gk = k0 + kk;
+        ra[v] = gm < M ? load4(A + static_cast<long>(gm) * lda + gk, kend - gk)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      const int kk = t / R4 + (64 / R4) * v, nn = (t % R4) * 4;   // B is K x N
       const int gk = k0 + kk, gn = n0 + nn;
-      Bs[kk][nn] = (gk < kend && gn < N) ? B[static_cast<long>(gk) * ldb + gn] : 0.f;
+      rb[v] = gk < kend ? load4(B + static_cast<long>(gk) * ldb + gn, N - gn)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    __syncthreads();
+  };
+  auto stash = [&](int buf) {
+#pragma unroll
+    for (int v = 0; v < V4; ++v) {
+      if (TA) {
+        const int kk = t / R4 + (64 / R4) * v, mm = (t % R4) * 4;
+        *reinterpret_cast<float4*>(&As[buf][kk][mm]) = ra[v];
+      } else {
+        const int mm = t % TM, kk = 4 * (t / TM + (64 / TM) * v);
+        As[buf][kk][mm] = ra[v].x;
+        As[buf][kk + 1][mm] = ra[v].y;
+        As[buf][kk + 2][mm] = ra[v].z;
+        As[buf][kk + 3][mm] = ra[v].w;
+      }
+      const int kk = t / R4 + (64 / R4) * v, nn = (t % R4) * 4;
+      *reinterpret_cast<float4*>(&Bs[buf][kk][nn]) = rb[v];
+    }
+  };
+  int buf = 0;
+  if (kbeg < kend) {
+    fetch(kbeg);
+    stash(0);
+  }
+  __syncthreads();
+  for (int k0 = kbeg; k0 < kend; k0 += BK) {
+    const bool more = k0 + BK < kend;
+    if (more) fetch(k0 + BK);
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
-      float av[4], bv[4];
+      float av[MT], bv[MT];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = As[kk][ty * 4 + i];
+      for (int q = 0; q < MT / 4; ++q) {
+        const float4 a4 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * MT + 4 * q]);
+        const float4 b4 = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * MT + 4 * q]);
+        av[4 * q] = a4.x; av[4 * q + 1] = a4.y; av[4 * q + 2] = a4.z; av[4 * q + 3] = a4.w;
+        bv[4 * q] = b4.x; bv[4 * q + 1] = b4.y; bv[4 * q + 2] = b4.z; bv[4 * q + 3] = b4.w;
+      }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
+      for (int i = 0; i < MT; ++i)
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        for (int j = 0; j < MT; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
+    if (more) stash(buf ^ 1);
     __syncthreads();
+    buf ^= 1;
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int gm = m0 + ty * 4 + i;
+  for (int i = 0; i < MT; ++i) {
+    const int gm = m0 + ty * MT + i;
     if (gm >= M) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int gn = n0 + tx * 4 + j;
+    for (int j = 0; j < MT; ++j) {
+      const int gn = n0 + tx * MT + j;
       if (gn >= N) continue;
       const long o = static_cast<long>(gm) * N + gn;
       if (EPI == kStore) {
@@ -96,6 +159,20 @@ __global__ void __launch_bounds__(256)
       }
     }
   }
+}
+
+// Q = a I + b S + c (sum of `ksplit` partials of S^2, ordered)
+__global__ void k_reduce_poly(const float* __restrict__ part, const float* __restrict__ S,
+                              float* __restrict__ Q, int n, int ksplit, float a, float b,
+                              float c, long sP, long sO) {
+  const int z = blockIdx.y;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n * n) return;
+  const float* p = part + z * sP;
+  float v = 0.f;
+  for (int s = 0; s < ksplit; ++s) v += p[static_cast<long>(s) * n * n + idx];
+  const int i = idx / n, j = idx % n;
+  Q[z * sO + idx] = (i == j ? a : 0.f) + b * S[z * sO + idx] + c * v;
 }
 
 // out = sum of `ksplit` partials (ordered); optionally symmetrised.
@@ -157,8 +234,17 @@ __global__ void k_axpy(const float* __restrict__ A, const float* __restrict__ D,
     y[z * sX + i] = A[z * sX + i] - lr * D[z * sX + i];
 }
 
+constexpr int TM = 32;   // output tile of the SPEL GEMMs
+
 inline dim3 gemm_grid(int M, int N, int zdim) {
-  return dim3((N + BN - 1) / BN, (M + BM - 1) / BM, zdim);
+  return dim3((N + TM - 1) / TM, (M + TM - 1) / TM, zdim);
+}
+
+// splits of the r-long sum in S^2 (bounded by the partial buffer's ks)
+inline int choose_ksplit_r(int r, int ks) {
+  int k = r / 64;
+  if (k < 1) k = 1;
+  return k < ks ? k : ks;
 }
 
 int choose_ksplit(int d) {
@@ -198,20 +284,20 @@ Ws carve(void* ws, int d, int r, int batch) {
 void pe_step(const float* Yin, float* Yout, const float* co, const Ws& w, int d, int r,
              int batch, cudaStream_t s) {
   EpiArgs none{};
-  k_sgemm<true, kStore><<<gemm_grid(r, r, batch * w.ks), 256, 0, s>>>(
+  k_sgemm<true, kStore, TM><<<gemm_grid(r, r, batch * w.ks), 64, 0, s>>>(
       Yin, Yin, w.part, r, r, d, r, r, w.dr, w.dr, w.rr * w.ks, w.ks, none);
   k_reduce<<<dim3((r * r + 255) / 256, batch), 256, 0, s>>>(w.part, w.S, r, w.ks, 0,
                                                             w.rr * w.ks, w.rr);
-  EpiArgs pe{};
-  pe.S = w.S;
-  pe.sS = w.rr;
-  pe.a = co[0];
-  pe.b = co[1];
-  pe.c = co[2];
-  k_sgemm<false, kPoly><<<gemm_grid(r, r, batch), 256, 0, s>>>(w.S, w.S, w.Q, r, r, r, r, r,
-                                                               w.rr, w.rr, w.rr, 1, pe);
-  k_sgemm<false, kStore><<<gemm_grid(d, r, batch), 256, 0, s>>>(Yin, w.Q, Yout, d, r, r, r, r,
-                                                                w.dr, w.rr, w.dr, 1, none);
+  // S^2 in split-K partials (a 4-aligned split of K = r for the plain A),
+  // then Q = a I + b S + c S^2 in the ordered reduction
+  const int kr = choose_ksplit_r(r, w.ks);
+  k_sgemm<false, kStore, TM><<<gemm_grid(r, r, batch * kr), 64, 0, s>>>(
+      w.S, w.S, w.part, r, r, r, r, r, w.rr, w.rr, w.rr * w.ks, kr, none);
+  k_reduce_poly<<<dim3((r * r + 255) / 256, batch), 256, 0, s>>>(
+      w.part, w.S, w.Q, r, kr, co[0], co[1], co[2], w.rr * w.ks, w.rr);
+  k_sgemm<false, kStore, TM><<<gemm_grid(d, r, batch), 64, 0, s>>>(Yin, w.Q, Yout, d, r, r, r,
+                                                                    r, w.dr, w.rr, w.dr, 1,
+                                                                    none);
 }
 
 }  // namespace
@@ -230,7 +316,7 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
   const Ws w = carve(ws, d, r, batch);
   EpiArgs none{};
   // H = sym(A^T G)
-  k_sgemm<true, kStore><<<gemm_grid(r, r, batch * w.ks), 256, 0, s>>>(
+  k_sgemm<true, kStore, TM><<<gemm_grid(r, r, batch * w.ks), 64, 0, s>>>(
       A, G, w.part, r, r, d, r, r, w.dr, w.dr, w.rr * w.ks, w.ks, none);
   k_reduce<<<dim3((r * r + 255) / 256, batch), 256, 0, s>>>(w.part, w.S, r, w.ks, 1,
                                                             w.rr * w.ks, w.rr);
@@ -241,7 +327,7 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
   mo.sG = w.dr;
   mo.sm = w.dr;
   mo.beta = beta;
-  k_sgemm<false, kMomentum><<<gemm_grid(d, r, batch), 256, 0, s>>>(A, w.S, nullptr, d, r, r, r,
+  k_sgemm<false, kMomentum, TM><<<gemm_grid(d, r, batch), 64, 0, s>>>(A, w.S, nullptr, d, r, r, r,
                                                                    r, w.dr, w.rr, 0, 1, mo);
   // Y = m / (||m||_F + 1e-7)
   k_sumsq_partial<<<dim3(kNormBlocks, batch), 256, 0, s>>>(m, w.dr, w.nrm_part, w.dr,

@@ -126,6 +126,31 @@ mapl_status mapl_decompress(mapl_plan plan, const void* payload, const int32_t* 
                             int64_t N, const void* E_recv, void* X_hat, cudaStream_t stream);
 
 /*
+ * Streaming codebook synchronisation (MAPL §3.5, App. F): sender and receiver
+ * keep identical codebooks by overwriting, each micro-batch, the same random
+ * subset of codes with the sender's current values.  The pages give the
+ * subset size as 1/K of the codes (§3.5), 1/5 per micro-batch (Table 8) and
+ * "interval 5" (App. E.4); it is a parameter here.
+ *
+ * mapl_stream_subset (host only, no GPU): the subset for micro-batch `step`.
+ *   The R*G*K codes (flat id = (rho*G + g)*K + k) are shuffled once per epoch
+ *   of ceil(total / per_batch) steps (Fisher-Yates driven by splitmix64 seeded
+ *   with `seed` and the epoch number), and step takes the epoch's
+ *   (step mod steps-per-epoch)-th block of per_batch ids.  Writes *count ids
+ *   (per_batch, or fewer for the last block of an epoch) to `ids`.  Both ends
+ *   compute the same subset, so only the code values need to travel.
+ * mapl_plan_update_codes: codes ids[i] (device int32) take the values
+ *   codes[i * gd .. +gd) (device, plan dtype); their ||c||^2 and every book's
+ *   max ||c|| are refreshed.  An id outside [0, R*G*K) sets the error word
+ *   (mapl_check reports MAPL_ERR_INVALID_ARG) and is skipped.  Async.
+ */
+mapl_status mapl_stream_subset(int64_t total, int64_t per_batch, uint64_t seed, int64_t step,
+                               int32_t* ids, int32_t* count);
+
+mapl_status mapl_plan_update_codes(mapl_plan plan, const int32_t* ids, int32_t count,
+                                   const void* codes, cudaStream_t stream);
+
+/*
  * Backward pass (MAPL §3.2: the gradient of the boundary activation is
  * routed through the same orthogonal projector A; §3.5: it is what the
  * gradient exchange compresses).  bf16 tensor-core plans only

@@ -17,6 +17,9 @@ Parallelism* (MAPL).  Every function names the passage it writes out:
 * grad_decompress   -- §3.2 (backward pass): dL/dX = gZ A^T
 * grad_A            -- Euclidean gradient of A that §3.3 feeds to SPEL, for the
                        composed codec X_hat = (X - E[ids] P) A A^T + E'[ids] P'
+* stream_subset     -- §3.5 / App. F streaming codebook synchronisation: the
+                       random subset of codes refreshed at a micro-batch
+* apply_code_update -- §3.5 / App. F: the shared codebook after a refresh
 * rvq_encode/decode -- §3.5 "Composing with vector quantization" and App. E.4:
                        G groups, R rounds of residual quantisation, K codes
 * tangent_project   -- §3.3, eq. (4): g - A sym(A^T g), sym(M) = (M + M^T)/2
@@ -50,7 +53,8 @@ import numpy as np
 
 __all__ = [
     "anchor", "compress", "compress_folded", "reconstruct", "grad_compress",
-    "grad_decompress", "grad_A", "grad_A_given", "rvq_encode",
+    "grad_decompress", "grad_A", "grad_A_given", "stream_subset", "apply_code_update",
+    "splitmix64", "rvq_encode",
     "rvq_encode_given", "rvq_decode", "tangent_project", "sym", "momentum",
     "polar_express", "spel_step", "payload_bytes_per_token",
 ]
@@ -223,6 +227,52 @@ def payload_bytes_per_token(r: int, dtype_bytes: int = 2, G: int = 0, R: int = 0
 
 
 # ---------------------------------------------------------------------------
+# streaming codebook synchronisation, §3.5 and App. F
+# ---------------------------------------------------------------------------
+_M64 = (1 << 64) - 1
+
+
+def splitmix64(state: int):
+    """One step of splitmix64 (Steele, Lea and Flood 2014, with the constants
+    of Vigna's reference implementation): returns (output, new state)."""
+    state = (state + 0x9E3779B97F4A7C15) & _M64
+    z = state
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _M64
+    return z ^ (z >> 31), state
+
+
+def stream_subset(total: int, per_batch: int, seed: int, step: int) -> np.ndarray:
+    """Codes refreshed at micro-batch `step`.  Reading of App. F ("the codebook
+    is partitioned into random subsets"): epoch e = step // n_sub (n_sub =
+    ceil(total / per_batch)) shuffles the flat code ids 0..total-1 with
+    Fisher-Yates (for i from total-1 down to 1, swap i with j = u_i mod
+    (i + 1)), the u_i drawn from splitmix64 seeded with
+    seed XOR (0xD1B54A32D192ED03 * (e + 1)); the step takes block
+    step % n_sub of per_batch consecutive entries."""
+    n_sub = -(-total // per_batch)
+    epoch, blk = divmod(step, n_sub)
+    perm = list(range(total))
+    state = (seed ^ ((0xD1B54A32D192ED03 * (epoch + 1)) & _M64)) & _M64
+    for i in range(total - 1, 0, -1):
+        u, state = splitmix64(state)
+        j = u % (i + 1)
+        perm[i], perm[j] = perm[j], perm[i]
+    return np.asarray(perm[blk * per_batch:(blk + 1) * per_batch], dtype=np.int64)
+
+
+def apply_code_update(C, ids, codes) -> np.ndarray:
+    """The shared codebook after a refresh: flat code ids[i] (over R x G x K)
+    take the values codes[i] (gd entries); every other code is unchanged."""
+    C = _f64(C).copy()
+    R, G, K, gd = C.shape
+    flat = C.reshape(R * G * K, gd)
+    flat[np.asarray(ids, dtype=np.int64)] = _f64(codes)
+    return flat.reshape(R, G, K, gd)
+
+
+# ---------------------------------------------------------------------------
+# SPEL projector update, §3.3 eqs. (4)-(7)# ---------------------------------------------------------------------------
 # SPEL projector update, §3.3 eqs. (4)-(7)
 # ---------------------------------------------------------------------------
 def sym(M) -> np.ndarray:

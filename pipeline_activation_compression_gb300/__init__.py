@@ -20,6 +20,7 @@ __all__ = [
     "mapl_compress_z32", "mapl_decompress", "mapl_check", "mapl_plan_destroy",
     "mapl_host_workspace_size", "mapl_compress_host", "mapl_decompress_host",
     "mapl_grad_compress", "mapl_grad_decompress", "mapl_grad_A",
+    "mapl_stream_subset", "mapl_plan_update_codes",
     "mapl_spel_workspace_size", "mapl_spel_step", "mapl_spel_step_static", "mapl_last_error",
     "mapl_version",
     "MAPL_F32", "MAPL_BF16", "STATUS",
@@ -77,6 +78,8 @@ def load_library():
         "mapl_grad_compress": [P, P, I64, P, P],
         "mapl_grad_decompress": [P, P, I64, P, P],
         "mapl_grad_A": [P, P, P, P, P, P, P, I64, P, P],
+        "mapl_stream_subset": [I64, I64, ctypes.c_uint64, I64, P, ctypes.POINTER(I32)],
+        "mapl_plan_update_codes": [P, P, I32, P, P],
         "mapl_compress_host": [P, P, P, I64, P, P, P, SZ, P],
         "mapl_decompress_host": [P, P, P, I64, P, P, P, SZ, P],
         "mapl_spel_workspace_size": [I64, I64, I32, ctypes.POINTER(SZ)],
@@ -291,6 +294,24 @@ def mapl_grad_A(plan: Plan, X, tids, E_send, gZ, gX_hat, Z, dA, stream=None):
         _ptr(gX_hat, torch.bfloat16, "gX_hat"), _ptr(Z, torch.bfloat16, "Z"),
         int(X.shape[0]), _ptr(dA, torch.float32, "dA"), _stream(stream)))
     return dA
+
+
+def mapl_stream_subset(total: int, per_batch: int, seed: int, step: int) -> np.ndarray:
+    """Code ids (flat over R x G x K) to refresh at micro-batch `step`; host only."""
+    ids = np.empty(int(per_batch), dtype=np.int32)
+    n = ctypes.c_int32(0)
+    _check(load_library().mapl_stream_subset(int(total), int(per_batch), ctypes.c_uint64(seed),
+                                             int(step), ids.ctypes.data_as(ctypes.c_void_p),
+                                             ctypes.byref(n)))
+    return ids[:n.value].copy()
+
+
+def mapl_plan_update_codes(plan: Plan, ids, codes, stream=None):
+    """Codes ids[i] (device int32) take the values codes[i] (device, count x gd)."""
+    import torch
+    _check(load_library().mapl_plan_update_codes(
+        plan.handle, _ptr(ids, torch.int32, "ids"), int(ids.numel()),
+        _ptr(codes, _tdtype(plan.cfg.dtype), "codes"), _stream(stream)))
 
 
 def mapl_check(plan: Plan, stream=None):

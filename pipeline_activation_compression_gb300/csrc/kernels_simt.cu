@@ -284,6 +284,47 @@ cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps
   return cudaGetLastError();
 }
 
+// Streaming codebook update (§3.5, App. F): code ids[i] (flat over R x G x
+// K) takes the values codes[i] (gd entries, plan dtype); its squared norm is
+// recomputed.  One thread per updated code; ids outside the table set the
+// error word and are skipped.
+__global__ void k_update_codes(const int32_t* ids, int count, const void* codes, int gd,
+                               int ncode, bool bf, __nv_bfloat16* Cb, float* C32, float* cnorm,
+                               int* err) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= count) return;
+  const int id = ids[i];
+  if (id < 0 || id >= ncode) {
+    atomicOr(err, kErrBadIndex);
+    return;
+  }
+  double s = 0.0;
+  for (int j = 0; j < gd; ++j) {
+    const size_t src = static_cast<size_t>(i) * gd + j, dst = static_cast<size_t>(id) * gd + j;
+    if (bf) {
+      const __nv_bfloat16 v = reinterpret_cast<const __nv_bfloat16*>(codes)[src];
+      Cb[dst] = v;
+      const double x = static_cast<double>(__bfloat162float(v));
+      s = fma(x, x, s);
+    } else {
+      const float v = reinterpret_cast<const float*>(codes)[src];
+      C32[dst] = v;
+      s = fma(static_cast<double>(v), static_cast<double>(v), s);
+    }
+  }
+  cnorm[id] = static_cast<float>(s);
+}
+
+cudaError_t launch_update_codes(const mapl_config& c, const int32_t* ids, int count,
+                                const void* codes, PlanDevice& p, cudaStream_t s) {
+  const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G), ncode = nb * c.K;
+  const bool bf = c.dtype == MAPL_BF16;
+  k_update_codes<<<blocks_for(static_cast<size_t>(count), 128), 128, 0, s>>>(
+      ids, count, codes, gd, ncode, bf, p.Cb, p.C32, p.cnorm, p.err);
+  k_prep_cmax<<<blocks_for(nb, 64), 64, 0, s>>>(p.cnorm, nb, c.K, p.cmax);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prep_f32(const mapl_config& c, const void* A, const void* Ps, const void* Pr,
                             const void* C, PlanDevice& p, bool A_only, cudaStream_t s) {
   const int d = static_cast<int>(c.d), r = static_cast<int>(c.r);

@@ -8,6 +8,8 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
+#include <algorithm>
 
 #include "mapl_internal.h"
 
@@ -360,6 +362,59 @@ mapl_status mapl_plan_update_A(mapl_plan pl, const void* A, cudaStream_t stream)
   cudaError_t e = pl->tc ? launch_prep_bf16(pl->cfg, A, pl->p.Ps, pl->p.Pr, nullptr, pl->p, true, stream)
                          : launch_prep_f32(pl->cfg, A, pl->p.Ps, pl->p.Pr, nullptr, pl->p, true, stream);
   if (e != cudaSuccess) return cuda_fail(e, "update_A");
+  return MAPL_OK;
+}
+
+mapl_status mapl_plan_update_codes(mapl_plan pl, const int32_t* ids, int32_t count,
+                                   const void* codes, cudaStream_t stream) {
+  if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
+  if (!pl->vq) return fail(MAPL_ERR_INVALID_ARG, "the plan has no codebooks");
+  if (count < 0) return fail(MAPL_ERR_INVALID_ARG, "count must be >= 0");
+  if (count == 0) return MAPL_OK;
+  if (!ids || !codes) return fail(MAPL_ERR_INVALID_ARG, "NULL pointer");
+  mapl_status st = check_device(pl);
+  if (st != MAPL_OK) return st;
+  cudaError_t e = launch_update_codes(pl->cfg, ids, count, codes, pl->p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "update_codes");
+  return MAPL_OK;
+}
+
+namespace {
+
+// splitmix64 (Steele, Lea, Flood 2014; Vigna's reference constants): the
+// counter-based generator both ends of a boundary run to agree on the subset.
+uint64_t splitmix64(uint64_t& x) {
+  x += 0x9E3779B97F4A7C15ull;
+  uint64_t z = x;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+}  // namespace
+
+mapl_status mapl_stream_subset(int64_t total, int64_t per_batch, uint64_t seed, int64_t step,
+                               int32_t* ids, int32_t* count) {
+  if (total < 1 || total > 0x7fffffffLL) return fail(MAPL_ERR_INVALID_ARG, "total must be in [1, 2^31)");
+  if (per_batch < 1 || per_batch > total)
+    return fail(MAPL_ERR_INVALID_ARG, "per_batch must be in [1, total]");
+  if (step < 0 || !ids || !count)
+    return fail(MAPL_ERR_INVALID_ARG, "step must be >= 0, ids and count non-NULL");
+  // epoch e = step / nsub is a fresh permutation of [0, total) (Fisher-Yates
+  // driven by splitmix64 seeded with seed and e); step takes its
+  // (step % nsub)-th block of per_batch codes (the last block is shorter)
+  const int64_t nsub = (total + per_batch - 1) / per_batch;
+  const int64_t epoch = step / nsub, blk = step % nsub;
+  std::vector<int32_t> perm(static_cast<size_t>(total));
+  for (int64_t i = 0; i < total; ++i) perm[static_cast<size_t>(i)] = static_cast<int32_t>(i);
+  uint64_t state = seed ^ (0xD1B54A32D192ED03ull * static_cast<uint64_t>(epoch + 1));
+  for (int64_t i = total - 1; i > 0; --i) {
+    const uint64_t j = splitmix64(state) % static_cast<uint64_t>(i + 1);
+    std::swap(perm[static_cast<size_t>(i)], perm[static_cast<size_t>(j)]);
+  }
+  const int64_t b = blk * per_batch, e = std::min(total, b + per_batch);
+  for (int64_t i = b; i < e; ++i) ids[i - b] = perm[static_cast<size_t>(i)];
+  *count = static_cast<int32_t>(e - b);
   return MAPL_OK;
 }
 

@@ -89,6 +89,9 @@ cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps
 cudaError_t launch_prep_f32(const mapl_config& c, const void* A, const void* Ps, const void* Pr,
                             const void* C, PlanDevice& p, bool A_only, cudaStream_t s);
 
+cudaError_t launch_update_codes(const mapl_config& c, const int32_t* ids, int count,
+                                const void* codes, PlanDevice& p, cudaStream_t s);
+
 cudaError_t launch_compress_tc(const CUtensorMap& tmX, const CUtensorMap& tmAt,
                                const CUtensorMap& tmMt, const CUtensorMap& tmC,
                                const CUtensorMap& tmE, const CompressArgs& a,

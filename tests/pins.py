@@ -372,6 +372,62 @@ def pin_grad_finite_differences(o):
     assert np.max(np.abs(given - gA)) < 1e-7 * max(1.0, np.max(np.abs(gA)))
 
 
+# ------------------------------------------------- §3.5 codebook streaming
+def pin_splitmix64_reference(o):
+    """Published first outputs of splitmix64 from state 0 (Vigna's reference
+    implementation): 0xe220a8397b1dcdaf, 0x6e789e6aa1b965f4,
+    0x06c45d188009454f."""
+    state, outs = 0, []
+    for _ in range(3):
+        u, state = o.splitmix64(state)
+        outs.append(u)
+    assert outs == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+
+
+def pin_stream_partition(o):
+    """App. F: the codebook is partitioned into random subsets.  Over one
+    epoch the subsets are disjoint and cover every code; the next epoch is a
+    different permutation; the subset is a function of (seed, step) only."""
+    total, per = 97, 20
+    n_sub = -(-total // per)
+    for epoch in range(2):
+        ids = [o.stream_subset(total, per, 5, epoch * n_sub + b) for b in range(n_sub)]
+        assert [len(x) for x in ids] == [20, 20, 20, 20, 17]
+        allids = np.concatenate(ids)
+        assert np.array_equal(np.sort(allids), np.arange(total))
+    e0 = np.concatenate([o.stream_subset(total, per, 5, b) for b in range(n_sub)])
+    e1 = np.concatenate([o.stream_subset(total, per, 5, n_sub + b) for b in range(n_sub)])
+    assert not np.array_equal(e0, e1)
+    assert np.array_equal(o.stream_subset(total, per, 5, 3), o.stream_subset(total, per, 5, 3))
+    assert not np.array_equal(o.stream_subset(total, per, 5, 0), o.stream_subset(total, per, 6, 0))
+    # a uniform shuffle of 10 ids leaves some id in place with probability
+    # about 1 - 1/e; a single-cycle shuffle (Sattolo) never does
+    fixed = [np.any(o.stream_subset(10, 10, sd, 0) == np.arange(10)) for sd in range(20)]
+    assert 6 <= sum(fixed) <= 19
+
+
+def pin_code_update_epoch(o):
+    """After a full epoch of refreshes from a live codebook C1, the shared
+    codebook equals C1 exactly; after part of it, exactly the refreshed
+    codes have moved."""
+    rng = np.random.default_rng(41)
+    R, G, K, gd = 2, 3, 8, 4
+    C0 = rng.standard_normal((R, G, K, gd))
+    C1 = rng.standard_normal((R, G, K, gd))
+    total, per = R * G * K, 10
+    flat1 = C1.reshape(-1, gd)
+    C = C0
+    moved = set()
+    for step in range(-(-total // per)):
+        ids = o.stream_subset(total, per, 9, step)
+        C = o.apply_code_update(C, ids, flat1[ids])
+        moved |= set(ids.tolist())
+        if step == 1:
+            diff = np.nonzero(np.any(C.reshape(-1, gd) != C0.reshape(-1, gd), axis=1))[0]
+            assert set(diff.tolist()) == moved
+    assert np.array_equal(C, C1)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

@@ -38,6 +38,10 @@ MUTANTS = {
     "gradA_no_anchor": ("    Xres = _f64(X) - anchor(E, P, tids)\n    A, g = _f64(A), _f64(gXhat)", "    Xres = _f64(X)\n    A, g = _f64(A), _f64(gXhat)"),
     "gradA_given_raw_X": ("    return Xres.T @ _f64(gZ) + _f64(gXhat).T @ _f64(Z)", "    return _f64(X).T @ _f64(gZ) + _f64(gXhat).T @ _f64(Z)"),
     "grad_decompress_no_T": ("return _f64(gZ) @ _f64(A).T", "return _f64(gZ) @ _f64(A).T * 2.0"),
+    "splitmix_shift": ("z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _M64", "z = ((z ^ (z >> 26)) * 0x94D049BB133111EB) & _M64"),
+    "subset_same_epoch": ("state = (seed ^ ((0xD1B54A32D192ED03 * (epoch + 1)) & _M64)) & _M64", "state = seed"),
+    "subset_off_by_one": ("        j = u % (i + 1)", "        j = u % i"),
+    "code_update_dropped": ("    flat[np.asarray(ids, dtype=np.int64)] = _f64(codes)", "    pass"),
 }
 
 

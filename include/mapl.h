@@ -89,6 +89,28 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
  * the operand layouts (§3.3: A_p changes every optimizer step). Async. */
 mapl_status mapl_plan_update_A(mapl_plan plan, const void* A, cudaStream_t stream);
 
+/*
+ * First-boundary anchor (Fig. 2 of the MAPL page: at the boundary after the
+ * first stage the anchor is the original token embedding itself).  After
+ * this call the plan's calls use
+ *   compress    Z     = (X - E_emb[tids]) A
+ *   decompress  X_hat = Z_hat A^T + E_emb[tids]
+ *   grad_A      dA    = (X - E_emb[tids])^T gZ + gX_hat^T Z
+ * and ignore their E_send / E_recv arguments (they may be NULL); P_send and
+ * P_recv are no longer used.
+ *   E_emb  V x d bf16, device, 16-byte aligned.  The plan keeps the POINTER
+ *          (not a copy): the caller keeps E_emb alive and unchanged while the
+ *          plan is used, and calls this again after changing it.
+ * The compress fold E_emb[tids] A is read from a V x r table T = E_emb A that
+ * the plan computes here and again in every mapl_plan_update_A (cuBLAS,
+ * fp32 accumulation), held as three bf16 terms T_hi + T_mid + T_lo so the
+ * tensor-core fold keeps about 24 bits of T.  Plan memory grows by
+ * V x r x 10 bytes.  bf16 plans only, r <= 170.  Async on `stream`.
+ * Errors: INVALID_ARG (null, alignment), UNSUPPORTED (f32 plan, r too
+ * large), CUDA.
+ */
+mapl_status mapl_plan_set_embedding_anchor(mapl_plan plan, const void* E_emb, cudaStream_t stream);
+
 /* Bytes of payload per token: 2r (bf16 Z), 4r (f32 Z) or R*G (uint8 idx). */
 mapl_status mapl_payload_bytes(const mapl_config* cfg, int64_t* bytes_per_token);
 

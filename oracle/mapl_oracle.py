@@ -12,6 +12,10 @@ Parallelism* (MAPL).  Every function names the passage it writes out:
 * anchor            -- §3.2, eq. (3): E_small[ids] P
 * compress          -- §3.2, eq. (1): Z = (X - E_small[ids] P) A
 * reconstruct       -- §3.2, eq. (2): X_hat = Z A^T + E_small_next[ids] P_next
+* compress_embed    -- Fig. 2 caption: at the first boundary the anchor is the
+                       original token embedding, Z = (X - E_emb[ids]) A
+* reconstruct_embed -- its receiver side, X_hat = Z A^T + E_emb[ids]
+* grad_A_embed      -- Euclidean gradient of A for that first-boundary codec
 * grad_compress     -- §3.2 (backward pass): the boundary gradient dL/dX_hat
                        routed through the same projector, gZ = dL/dX_hat A
 * grad_decompress   -- §3.2 (backward pass): dL/dX = gZ A^T
@@ -52,7 +56,8 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "anchor", "compress", "compress_folded", "reconstruct", "grad_compress",
+    "anchor", "compress", "compress_folded", "reconstruct", "compress_embed",
+    "reconstruct_embed", "grad_A_embed", "grad_compress",
     "grad_decompress", "grad_A", "grad_A_given", "stream_subset", "apply_code_update",
     "splitmix64", "rvq_encode",
     "rvq_encode_given", "rvq_decode", "tangent_project", "sym", "momentum",
@@ -97,6 +102,30 @@ def reconstruct(Zhat, tids, A, E_next, P_next) -> np.ndarray:
     """Receiver side, eq. (2): X_hat = Z A^T + E_small_{p+1}[tids] P_{p+1}."""
     Zhat, A = _f64(Zhat), _f64(A)
     return Zhat @ A.T + anchor(E_next, P_next, tids)
+
+
+# ---------------------------------------------------------------------------
+# first boundary, Fig. 2: the anchor is the full token embedding
+# ---------------------------------------------------------------------------
+def compress_embed(X, tids, A, E_emb) -> np.ndarray:
+    """Sender side at the first boundary: Z = (X - E_emb[tids]) A, with the
+    V x d embedding table itself as the anchor (no low-rank factor)."""
+    X, A, E_emb = _f64(X), _f64(A), _f64(E_emb)
+    return (X - E_emb[np.asarray(tids, dtype=np.int64)]) @ A
+
+
+def reconstruct_embed(Zhat, tids, A, E_emb) -> np.ndarray:
+    """Receiver side at the first boundary: X_hat = Z A^T + E_emb[tids]."""
+    Zhat, A, E_emb = _f64(Zhat), _f64(A), _f64(E_emb)
+    return Zhat @ A.T + E_emb[np.asarray(tids, dtype=np.int64)]
+
+
+def grad_A_embed(X, tids, E_emb, gZ, gXhat, Z) -> np.ndarray:
+    """dL/dA for X_hat = (X - E_emb[tids]) A A^T + E_emb[tids], given the
+    gradient gZ of Z and Z itself: X_res^T gZ + gX_hat^T Z with
+    X_res = X - E_emb[tids]."""
+    Xres = _f64(X) - _f64(E_emb)[np.asarray(tids, dtype=np.int64)]
+    return Xres.T @ _f64(gZ) + _f64(gXhat).T @ _f64(Z)
 
 
 # ---------------------------------------------------------------------------

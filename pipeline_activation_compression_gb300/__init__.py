@@ -16,7 +16,8 @@ import numpy as np
 
 __all__ = [
     "MaplError", "MaplConfig", "Plan", "load_library", "library_path", "build",
-    "mapl_plan_create", "mapl_plan_update_A", "mapl_payload_bytes", "mapl_compress",
+    "mapl_plan_create", "mapl_plan_update_A", "mapl_plan_set_embedding_anchor",
+    "mapl_payload_bytes", "mapl_compress",
     "mapl_compress_z32", "mapl_decompress", "mapl_check", "mapl_plan_destroy",
     "mapl_host_workspace_size", "mapl_compress_host", "mapl_decompress_host",
     "mapl_grad_compress", "mapl_grad_decompress", "mapl_grad_A",
@@ -69,6 +70,7 @@ def load_library():
     sig = {
         "mapl_plan_create": [ctypes.POINTER(P), ctypes.POINTER(MaplConfig), P, P, P, P, P],
         "mapl_plan_update_A": [P, P, P],
+        "mapl_plan_set_embedding_anchor": [P, P, P],
         "mapl_payload_bytes": [ctypes.POINTER(MaplConfig), ctypes.POINTER(I64)],
         "mapl_compress": [P, P, P, I64, P, P, P],
         "mapl_compress_z32": [P, P, P, I64, P, P, P],
@@ -195,6 +197,13 @@ def mapl_plan_create(cfg: MaplConfig, A, P_send, P_recv, codebooks=None, stream=
 def mapl_plan_update_A(plan: Plan, A, stream=None):
     _check(load_library().mapl_plan_update_A(plan.handle, _ptr(A, _tdtype(plan.cfg.dtype), "A"),
                                              _stream(stream)))
+
+
+def mapl_plan_set_embedding_anchor(plan: Plan, E_emb, stream=None):
+    """First-boundary anchor: the plan keeps a reference to E_emb (V x d bf16)."""
+    _check(load_library().mapl_plan_set_embedding_anchor(
+        plan.handle, _ptr(E_emb, _tdtype(plan.cfg.dtype), "E_emb"), _stream(stream)))
+    plan.E_emb = E_emb
 
 
 def mapl_compress(plan: Plan, X, tids, E_send, payload, stream=None):

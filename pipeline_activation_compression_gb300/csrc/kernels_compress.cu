@@ -79,7 +79,7 @@ __device__ __forceinline__ void give_up(Ctl* ctl, int* err) {
 }
 
 struct Geo {
-  int r, nkx, nkr, na, nP, nV, nh, nrow, GD, B, nzb, zstride;
+  int r, nkx, nkr, na, nP, nV, nh, nrow, GD, B, nzb, zstride, nsplit;
   bool share;   // anchor rows gathered once per block for all -M splits
 };
 
@@ -87,8 +87,9 @@ __device__ __forceinline__ Geo geometry(const CompressArgs& a, bool vq) {
   Geo g;
   g.r = a.r;
   g.nkx = a.d / 64;
-  g.nkr = a.r / 64;
-  g.na = kNumSplit * g.nkr;
+  g.nkr = a.re / 64;
+  g.nsplit = a.nsplit;
+  g.na = a.nsplit * g.nkr;
   g.nP = g.nkx + (a.anchor ? g.na : 0);
   g.nV = vq ? a.G * a.R : 0;
   g.nh = a.r > 256 ? 2 : 1;
@@ -97,7 +98,7 @@ __device__ __forceinline__ Geo geometry(const CompressArgs& a, bool vq) {
   g.B = a.G < kNSlot ? a.G : kNSlot;
   g.nzb = vq ? (a.r <= 128 ? 2 : 1) : (2 * a.r <= 512 ? 2 : 1);
   g.zstride = a.r;
-  g.share = a.nstage >= kNumSplit;
+  g.share = a.nsplit > 1 && a.nstage >= a.nsplit;
   return g;
 }
 
@@ -591,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // E[tids] of block kb come with sp == 0 (or every sp when the
             // ring is too short to keep that stage while the other splits
             // stream)
-            const int j = p - geo.nkx, kb = j / kNumSplit, sp = j - kb * kNumSplit;
+            const int j = p - geo.nkx, kb = j / geo.nsplit, sp = j - kb * geo.nsplit;
             const bool gather = sp == 0 || !geo.share;
             mbar_arrive_expect_tx(fb, (gather ? kBlockBytes : 0u) + geo.r * 128u);
             for (int hh = 0; hh < geo.nh; ++hh)
@@ -731,10 +732,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                        (pj_p | k) != 0 ? 1u : 0u);
           if (!anchor || !geo.share) {
             mma_commit(smem_u32(&ctl->empty[pj_s]));
-          } else if (pj_sp == kNumSplit - 1) {
+          } else if (pj_sp == geo.nsplit - 1) {
             // release the block's stages together (split 0 held the rows)
             mma_commit(smem_u32(&ctl->empty[blk0]));
-            if (kNumSplit > 2) mma_commit(smem_u32(&ctl->empty[blk1]));
+            if (geo.nsplit > 2) mma_commit(smem_u32(&ctl->empty[blk1]));
             mma_commit(smem_u32(&ctl->empty[pj_s]));
           }
           progressed = true;
@@ -742,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pj_s = 0;
             pj_ph ^= 1u;
           }
-          if (anchor && ++pj_sp == kNumSplit) pj_sp = 0;
+          if (anchor && ++pj_sp == geo.nsplit) pj_sp = 0;
           if (++pj_p == geo.nP) {
             mma_commit(smem_u32(&ctl->zfull[zb]));
             pj_p = 0;

@@ -7,6 +7,9 @@
 //           = X^T gZ + dL/dX_hat^T Z - P^T (E[tids]^T gZ).
 // The products are plain GEMMs (cuBLAS); this file gathers the anchor rows
 // E[tids] into a dense N x r operand and widens P to fp32 for the last one.
+// It also lays out the first-boundary anchor table (Fig. 2: the first stage
+// subtracts the original token embeddings): (E_emb A)[tids] as three bf16
+// terms multiplied by -[I; I; I] in the compress kernel's anchor fold.
 #include "mapl_internal.h"
 
 namespace mapl {
@@ -23,6 +26,31 @@ __global__ void k_gather_rows(const int32_t* __restrict__ tids, const uint4* __r
   Eg[x] = (t >= 0 && t < V) ? E[static_cast<size_t>(t) * row16 + c] : make_uint4(0u, 0u, 0u, 0u);
 }
 
+// First-boundary anchor table: row v of T = E_emb A (fp32, V x r) as three
+// bf16 terms side by side, [hi | mid | lo] (V x 3r), the remainder of each
+// term carried into the next.
+__global__ void k_split3(const float* __restrict__ T, size_t V, int r, __nv_bfloat16* __restrict__ Tb) {
+  const size_t x = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (x >= V * r) return;
+  const size_t v = x / r;
+  const int j = static_cast<int>(x % r);
+  float rem = T[x];
+  for (int s = 0; s < 3; ++s) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(rem);
+    Tb[v * 3 * r + s * r + j] = b;
+    rem -= __bfloat162float(b);
+  }
+}
+
+// -[I; I; I]^T as the K-major B operand of the anchor fold (r x 3r):
+// entry (j, k) is -1 where k mod r == j.
+__global__ void k_neg_identity3(int r, __nv_bfloat16* __restrict__ M) {
+  const int x = blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= 3 * r * r) return;
+  const int j = x / (3 * r), k = x % (3 * r);
+  M[x] = __float2bfloat16_rn(k % r == j ? -1.f : 0.f);
+}
+
 __global__ void k_widen(const __nv_bfloat16* __restrict__ a, size_t n, float* __restrict__ b) {
   const size_t x = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (x < n) b[x] = __bfloat162float(a[x]);
@@ -36,6 +64,17 @@ cudaError_t launch_gather_rows(const int32_t* tids, const __nv_bfloat16* E, int 
   const size_t total = static_cast<size_t>(N) * row16;
   k_gather_rows<<<static_cast<unsigned>((total + 255) / 256), 256, 0, s>>>(
       tids, reinterpret_cast<const uint4*>(E), N, V, row16, reinterpret_cast<uint4*>(Eg));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split3(const float* T, size_t V, int r, __nv_bfloat16* Tb, cudaStream_t s) {
+  const size_t n = V * static_cast<size_t>(r);
+  k_split3<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(T, V, r, Tb);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_neg_identity3(int r, __nv_bfloat16* M, cudaStream_t s) {
+  k_neg_identity3<<<(3 * r * r + 255) / 256, 256, 0, s>>>(r, M);
   return cudaGetLastError();
 }
 

@@ -628,10 +628,15 @@ __global__ void __launch_bounds__(kPtThreads, 1)
       const int row0 = tile * kTile + q * 32;     // first row of this warp's box
       const bool any = row0 < a.N;
       bool bad = false;
-      if (n < a.N && a.anchor) {
-        const int t = __ldg(a.tids + n);
+      int t = 0;
+      if (n < a.N && (a.anchor || a.Eadd)) {
+        t = __ldg(a.tids + n);
         bad = t < 0 || t >= a.V;
+        if (bad && !a.anchor) atomicOr(a.err, kErrBadToken);   // no builder saw this id
       }
+      // first-boundary anchor: the full embedding row is added in fp32
+      const __nv_bfloat16* erow =
+          (a.Eadd && n < a.N && !bad) ? a.Eadd + static_cast<size_t>(t) * a.d : nullptr;
       for (int c = 0; c < nchunk; ++c, ++cc) {
         const int acc = cc & 1;
         bool ok = mbar_wait(smem_u32(&ctl->tfull[acc]), (cc >> 1) & 1, &ctl->abort, bud);
@@ -644,10 +649,28 @@ __global__ void __launch_bounds__(kPtThreads, 1)
         tc_fence_after();
         for (int c0 = 0; c0 < NC; c0 += 64) {
           float v0[32], v1[32];
+          uint4 ev[8];
+          if (erow) {
+            const uint4* src = reinterpret_cast<const uint4*>(erow + c * NC + c0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ev[j] = __ldg(src + j);
+          }
           __syncwarp();
           tmem_ld32(trow + acc * NC + c0, v0);
           tmem_ld32(trow + acc * NC + c0 + 32, v1);
           tmem_wait_ld();
+          if (erow) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float* vv = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
+              const uint32_t w4[4] = {ev[j].x, ev[j].y, ev[j].z, ev[j].w};
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                vv[2 * h] += __uint_as_float(w4[h] << 16);
+                vv[2 * h + 1] += __uint_as_float(w4[h] & 0xffff0000u);
+              }
+            }
+          }
           if (!any) continue;   // no collective operation follows in this iteration
           if (lane == 0) bulk_wait_read<0>();   // the previous store has read the tile
           __syncwarp();

@@ -36,7 +36,16 @@ struct mapl_plan_s {
   // [P_send as fp32, r x d | S^T, r x r fp32 | E[tids], g_rows x r bf16]
   cublasHandle_t blas = nullptr;
   void* gws = nullptr;
-  int64_t g_rows = 0;
+  int64_t g_rows = 0, g_cols = 0;
+  // sender anchor: E_send[tids] P_send (re = r, three -M terms), or with
+  // mapl_plan_set_embedding_anchor the first-boundary E_emb[tids] (re = 3r,
+  // one term): table [hi|mid|lo] of E_emb A and -[I; I; I]
+  int re = 0, nsplit = kNumSplit;
+  const void* E_emb = nullptr;
+  void* emb_pool = nullptr;           // [T fp32 V x r | table V x 3r bf16 | M r x 3r bf16]
+  float* emb_T = nullptr;
+  __nv_bfloat16* emb_tab = nullptr;
+  CUtensorMap tmMt_emb{};
 };
 
 namespace {
@@ -269,6 +278,7 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   pl->vq = vq;
   pl->tc = cfg->dtype == MAPL_BF16;
   pl->gd = vq ? static_cast<int>(cfg->r / cfg->G) : 0;
+  pl->re = static_cast<int>(cfg->r);
   cudaError_t e = cudaGetDevice(&pl->device);
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&pl->num_sms, cudaDevAttrMultiProcessorCount, pl->device);
@@ -354,6 +364,66 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   return MAPL_OK;
 }
 
+// T = E_emb A (cuBLAS, bf16 in, fp32 out) split into the [hi|mid|lo] table.
+static mapl_status embedding_table(mapl_plan pl, cudaStream_t stream) {
+  const mapl_config& c = pl->cfg;
+  if (!pl->blas && cublasCreate(&pl->blas) != CUBLAS_STATUS_SUCCESS) {
+    pl->blas = nullptr;
+    return fail(MAPL_ERR_CUDA, "cublasCreate failed");
+  }
+  if (cublasSetStream(pl->blas, stream) != CUBLAS_STATUS_SUCCESS)
+    return fail(MAPL_ERR_CUDA, "cublasSetStream failed");
+  // column-major: T^T (r x V) = A^T * E_emb^T, with the plan's row-major
+  // A^T (r x d) read as the column-major d x r matrix A and transposed
+  const float one = 1.f, zero = 0.f;
+  const cublasStatus_t bs = cublasGemmEx(
+      pl->blas, CUBLAS_OP_T, CUBLAS_OP_N, static_cast<int>(c.r), static_cast<int>(c.V),
+      static_cast<int>(c.d), &one, pl->p.At, CUDA_R_16BF, static_cast<int>(c.d), pl->E_emb,
+      CUDA_R_16BF, static_cast<int>(c.d), &zero, pl->emb_T, CUDA_R_32F, static_cast<int>(c.r),
+      CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+  if (bs != CUBLAS_STATUS_SUCCESS) return fail(MAPL_ERR_CUDA, "cuBLAS GEMM failed (%d)", (int)bs);
+  const cudaError_t e = launch_split3(pl->emb_T, static_cast<size_t>(c.V), static_cast<int>(c.r),
+                                      pl->emb_tab, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "embedding anchor table");
+  return MAPL_OK;
+}
+
+mapl_status mapl_plan_set_embedding_anchor(mapl_plan pl, const void* E_emb, cudaStream_t stream) {
+  if (!pl || !E_emb) return fail(MAPL_ERR_INVALID_ARG, "NULL argument");
+  if (!pl->tc) return fail(MAPL_ERR_UNSUPPORTED, "the embedding anchor needs a bf16 plan");
+  if (!aligned16(E_emb)) return fail(MAPL_ERR_INVALID_ARG, "E_emb must be 16-byte aligned");
+  if (3 * pl->cfg.r > 512)
+    return fail(MAPL_ERR_UNSUPPORTED, "the embedding anchor needs r <= 170 (3r table columns)");
+  mapl_status st = check_device(pl);
+  if (st != MAPL_OK) return st;
+  const mapl_config& c = pl->cfg;
+  const size_t r = static_cast<size_t>(c.r), V = static_cast<size_t>(c.V);
+  const size_t oT = 0, oTab = up256(V * r * 4), oM = oTab + up256(V * 3 * r * 2);
+  cudaError_t e;
+  if (!pl->emb_pool) {
+    e = cudaMalloc(&pl->emb_pool, oM + up256(r * 3 * r * 2));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(embedding anchor)");
+  }
+  char* b = static_cast<char*>(pl->emb_pool);
+  pl->emb_T = reinterpret_cast<float*>(b + oT);
+  pl->emb_tab = reinterpret_cast<__nv_bfloat16*>(b + oTab);
+  __nv_bfloat16* M = reinterpret_cast<__nv_bfloat16*>(b + oM);
+  e = launch_neg_identity3(static_cast<int>(r), M, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "embedding anchor operand");
+  const uint32_t nrow = c.r > 256 ? 256u : static_cast<uint32_t>(c.r);
+  if (!make_tmap(&pl->tmMt_emb, M, 3 * r, r, 64, nrow))
+    return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (-[I;I;I])");
+  pl->E_emb = E_emb;
+  st = embedding_table(pl, stream);
+  if (st != MAPL_OK) {
+    pl->E_emb = nullptr;
+    return st;
+  }
+  pl->re = static_cast<int>(3 * r);
+  pl->nsplit = 1;
+  return MAPL_OK;
+}
+
 mapl_status mapl_plan_update_A(mapl_plan pl, const void* A, cudaStream_t stream) {
   if (!pl || !A) return fail(MAPL_ERR_INVALID_ARG, "plan and A must be non-NULL");
   if (!aligned16(A)) return fail(MAPL_ERR_INVALID_ARG, "A must be 16-byte aligned");
@@ -362,6 +432,7 @@ mapl_status mapl_plan_update_A(mapl_plan pl, const void* A, cudaStream_t stream)
   cudaError_t e = pl->tc ? launch_prep_bf16(pl->cfg, A, pl->p.Ps, pl->p.Pr, nullptr, pl->p, true, stream)
                          : launch_prep_f32(pl->cfg, A, pl->p.Ps, pl->p.Pr, nullptr, pl->p, true, stream);
   if (e != cudaSuccess) return cuda_fail(e, "update_A");
+  if (pl->E_emb) return embedding_table(pl, stream);
   return MAPL_OK;
 }
 
@@ -422,6 +493,7 @@ void mapl_plan_destroy(mapl_plan pl) {
   if (!pl) return;
   if (pl->blas) cublasDestroy(pl->blas);
   if (pl->gws) cudaFree(pl->gws);
+  if (pl->emb_pool) cudaFree(pl->emb_pool);
   if (pl->p.pool) cudaFree(pl->p.pool);
   delete pl;
 }
@@ -430,11 +502,12 @@ static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* t
                                    const void* E, void* out, int mode, cudaStream_t stream,
                                    bool anchor = true) {
   if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
-  if (!X || !out || (anchor && (!tids || !E)))
+  const bool own_table = pl->E_emb != nullptr;   // E_send is not read
+  if (!X || !out || (anchor && (!tids || (!E && !own_table))))
     return fail(MAPL_ERR_INVALID_ARG, "NULL tensor pointer");
   if (N < 1 || N > 0x7fffffffLL) return fail(MAPL_ERR_INVALID_ARG, "N must be in [1, 2^31)");
   if (!aligned16(X) || !aligned16(out) ||
-      (anchor && (!aligned16(E) || (reinterpret_cast<uintptr_t>(tids) & 3u))))
+      (anchor && ((!own_table && !aligned16(E)) || (reinterpret_cast<uintptr_t>(tids) & 3u))))
     return fail(MAPL_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned (tids 4-byte)");
   mapl_status st = check_device(pl);
   if (st != MAPL_OK) return st;
@@ -451,8 +524,10 @@ static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* t
   CUtensorMap tmX, tmE;
   if (!make_tmap(&tmX, X, c.d, static_cast<uint64_t>(N), 64, kTile))
     return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (X)");
+  const bool emb = anchor && pl->E_emb != nullptr;
+  if (emb) E = pl->emb_tab;   // first-boundary anchor: the plan's own table
   if (anchor) {
-    if (!make_tmap(&tmE, E, c.r, static_cast<uint64_t>(c.V), 64, 1))
+    if (!make_tmap(&tmE, E, static_cast<uint64_t>(pl->re), static_cast<uint64_t>(c.V), 64, 1))
       return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (E)");
   } else {
     tmE = tmX;   // unused
@@ -460,6 +535,8 @@ static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* t
   CompressArgs a{};
   a.tids = tids;
   a.E = reinterpret_cast<const __nv_bfloat16*>(E);
+  a.re = pl->re;
+  a.nsplit = pl->nsplit;
   a.Cb = pl->p.Cb;
   a.cnorm = pl->p.cnorm;
   a.cmax = pl->p.cmax;
@@ -480,7 +557,8 @@ static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* t
   a.timeout_ns = pl->timeout_ns;
   const int ntiles = static_cast<int>((N + kTile - 1) / kTile);
   const int grid = ntiles < pl->num_sms ? ntiles : pl->num_sms;
-  e = launch_compress_tc(tmX, pl->tmAt, pl->tmMt, pl->tmC, tmE, a, pl->c_smem, grid, stream);
+  e = launch_compress_tc(tmX, pl->tmAt, emb ? pl->tmMt_emb : pl->tmMt, pl->tmC, tmE, a,
+                         pl->c_smem, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "compress launch");
   return MAPL_OK;
 }
@@ -503,11 +581,13 @@ static mapl_status decompress_common(mapl_plan pl, const void* payload, const in
                                      int64_t N, const void* E_recv, void* X_hat,
                                      cudaStream_t stream, bool anchor) {
   if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
-  if (!payload || !X_hat || (anchor && (!tids || !E_recv)))
+  // first-boundary anchor: X_hat = Z_hat A^T + E_emb[tids], E_recv not read
+  const bool emb = anchor && pl->E_emb != nullptr;
+  if (!payload || !X_hat || (anchor && (!tids || (!E_recv && !emb))))
     return fail(MAPL_ERR_INVALID_ARG, "NULL tensor pointer");
   if (N < 1 || N > 0x7fffffffLL) return fail(MAPL_ERR_INVALID_ARG, "N must be in [1, 2^31)");
   if (!aligned16(payload) || !aligned16(X_hat) ||
-      (anchor && (!aligned16(E_recv) || (reinterpret_cast<uintptr_t>(tids) & 3u))))
+      (anchor && ((!emb && !aligned16(E_recv)) || (reinterpret_cast<uintptr_t>(tids) & 3u))))
     return fail(MAPL_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned (tids 4-byte)");
   mapl_status st = check_device(pl);
   if (st != MAPL_OK) return st;
@@ -545,7 +625,8 @@ static mapl_status decompress_common(mapl_plan pl, const void* payload, const in
   a.K = c.K;
   a.gd = pl->gd;
   a.vq = vq ? 1 : 0;
-  a.anchor = anchor ? 1 : 0;
+  a.anchor = anchor && !emb ? 1 : 0;
+  a.Eadd = emb ? reinterpret_cast<const __nv_bfloat16*>(pl->E_emb) : nullptr;
   a.a_stream = pl->d_stream ? 1 : 0;
   a.nc = static_cast<int>(pl->d_nc);
   a.nab = pl->d_nab;
@@ -556,7 +637,7 @@ static mapl_status decompress_common(mapl_plan pl, const void* payload, const in
   const int ntiles = static_cast<int>((N + kTile - 1) / kTile);
   if (pl->d_nab > 0) {
     CUtensorMap tmE = tmZ;   // unused without the anchor
-    if (anchor && !make_tmap(&tmE, E_recv, c.r, static_cast<uint64_t>(c.V), 64, 1))
+    if (a.anchor && !make_tmap(&tmE, E_recv, c.r, static_cast<uint64_t>(c.V), 64, 1))
       return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (E')");
     CUtensorMap tmXh;
     if (!make_tmap(&tmXh, X_hat, c.d, static_cast<uint64_t>(N), 64, 32))
@@ -564,6 +645,7 @@ static mapl_status decompress_common(mapl_plan pl, const void* payload, const in
     const int grid = ntiles < pl->num_sms ? ntiles : pl->num_sms;
     e = launch_decompress_pt(pl->tmB, tmZ, tmE, tmXh, a, pl->d_smem, grid, stream);
   } else {
+    if (emb) return fail(MAPL_ERR_UNSUPPORTED, "the embedding anchor needs the persistent decompress");
     e = launch_decompress_tc(pl->tmB, tmZ, a, pl->d_smem, ntiles, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "decompress launch");
@@ -590,16 +672,18 @@ mapl_status mapl_grad_A(mapl_plan pl, const void* X, const int32_t* tids, const 
                         const void* gZ, const void* gX_hat, const void* Z, int64_t N, float* dA,
                         cudaStream_t stream) {
   if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
-  if (!X || !tids || !E_send || !gZ || !gX_hat || !Z || !dA)
+  const bool emb = pl->E_emb != nullptr;   // first-boundary anchor: E_send is not read
+  if (!X || !tids || (!E_send && !emb) || !gZ || !gX_hat || !Z || !dA)
     return fail(MAPL_ERR_INVALID_ARG, "NULL tensor pointer");
   if (N < 1 || N > 0x7fffffffLL) return fail(MAPL_ERR_INVALID_ARG, "N must be in [1, 2^31)");
   if (!pl->tc) return fail(MAPL_ERR_UNSUPPORTED, "gradient calls need a bf16 (tensor-core) plan");
-  if (!aligned16(E_send)) return fail(MAPL_ERR_INVALID_ARG, "E_send must be 16-byte aligned");
+  if (!emb && !aligned16(E_send)) return fail(MAPL_ERR_INVALID_ARG, "E_send must be 16-byte aligned");
   mapl_status st = check_device(pl);
   if (st != MAPL_OK) return st;
   const mapl_config& c = pl->cfg;
   const size_t r = static_cast<size_t>(c.r), d = static_cast<size_t>(c.d);
   const size_t oP = 0, oT = up256(r * d * 4), oEg = oT + up256(r * r * 4);
+  const int64_t gcols = emb ? c.d : c.r;   // columns of the gathered anchor rows
   cudaError_t e;
   if (!pl->blas) {
     if (cublasCreate(&pl->blas) != CUBLAS_STATUS_SUCCESS) {
@@ -607,16 +691,17 @@ mapl_status mapl_grad_A(mapl_plan pl, const void* X, const int32_t* tids, const 
       return fail(MAPL_ERR_CUDA, "cublasCreate failed");
     }
   }
-  if (!pl->gws || pl->g_rows < N) {
-    // scratch sized for N rows of E[tids]; P_send is widened once per buffer
+  if (!pl->gws || pl->g_rows < N || pl->g_cols < gcols) {
+    // scratch sized for N gathered anchor rows; P_send is widened once per buffer
     e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     if (pl->gws) cudaFree(pl->gws);
     pl->gws = nullptr;
     pl->g_rows = 0;
-    e = cudaMalloc(&pl->gws, oEg + up256(static_cast<size_t>(N) * r * 2));
+    e = cudaMalloc(&pl->gws, oEg + up256(static_cast<size_t>(N) * gcols * 2));
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(gradient scratch)");
     pl->g_rows = N;
+    pl->g_cols = gcols;
     e = launch_widen(reinterpret_cast<const __nv_bfloat16*>(pl->p.Ps), r * d,
                      reinterpret_cast<float*>(static_cast<char*>(pl->gws) + oP), stream);
     if (e != cudaSuccess) return cuda_fail(e, "widen P_send");
@@ -625,12 +710,31 @@ mapl_status mapl_grad_A(mapl_plan pl, const void* X, const int32_t* tids, const 
   float* P32 = reinterpret_cast<float*>(ws + oP);
   float* T = reinterpret_cast<float*>(ws + oT);
   __nv_bfloat16* Eg = reinterpret_cast<__nv_bfloat16*>(ws + oEg);
-  e = launch_gather_rows(tids, reinterpret_cast<const __nv_bfloat16*>(E_send),
-                         static_cast<int>(N), static_cast<int>(c.V), static_cast<int>(r), Eg,
+  e = launch_gather_rows(tids, reinterpret_cast<const __nv_bfloat16*>(emb ? pl->E_emb : E_send),
+                         static_cast<int>(N), static_cast<int>(c.V), static_cast<int>(gcols), Eg,
                          stream);
   if (e != cudaSuccess) return cuda_fail(e, "gather E[tids]");
   if (cublasSetStream(pl->blas, stream) != CUBLAS_STATUS_SUCCESS)
     return fail(MAPL_ERR_CUDA, "cublasSetStream failed");
+  if (emb) {
+    // Z = (X - E_emb[tids]) A, X_hat = Z_hat A^T + E_emb[tids]:
+    //   dA^T (r x d) = gZ^T X - gZ^T E_emb[tids] + Z^T gX_hat
+    const int m = static_cast<int>(r), n = static_cast<int>(d), k = static_cast<int>(N);
+    const float one = 1.f, zero = 0.f, minus = -1.f;
+    cublasStatus_t bs = cublasGemmEx(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, n, k, &one, gZ,
+                                     CUDA_R_16BF, m, X, CUDA_R_16BF, n, &zero, dA, CUDA_R_32F, m,
+                                     CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+    if (bs == CUBLAS_STATUS_SUCCESS)
+      bs = cublasGemmEx(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, n, k, &minus, gZ, CUDA_R_16BF, m,
+                        Eg, CUDA_R_16BF, n, &one, dA, CUDA_R_32F, m, CUBLAS_COMPUTE_32F,
+                        CUBLAS_GEMM_DEFAULT);
+    if (bs == CUBLAS_STATUS_SUCCESS)
+      bs = cublasGemmEx(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, n, k, &one, Z, CUDA_R_16BF, m,
+                        gX_hat, CUDA_R_16BF, n, &one, dA, CUDA_R_32F, m, CUBLAS_COMPUTE_32F,
+                        CUBLAS_GEMM_DEFAULT);
+    if (bs != CUBLAS_STATUS_SUCCESS) return fail(MAPL_ERR_CUDA, "cuBLAS GEMM failed (%d)", (int)bs);
+    return MAPL_OK;
+  }
   // Everything column-major (the row-major tensors read transposed):
   //   dA^T (r x d)  = gZ^T X + Z^T gX_hat - (E[tids]^T gZ)^T P
   //   T = S^T (r x r) = gZ^T E[tids]

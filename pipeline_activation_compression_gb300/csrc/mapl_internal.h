@@ -55,6 +55,8 @@ struct CompressArgs {
   int N, d, r, V, G, R, K, gd;
   int mode;
   int anchor;                       // 0: no anchor term (backward pass: gZ = dX_hat A)
+  int re;                           // columns of the anchor table E (multiple of 64)
+  int nsplit;                       // bf16 terms of -M (re x r) in the folded anchor
   int nstage;
   uint32_t stage_bytes;
   uint64_t timeout_ns;
@@ -73,6 +75,7 @@ struct DecompressArgs {
   int nc;                           // output columns per accumulator chunk
   int nab;                          // A operand buffers (persistent kernel)
   int anchor;                       // 0: no E' term (backward pass: dX = gZ A^T)
+  const __nv_bfloat16* Eadd;        // V x d rows added to X_hat (first-boundary anchor) or null
   int nstage;
   uint32_t stage_bytes;
   uint32_t a_bytes;                 // resident A operand bytes (0 when streamed)
@@ -105,6 +108,10 @@ cudaError_t launch_decompress_pt(const CUtensorMap& tmB, const CUtensorMap& tmZ,
 cudaError_t launch_gather_rows(const int32_t* tids, const __nv_bfloat16* E, int N, int V, int r,
                                __nv_bfloat16* Eg, cudaStream_t s);
 cudaError_t launch_widen(const __nv_bfloat16* a, size_t n, float* b, cudaStream_t s);
+// First-boundary anchor: T (V x r fp32) -> [hi | mid | lo] bf16 (V x 3r), and
+// the r x 3r operand -[I; I; I]^T.
+cudaError_t launch_split3(const float* T, size_t V, int r, __nv_bfloat16* Tb, cudaStream_t s);
+cudaError_t launch_neg_identity3(int r, __nv_bfloat16* M, cudaStream_t s);
 cudaError_t launch_decompress_tc(const CUtensorMap& tmB, const CUtensorMap& tmZ,
                                  const DecompressArgs& a, uint32_t smem_bytes, int grid,
                                  cudaStream_t s);

@@ -26,6 +26,10 @@ Workload recipe (stated in full so it can be re-derived):
   residual for rho = 0, the round-1 residual for rho = 1); those two numbers
   were measured once with the fp64 oracle on a 4096-token sample of each
   workload by ``tests/golden/make_codebook_rms.py`` and are stored below.
+* First boundary (``make_first_boundary``): the anchor is a full V x d token
+  embedding ``E_emb`` with N(0, 1) entries; ``X = E_emb[tids]`` + the same
+  kind of unit-RMS rank-R signal + ``0.05 * N(0,1)`` noise, drawn from a
+  stream of their own; tids, A and C are those of ``make_boundary``.
 * SPEL gradients: N(0, 1e-3) entries, a fresh draw each step.
 
 Storage: fp32 workloads keep every tensor in float32.  bf16 workloads round
@@ -42,7 +46,7 @@ import numpy as np
 
 __all__ = [
     "Workload", "WORKLOADS", "SPEL_WORKLOADS", "SpelWorkload", "make_boundary",
-    "make_spel", "spel_gradients", "bf16_bits", "bf16_to_f64", "widen",
+    "make_first_boundary", "make_spel", "spel_gradients", "bf16_bits", "bf16_to_f64", "widen",
 ]
 
 # order of the SeedSequence children; never reorder (it would change inputs)
@@ -237,6 +241,34 @@ def make_boundary_grad(w: Workload | str, seed: int = 0, n_tokens: int | None = 
     n = w.N if n_tokens is None else int(n_tokens)
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 7, 1]).spawn(1)[0]))
     return _store(scale * rng.standard_normal((n, w.d)), w.dtype)
+
+
+def make_first_boundary(w: Workload | str, seed: int = 0, n_tokens: int | None = None,
+                        emb_std: float = 1.0) -> dict:
+    """Inputs of the first boundary, where the anchor is the full token
+    embedding (V x d) rather than a low-rank factor.
+
+    Same shapes, token law, projector and codebooks as ``make_boundary`` for
+    the same seed; E_emb ~ emb_std * N(0, 1) from its own seeded stream, and
+    X = E_emb[tids] + signal (unit RMS, rank ``signal_rank``) + 0.05 noise:
+    right after the first stage the residual stream still carries the
+    embedding at full strength.  Returns X, tids, A, E_emb (and C with VQ).
+    """
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    base = make_boundary(w, seed=seed, n_tokens=n_tokens)
+    n = base["X"].shape[0]
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 11, 1]).spawn(1)[0]))
+    st = lambda x: _store(x, w.dtype)
+    E_emb = st(emb_std * rng.standard_normal((w.V, w.d)))
+    k = min(w.signal_rank, w.d)
+    sig = rng.standard_normal((n, k)) @ rng.standard_normal((k, w.d))
+    rms = np.sqrt(np.mean(sig * sig)) if sig.size else 1.0
+    X = widen(E_emb)[base["tids"]] + sig / rms + 0.05 * rng.standard_normal((n, w.d))
+    out = dict(X=st(X), tids=base["tids"], A=base["A"], E_emb=E_emb)
+    if w.vq:
+        out["C"] = base["C"]
+    return out
 
 
 def make_spel(w: SpelWorkload | str, seed: int = 0) -> dict:

@@ -372,6 +372,75 @@ def pin_grad_finite_differences(o):
     assert np.max(np.abs(given - gA)) < 1e-7 * max(1.0, np.max(np.abs(gA)))
 
 
+# ------------------------------------------- Fig. 2 first-boundary anchor
+def pin_embed_exact_reconstruction(o):
+    """Fig. 2 (first boundary): an activation that is its token's embedding
+    plus a component S A^T inside span(A) is sent as exactly S and rebuilt
+    exactly; a component orthogonal to span(A) is dropped, so X_hat is the
+    orthogonal projection of X - E_emb[t] onto span(A) plus E_emb[t]."""
+    rng = np.random.default_rng(41)
+    d, r, V, n = 24, 6, 9, 11
+    A = _orth(rng, d, r)
+    E = rng.standard_normal((V, d))
+    t = rng.integers(0, V, n)
+    S = rng.standard_normal((n, r))
+    X = E[t] + S @ A.T
+    Z = o.compress_embed(X, t, A, E)
+    assert np.max(np.abs(Z - S)) < 1e-12
+    assert np.max(np.abs(o.reconstruct_embed(Z, t, A, E) - X)) < 1e-12
+    # off-subspace part: lstsq projection of the residual onto span(A)
+    Y = rng.standard_normal((n, d))
+    coef = np.linalg.lstsq(A, (Y - E[t]).T, rcond=None)[0]
+    Xh = o.reconstruct_embed(o.compress_embed(Y, t, A, E), t, A, E)
+    assert np.max(np.abs(Xh - (E[t] + (A @ coef).T))) < 1e-12
+
+
+def pin_embed_one_hot(o):
+    """A one-hot embedding row: token v's anchor is e_j, so token v's Z row is
+    X A minus row j of A; tokens are looked up by id, not by position."""
+    d, r, V = 8, 3, 4
+    rng = np.random.default_rng(43)
+    A = _orth(rng, d, r)
+    E = np.zeros((V, d))
+    for v in range(V):
+        E[v, (3 * v + 1) % d] = 1.0
+    t = np.array([2, 0, 3, 3, 1])
+    X = rng.standard_normal((len(t), d))
+    Z = o.compress_embed(X, t, A, E)
+    for i, v in enumerate(t):
+        expect = X[i] @ A - A[(3 * v + 1) % d]
+        assert np.max(np.abs(Z[i] - expect)) < 1e-14
+    Xh = o.reconstruct_embed(np.zeros((len(t), r)), t, A, E)
+    for i, v in enumerate(t):
+        assert Xh[i, (3 * v + 1) % d] == 1.0 and np.count_nonzero(Xh[i]) == 1
+
+
+def pin_embed_grad_finite_differences(o):
+    """grad_A_embed is the derivative in A of <W, X_hat(A)> for the
+    first-boundary codec X_hat = (X - E_emb[t]) A A^T + E_emb[t]; the loss is
+    quadratic in A, so central differences are exact up to rounding."""
+    rng = np.random.default_rng(47)
+    d, r, V, n = 7, 3, 5, 6
+    A = _orth(rng, d, r)
+    E = rng.standard_normal((V, d))
+    X, W = rng.standard_normal((n, d)), rng.standard_normal((n, d))
+    t = rng.integers(0, V, n)
+
+    def loss(Am):
+        return float(np.sum(W * o.reconstruct_embed(o.compress_embed(X, t, Am, E), t, Am, E)))
+
+    h = 1e-4
+    gA = np.zeros_like(A)
+    for i in range(d):
+        for j in range(r):
+            Ap, Am = A.copy(), A.copy()
+            Ap[i, j] += h
+            Am[i, j] -= h
+            gA[i, j] = (loss(Ap) - loss(Am)) / (2 * h)
+    got = o.grad_A_embed(X, t, E, W @ A, W, o.compress_embed(X, t, A, E))
+    assert np.max(np.abs(got - gA)) < 1e-7 * max(1.0, np.max(np.abs(gA)))
+
+
 # ------------------------------------------------- §3.5 codebook streaming
 def pin_splitmix64_reference(o):
     """Published first outputs of splitmix64 from state 0 (Vigna's reference

@@ -34,9 +34,15 @@ MUTANTS = {
     "spel_step_sign": ("A_new = polar_express(_f64(A) - lr * d, coeffs_retr)", "A_new = polar_express(_f64(A) + lr * d, coeffs_retr)"),
     "spel_no_retraction": ("A_new = polar_express(_f64(A) - lr * d, coeffs_retr)", "A_new = _f64(A) - lr * d"),
     "spel_raw_gradient": ("m_new = momentum(m, gR, beta)", "m_new = momentum(m, g, beta)"),
+    "embed_anchor_sign": ("return (X - E_emb[np.asarray(tids, dtype=np.int64)]) @ A", "return (X + E_emb[np.asarray(tids, dtype=np.int64)]) @ A"),
+    "embed_anchor_projected_twice": ("return (X - E_emb[np.asarray(tids, dtype=np.int64)]) @ A", "return X @ A - (E_emb[np.asarray(tids, dtype=np.int64)] @ A) @ (A.T @ A) * 0.5"),
+    "embed_recon_no_anchor": ("return Zhat @ A.T + E_emb[np.asarray(tids, dtype=np.int64)]", "return Zhat @ A.T"),
+    "embed_recon_positional": ("return Zhat @ A.T + E_emb[np.asarray(tids, dtype=np.int64)]", "return Zhat @ A.T + E_emb[np.arange(Zhat.shape[0]) % E_emb.shape[0]]"),
+    "embed_gradA_raw_X": ("    Xres = _f64(X) - _f64(E_emb)[np.asarray(tids, dtype=np.int64)]\n    return Xres.T", "    Xres = _f64(X)\n    return Xres.T"),
+    "embed_gradA_term_dropped": ("    return Xres.T @ _f64(gZ) + _f64(gXhat).T @ _f64(Z)\n\n\n# ----", "    return Xres.T @ _f64(gZ)\n\n\n# ----"),
     "gradA_term_dropped": ("return Xres.T @ (g @ A) + g.T @ (Xres @ A)", "return Xres.T @ (g @ A)"),
     "gradA_no_anchor": ("    Xres = _f64(X) - anchor(E, P, tids)\n    A, g = _f64(A), _f64(gXhat)", "    Xres = _f64(X)\n    A, g = _f64(A), _f64(gXhat)"),
-    "gradA_given_raw_X": ("    return Xres.T @ _f64(gZ) + _f64(gXhat).T @ _f64(Z)", "    return _f64(X).T @ _f64(gZ) + _f64(gXhat).T @ _f64(Z)"),
+    "gradA_given_raw_X": ("    Xres = _f64(X) - anchor(E, P, tids)\n    return Xres.T @ _f64(gZ)", "    Xres = _f64(X) - anchor(E, P, tids)\n    return _f64(X).T @ _f64(gZ)"),
     "grad_decompress_no_T": ("return _f64(gZ) @ _f64(A).T", "return _f64(gZ) @ _f64(A).T * 2.0"),
     "splitmix_shift": ("z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _M64", "z = ((z ^ (z >> 26)) * 0x94D049BB133111EB) & _M64"),
     "subset_same_epoch": ("state = (seed ^ ((0xD1B54A32D192ED03 * (epoch + 1)) & _M64)) & _M64", "state = seed"),
@@ -47,7 +53,7 @@ MUTANTS = {
 
 def _mutant(old, new):
     src = inspect.getsource(real)
-    assert src.count(old) >= 1, old
+    assert src.count(old) == 1, old
     src = src.replace(old, new, 1)
     mod = types.ModuleType("oracle_mutant")
     exec(compile(src, "oracle_mutant", "exec"), mod.__dict__)

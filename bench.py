@@ -404,6 +404,40 @@ def run_ours(args, ws, rank):
         s1.record(stream)
         torch.cuda.synchronize()
         spel[sname + "_us"] = s0.elapsed_time(s1) / ns * 1e3
+        if sname == "spel_d1024_r256":
+            # the projector broadcast: three bf16 plans of this (d, r)
+            # refreshed by the step itself, against the step followed by one
+            # mapl_plan_update_A per boundary
+            wr = synth.WORKLOADS["proj_d1024_r256"]
+            br = synth.make_boundary(wr, n_tokens=8)
+            cfg_r = mapl.make_config(wr.d, wr.r, wr.V, dtype=mapl.MAPL_BF16)
+            plans_r = [mapl.mapl_plan_create(cfg_r, to_dev(br["A"]), to_dev(br["P"]),
+                                             to_dev(br["P_next"])) for _ in range(sw.batch)]
+            Ab = torch.empty(sw.batch, sw.d, sw.r, dtype=torch.bfloat16, device="cuda")
+
+            def separate():
+                mapl.mapl_spel_step(As, Gs, ms, sw.lr, sw.beta, co, 5, 5, wsp_s, stream)
+                Ab.copy_(As)
+                for q in range(sw.batch):
+                    mapl.mapl_plan_update_A(plans_r[q], Ab[q], stream)
+
+            def fused():
+                mapl.mapl_spel_step_refresh(As, Gs, ms, sw.lr, sw.beta, co, 5, 5, plans_r,
+                                            wsp_s, stream)
+
+            for key, fn in (("spel_then_update_A_x3_us", separate),
+                            ("spel_step_refresh_x3_us", fused)):
+                for _ in range(3):
+                    fn()
+                torch.cuda.synchronize()
+                s0.record(stream)
+                for _ in range(ns):
+                    fn()
+                s1.record(stream)
+                torch.cuda.synchronize()
+                spel[key] = s0.elapsed_time(s1) / ns * 1e3
+            for pr in plans_r:
+                pr.destroy()
     A_dev = to_dev(b["A"])
     for _ in range(3):
         mapl.mapl_plan_update_A(plan, A_dev, stream)
@@ -416,7 +450,8 @@ def run_ours(args, ws, rank):
     torch.cuda.synchronize()
     spel["plan_update_A_us"] = s0.elapsed_time(s1) / 20 * 1e3
     spel["note"] = ("one SPEL step for a batch of 3 boundaries (5 LMO + 5 retraction "
-                    "PolarExpress iterations, fp32); plan refresh after an A update")
+                    "PolarExpress iterations, fp32); plan refresh after an A update; the "
+                    "step with the projector broadcast to 3 bf16 plans, separate vs fused")
     mapl.mapl_check(plan)
 
     # first-boundary anchor (the full token embedding E_emb, V x d): the same

@@ -268,6 +268,25 @@ mapl_status mapl_spel_step(float* A, const float* G, float* m, int64_t d, int64_
                            size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * mapl_spel_step_refresh -- mapl_spel_step, then the projector broadcast of
+ * §3.3 ("the updated A_p is sent to the next stage after every optimizer
+ * step") applied to the codec plans on this device: plans[b] (NULL to skip
+ * boundary b) takes bf16(A[b]) (round to nearest even) as its projector, with
+ * the same result as mapl_plan_update_A(plans[b], bf16(A[b])).  The final
+ * retraction product writes the plans' A^T and [A | P_recv^T] operands in its
+ * epilogue and one launch forms M = P_send A for every plan, so the refresh
+ * adds no pass over A.  Embedding-anchor plans also recompute E_emb A.
+ *   plans  HOST array of `batch` plan handles; bf16 plans with this (d, r),
+ *          each at most once.  batch <= 16.
+ * Other arguments and requirements as mapl_spel_step.  Async.
+ * Errors: INVALID_ARG, UNSUPPORTED (f32 plan, batch > 16), CUDA.
+ */
+mapl_status mapl_spel_step_refresh(float* A, const float* G, float* m, int64_t d, int64_t r,
+                                   int32_t batch, float lr, float beta, const float* coeffs,
+                                   int32_t n_lmo, int32_t n_retr, const mapl_plan* plans,
+                                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * mapl_spel_step_static -- the SPEL step above without a caller workspace.
  * The MAPL paper has no counterpart; this entry exists for callers that
  * cannot allocate device memory when they run the update: a framework whose

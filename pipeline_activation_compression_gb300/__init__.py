@@ -22,7 +22,8 @@ __all__ = [
     "mapl_host_workspace_size", "mapl_compress_host", "mapl_decompress_host",
     "mapl_grad_compress", "mapl_grad_decompress", "mapl_grad_A",
     "mapl_stream_subset", "mapl_plan_update_codes",
-    "mapl_spel_workspace_size", "mapl_spel_step", "mapl_spel_step_static", "mapl_last_error",
+    "mapl_spel_workspace_size", "mapl_spel_step", "mapl_spel_step_refresh",
+    "mapl_spel_step_static", "mapl_last_error",
     "mapl_version",
     "MAPL_F32", "MAPL_BF16", "STATUS",
 ]
@@ -89,6 +90,8 @@ def load_library():
                            P, SZ, P],
         "mapl_spel_step_static": [P, P, P, I64, I64, I32, ctypes.c_float, ctypes.c_float, P,
                                   I32, I32, P],
+        "mapl_spel_step_refresh": [P, P, P, I64, I64, I32, ctypes.c_float, ctypes.c_float, P,
+                                   I32, I32, P, P, SZ, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -351,6 +354,25 @@ def mapl_spel_step(A, G, m, lr: float, beta: float, coeffs, n_lmo: int, n_retr: 
         d, r, b, float(lr), float(beta), co.ctypes.data_as(ctypes.c_void_p), int(n_lmo),
         int(n_retr), _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def mapl_spel_step_refresh(A, G, m, lr: float, beta: float, coeffs, n_lmo: int, n_retr: int,
+                           plans, workspace, stream=None):
+    """mapl_spel_step, then plans[b] (a Plan or None per boundary) refreshed
+    from bf16(A[b]) by the same launches (see include/mapl.h)."""
+    import torch
+    co = np.ascontiguousarray(np.asarray(coeffs, dtype=np.float32).reshape(-1))
+    if co.size != 3 * (n_lmo + n_retr):
+        raise ValueError("coeffs must hold (n_lmo + n_retr) rows of (a, b, c)")
+    b, d, r = A.shape
+    if len(plans) != b:
+        raise ValueError("plans must hold one entry (Plan or None) per boundary")
+    handles = (ctypes.c_void_p * b)(*[None if p is None else p.handle for p in plans])
+    _check(load_library().mapl_spel_step_refresh(
+        _ptr(A, torch.float32, "A"), _ptr(G, torch.float32, "G"), _ptr(m, torch.float32, "m"),
+        d, r, b, float(lr), float(beta), co.ctypes.data_as(ctypes.c_void_p), int(n_lmo),
+        int(n_retr), ctypes.cast(handles, ctypes.c_void_p), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def mapl_spel_step_static(A, G, m, lr: float, beta: float, coeffs, n_lmo: int, n_retr: int,

@@ -41,29 +41,45 @@ __device__ __forceinline__ void two_sum_f(float a, float b, float& s, float& e) 
 // k in its eighth of [0, d) with four independent compensated sums (k mod 4),
 // each term an exact product split by fma; the pairs are combined in shared
 // memory.
-__global__ void __launch_bounds__(256) k_prep_M(const void* Ps, const void* A, int d, int r,
-                                                bool bf, __nv_bfloat16* Mts, float* M32) {
+// a_round: A is fp32 and enters as its bf16 rounding (RNE), i.e. the value a
+// bf16 plan would have been given.
+__device__ __forceinline__ void prep_M_block(const void* Ps, const void* A, int d, int r, bool bf,
+                                             bool a_round, __nv_bfloat16* Mts, float* M32) {
   __shared__ float ph[8][32], pl[8][32];
   const int nj = (r + 31) / 32;
   const int i = blockIdx.x / nj, j = (blockIdx.x % nj) * 32 + (threadIdx.x & 31);
   const int w = threadIdx.x >> 5;
   const int kc = (d + 7) / 8, kb = w * kc, ke = min(d, kb + kc);
   float h[4] = {0.f, 0.f, 0.f, 0.f}, l[4] = {0.f, 0.f, 0.f, 0.f};
-  if (j < r) {
-    for (int k0 = kb; k0 < ke; k0 += 4) {
+  // 32 k per pass: lane q fetches P[i][k0 + q] (coalesced, then broadcast by
+  // shuffle) and every lane its 32 A values, all loads in flight together.
+  // Terms past the end are 0 * 0, which leaves a compensated sum unchanged,
+  // so chain k mod 4 sees the same terms in the same order as a plain loop.
+  const int lane = threadIdx.x & 31;
+  const bool jv = j < r;
+  for (int k0 = kb; k0 < ke; k0 += 32) {
+    const int kp = k0 + lane;
+    const float pv = kp < ke ? ld_f32(Ps, static_cast<size_t>(i) * d + kp, bf) : 0.f;
+    float av[32];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int k = k0 + u;
-        if (k < ke) {
-          const float a = ld_f32(Ps, static_cast<size_t>(i) * d + k, bf);
-          const float b = ld_f32(A, static_cast<size_t>(k) * r + j, bf);
-          const float p = a * b, pe = fmaf(a, b, -p);
-          float t, te;
-          two_sum_f(h[u], p, t, te);
-          h[u] = t;
-          l[u] += te + pe;
-        }
+    for (int u = 0; u < 32; ++u) {
+      const int k = k0 + u;
+      float b = 0.f;
+      if (jv && k < ke) {
+        const size_t x = static_cast<size_t>(k) * r + j;
+        b = a_round ? __bfloat162float(__float2bfloat16_rn(static_cast<const float*>(A)[x]))
+                    : ld_f32(A, x, bf);
       }
+      av[u] = b;
+    }
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      const float a = __shfl_sync(0xffffffffu, pv, u);
+      const float p = a * av[u], pe = fmaf(a, av[u], -p);
+      float t, te;
+      two_sum_f(h[u & 3], p, t, te);
+      h[u & 3] = t;
+      l[u & 3] += te + pe;
     }
   }
   float s01, e01, s23, e23, hi, e;
@@ -98,6 +114,20 @@ __global__ void __launch_bounds__(256) k_prep_M(const void* Ps, const void* A, i
       vl = te;
     }
   }
+}
+
+__global__ void __launch_bounds__(256) k_prep_M(const void* Ps, const void* A, int d, int r,
+                                                bool bf, __nv_bfloat16* Mts, float* M32) {
+  prep_M_block(Ps, A, d, r, bf, false, Mts, M32);
+}
+
+// one grid row (blockIdx.y) per boundary of a SPEL batch
+__global__ void __launch_bounds__(256) k_prep_M_refresh(RefreshTable rt, const float* A, int d,
+                                                        int r) {
+  const int z = blockIdx.y;
+  if (z >= rt.n || rt.Mts[z] == nullptr) return;
+  prep_M_block(rt.Ps[z], A + static_cast<size_t>(z) * d * r, d, r, true, true, rt.Mts[z],
+               nullptr);
 }
 
 __global__ void k_prep_At(const __nv_bfloat16* A, int d, int r, __nv_bfloat16* At) {
@@ -281,6 +311,12 @@ cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps
         C, nb, c.K, gd, true, p.Cb, nullptr, p.cnorm);
     k_prep_cmax<<<blocks_for(nb, 64), 64, 0, s>>>(p.cnorm, nb, c.K, p.cmax);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep_M_refresh(const RefreshTable& rt, const float* A, int d, int r,
+                                  cudaStream_t s) {
+  k_prep_M_refresh<<<dim3(r * ((r + 31) / 32), rt.n), 256, 0, s>>>(rt, A, d, r);
   return cudaGetLastError();
 }
 

@@ -19,7 +19,7 @@ namespace {
 
 constexpr int BK = 16;
 
-enum Epi { kStore = 0, kMomentum = 1, kPoly = 2 };
+enum Epi { kStore = 0, kMomentum = 1, kPoly = 2, kRefresh = 3 };
 
 struct EpiArgs {
   const float* G;     // kMomentum: gradient
@@ -27,6 +27,7 @@ struct EpiArgs {
   const float* S;     // kPoly: S
   float beta, a, b, c;
   long sG, sm, sS;    // batch strides
+  RefreshTable rt;    // kRefresh: bf16 plan operands written beside C
 };
 
 // C[z] = op(A) B for z = blockIdx.z / ksplit; with ksplit > 1 each split
@@ -149,6 +150,15 @@ __global__ void __launch_bounds__(64)
       const long o = static_cast<long>(gm) * N + gn;
       if (EPI == kStore) {
         C[z * sC + static_cast<long>(ks) * M * N + o] = acc[i][j];
+      } else if (EPI == kRefresh) {
+        // the new A (M = d rows, N = r columns) and, for a refreshed plan,
+        // its bf16 rounding as A^T (r x d) and as columns [0, r) of [A | P^T]
+        C[z * sC + o] = acc[i][j];
+        if (z < e.rt.n && e.rt.At[z] != nullptr) {
+          const __nv_bfloat16 v = __float2bfloat16_rn(acc[i][j]);
+          e.rt.At[z][static_cast<long>(gn) * M + gm] = v;
+          e.rt.Bcat[z][static_cast<long>(gm) * 2 * N + gn] = v;
+        }
       } else if (EPI == kMomentum) {
         float* mp = e.m + z * e.sm + o;
         const float gR = e.G[z * e.sG + o] - acc[i][j];
@@ -280,9 +290,10 @@ Ws carve(void* ws, int d, int r, int batch) {
   return w;
 }
 
-// Y_out = Y_in (a I + b S + c S^2), S = Y_in^T Y_in
+// Y_out = Y_in (a I + b S + c S^2), S = Y_in^T Y_in; with rt the final
+// product also writes the refreshed plans' bf16 operands
 void pe_step(const float* Yin, float* Yout, const float* co, const Ws& w, int d, int r,
-             int batch, cudaStream_t s) {
+             int batch, cudaStream_t s, const RefreshTable* rt = nullptr) {
   EpiArgs none{};
   k_sgemm<true, kStore, TM><<<gemm_grid(r, r, batch * w.ks), 64, 0, s>>>(
       Yin, Yin, w.part, r, r, d, r, r, w.dr, w.dr, w.rr * w.ks, w.ks, none);
@@ -295,9 +306,29 @@ void pe_step(const float* Yin, float* Yout, const float* co, const Ws& w, int d,
       w.S, w.S, w.part, r, r, r, r, r, w.rr, w.rr, w.rr * w.ks, kr, none);
   k_reduce_poly<<<dim3((r * r + 255) / 256, batch), 256, 0, s>>>(
       w.part, w.S, w.Q, r, kr, co[0], co[1], co[2], w.rr * w.ks, w.rr);
-  k_sgemm<false, kStore, TM><<<gemm_grid(d, r, batch), 64, 0, s>>>(Yin, w.Q, Yout, d, r, r, r,
-                                                                    r, w.dr, w.rr, w.dr, 1,
-                                                                    none);
+  if (rt) {
+    EpiArgs re{};
+    re.rt = *rt;
+    k_sgemm<false, kRefresh, TM><<<gemm_grid(d, r, batch), 64, 0, s>>>(
+        Yin, w.Q, Yout, d, r, r, r, r, w.dr, w.rr, w.dr, 1, re);
+  } else {
+    k_sgemm<false, kStore, TM><<<gemm_grid(d, r, batch), 64, 0, s>>>(
+        Yin, w.Q, Yout, d, r, r, r, r, w.dr, w.rr, w.dr, 1, none);
+  }
+}
+
+// bf16 operands of the refreshed plans from an fp32 A (used when the step
+// has no retraction product to carry them)
+__global__ void k_refresh_AB(const float* __restrict__ A, int d, int r, long sA, RefreshTable rt) {
+  const int z = blockIdx.y;
+  if (z >= rt.n || rt.At[z] == nullptr) return;
+  for (long x = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x;
+       x < static_cast<long>(d) * r; x += static_cast<long>(gridDim.x) * blockDim.x) {
+    const int k = static_cast<int>(x / r), j = static_cast<int>(x % r);
+    const __nv_bfloat16 v = __float2bfloat16_rn(A[z * sA + x]);
+    rt.At[z][static_cast<long>(j) * d + k] = v;
+    rt.Bcat[z][static_cast<long>(k) * 2 * r + j] = v;
+  }
 }
 
 }  // namespace
@@ -312,7 +343,7 @@ size_t spel_workspace_bytes(int64_t d, int64_t r, int32_t batch) {
 
 cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int batch, float lr,
                         float beta, const float* coeffs, int n_lmo, int n_retr, void* ws,
-                        cudaStream_t s) {
+                        cudaStream_t s, const RefreshTable* rt) {
   const Ws w = carve(ws, d, r, batch);
   EpiArgs none{};
   // H = sym(A^T G)
@@ -344,12 +375,20 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
   k_axpy<<<dim3(256, batch), 256, 0, s>>>(A, cur, lr, nxt, w.dr, w.dr);
   { float* tmp = cur; cur = nxt; nxt = tmp; }
   for (int t = 0; t < n_retr; ++t) {
-    float* out = (t == n_retr - 1) ? A : nxt;
-    pe_step(cur, out, coeffs + 3 * (n_lmo + t), w, d, r, batch, s);
+    const bool last = t == n_retr - 1;
+    float* out = last ? A : nxt;
+    pe_step(cur, out, coeffs + 3 * (n_lmo + t), w, d, r, batch, s, last ? rt : nullptr);
     float* tmp = cur; cur = out; nxt = tmp;
   }
-  if (n_retr == 0)
+  if (n_retr == 0) {
     cudaMemcpyAsync(A, cur, sizeof(float) * w.dr * batch, cudaMemcpyDeviceToDevice, s);
+    if (rt) k_refresh_AB<<<dim3(256, batch), 256, 0, s>>>(A, d, r, w.dr, *rt);
+  }
+  if (rt) {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_prep_M_refresh(*rt, A, d, r, s);
+  }
   return cudaGetLastError();
 }
 

@@ -901,6 +901,55 @@ mapl_status mapl_spel_step(float* A, const float* G, float* m, int64_t d, int64_
   return MAPL_OK;
 }
 
+mapl_status mapl_spel_step_refresh(float* A, const float* G, float* m, int64_t d, int64_t r,
+                                   int32_t batch, float lr, float beta, const float* coeffs,
+                                   int32_t n_lmo, int32_t n_retr, const mapl_plan* plans,
+                                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!plans) return fail(MAPL_ERR_INVALID_ARG, "plans is NULL");
+  if (batch < 1 || batch > kMaxRefresh)
+    return fail(MAPL_ERR_UNSUPPORTED, "the fused plan refresh takes 1 to %d boundaries", kMaxRefresh);
+  RefreshTable rt{};
+  rt.n = batch;
+  for (int b = 0; b < batch; ++b) {
+    mapl_plan pl = plans[b];
+    if (!pl) continue;
+    if (!pl->tc) return fail(MAPL_ERR_UNSUPPORTED, "plan %d: the fused refresh needs a bf16 plan", b);
+    if (pl->cfg.d != d || pl->cfg.r != r)
+      return fail(MAPL_ERR_INVALID_ARG, "plan %d has (d, r) = (%lld, %lld), the step (%lld, %lld)",
+                  b, static_cast<long long>(pl->cfg.d), static_cast<long long>(pl->cfg.r),
+                  static_cast<long long>(d), static_cast<long long>(r));
+    for (int q = 0; q < b; ++q)
+      if (plans[q] == pl) return fail(MAPL_ERR_INVALID_ARG, "plan %d appears twice", b);
+    mapl_status st = check_device(pl);
+    if (st != MAPL_OK) return st;
+    rt.At[b] = pl->p.At;
+    rt.Bcat[b] = pl->p.Bcat;
+    rt.Mts[b] = pl->p.Mts;
+    rt.Ps[b] = pl->p.Ps;
+  }
+  if (!A || !G || !m || !coeffs || !workspace)
+    return fail(MAPL_ERR_INVALID_ARG, "NULL pointer argument");
+  size_t need = 0;
+  mapl_status st = mapl_spel_workspace_size(d, r, batch, &need);
+  if (st != MAPL_OK) return st;
+  if (workspace_bytes < need)
+    return fail(MAPL_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+  if (n_lmo < 0 || n_retr < 0 || n_lmo + n_retr < 1 || n_lmo + n_retr > 32)
+    return fail(MAPL_ERR_INVALID_ARG, "need 1 <= n_lmo + n_retr <= 32");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) || !aligned16(A) || !aligned16(G) || !aligned16(m))
+    return fail(MAPL_ERR_INVALID_ARG, "workspace must be 256-byte, tensors 16-byte aligned");
+  if (!(beta >= 0.f && beta < 1.f)) return fail(MAPL_ERR_INVALID_ARG, "beta must be in [0, 1)");
+  cudaError_t e = launch_spel(A, G, m, static_cast<int>(d), static_cast<int>(r), batch, lr, beta,
+                              coeffs, n_lmo, n_retr, workspace, stream, &rt);
+  if (e != cudaSuccess) return cuda_fail(e, "spel launch");
+  for (int b = 0; b < batch; ++b)
+    if (plans[b] && plans[b]->E_emb) {
+      st = embedding_table(plans[b], stream);
+      if (st != MAPL_OK) return st;
+    }
+  return MAPL_OK;
+}
+
 mapl_status mapl_spel_step_static(float* A, const float* G, float* m, int64_t d, int64_t r,
                                   int32_t batch, float lr, float beta, const float* coeffs,
                                   int32_t n_lmo, int32_t n_retr, cudaStream_t stream) {

@@ -47,6 +47,7 @@ constexpr int kNSlot = 2;                       // residual operand slots (group
 constexpr int kCbStages = 2;                    // codebook ring
 constexpr uint32_t kBlockBytes = kTile * 128;   // 128 rows x 64 bf16, 128B swizzled
 constexpr uint32_t kFull = 0xffffffffu;
+static_assert(kTile == 4 * 32, "one four-row gather per lane of the producer warp");
 
 struct Ctl {
   uint64_t full[kMaxStages];
@@ -576,17 +577,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tile = blockIdx.x + it * gridDim.x;
       int nv[kIdsPerLane];
       if (it + 1 < L) fetch_ids(tile + gridDim.x, nv);
-      if (lane == 0) {
+      {
+        // the whole warp walks the items: lane 0 issues the block loads,
+        // every lane one of the 32 four-row gathers of an anchor block (a
+        // single thread issuing them all would hold the tile back)
         const int* ts = tids_s + (it & 1) * kTile;
         for (int p = 0; p < geo.nP; ++p) {
-          if (!(ok = mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, &ctl->abort, bud))) break;
+          if (!(ok = warp_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, ctl, bud))) break;
           const uint32_t st = ring + s * sb;
           const uint32_t fb = smem_u32(&ctl->full[s]);
           if (p < geo.nkx) {
-            mbar_arrive_expect_tx(fb, kBlockBytes + geo.r * 128u);
-            tma_load_2d(st, &tmX, p * 64, tile * kTile, fb);
-            for (int hh = 0; hh < geo.nh; ++hh)
-              tma_load_2d(st + kBlockBytes + hh * 256u * 128u, &tmAt, p * 64, hh * 256, fb);
+            if (lane == 0) {
+              mbar_arrive_expect_tx(fb, kBlockBytes + geo.r * 128u);
+              tma_load_2d(st, &tmX, p * 64, tile * kTile, fb);
+              for (int hh = 0; hh < geo.nh; ++hh)
+                tma_load_2d(st + kBlockBytes + hh * 256u * 128u, &tmAt, p * 64, hh * 256, fb);
+            }
           } else {
             // anchor item (kb, sp): -M^T split sp, block kb; the anchor rows
             // E[tids] of block kb come with sp == 0 (or every sp when the
@@ -594,14 +600,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // stream)
             const int j = p - geo.nkx, kb = j / geo.nsplit, sp = j - kb * geo.nsplit;
             const bool gather = sp == 0 || !geo.share;
-            mbar_arrive_expect_tx(fb, (gather ? kBlockBytes : 0u) + geo.r * 128u);
-            for (int hh = 0; hh < geo.nh; ++hh)
-              tma_load_2d(st + kBlockBytes + hh * 256u * 128u, &tmMt, kb * 64,
-                          sp * geo.r + hh * geo.nrow, fb);
+            if (lane == 0) {
+              mbar_arrive_expect_tx(fb, (gather ? kBlockBytes : 0u) + geo.r * 128u);
+              for (int hh = 0; hh < geo.nh; ++hh)
+                tma_load_2d(st + kBlockBytes + hh * 256u * 128u, &tmMt, kb * 64,
+                            sp * geo.r + hh * geo.nrow, fb);
+            }
+            // full[s] completes only when every byte armed above has landed,
+            // so the lanes' gathers may be issued in any order around it
             if (gather)
-              for (int q4 = 0; q4 < kTile / 4; ++q4)
-                tma_gather4(st + q4 * 512, &tmE, kb * 64, ts[4 * q4], ts[4 * q4 + 1],
-                            ts[4 * q4 + 2], ts[4 * q4 + 3], fb);
+              tma_gather4(st + lane * 512, &tmE, kb * 64, ts[4 * lane], ts[4 * lane + 1],
+                          ts[4 * lane + 2], ts[4 * lane + 3], fb);
           }
           if (++s == nst) {
             s = 0;
@@ -609,7 +618,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
       // the gathers that read this buffer two tiles ago were issued already
       // (their row ids travel with the instruction)
       if (it + 1 < L) store_ids((it + 1) & 1, nv);

@@ -76,8 +76,8 @@ typedef struct mapl_plan_s* mapl_plan;
  *   P_send     r x d   sender's frozen anchor projector P_p      (eq. (3))
  *   P_recv     r x d   receiver's anchor projector P_{p+1}       (eq. (2))
  *   codebooks  R x G x K x gd  C[rho][g][k][:] (NULL without VQ) (§3.5)
- * and precomputes M = P_send A (r x r; exact products summed with
- * compensated fp32 arithmetic, about fp64 accuracy), the operand
+ * and precomputes M = P_send A (r x r; bf16 plans: a cuBLAS GEMM with fp32
+ * accumulation, fp32 plans: compensated fp32 sums), the operand
  * layouts of the kernels and the codebook norms.  The plan owns that device
  * memory; mapl_plan_destroy frees it.  Blocks until the copies are done.
  * Errors: INVALID_ARG (sizes, null), UNSUPPORTED, CUDA.

@@ -36,15 +36,13 @@ __device__ __forceinline__ void two_sum_f(float a, float b, float& s, float& e) 
   e = (a - (s - bb)) + (b - bb);
 }
 
-// M[i][j] = sum_k P_send[i][k] A[k][j].  One block (8 warps) per row i and
+// fp32 plans: M[i][j] = sum_k P_send[i][k] A[k][j].  One block (8 warps) per row i and
 // 32 columns (lane = column, reads of A coalesced, P broadcast); warp w sums
 // k in its eighth of [0, d) with four independent compensated sums (k mod 4),
 // each term an exact product split by fma; the pairs are combined in shared
 // memory.
-// a_round: A is fp32 and enters as its bf16 rounding (RNE), i.e. the value a
-// bf16 plan would have been given.
 __device__ __forceinline__ void prep_M_block(const void* Ps, const void* A, int d, int r, bool bf,
-                                             bool a_round, __nv_bfloat16* Mts, float* M32) {
+                                             float* M32) {
   __shared__ float ph[8][32], pl[8][32];
   const int nj = (r + 31) / 32;
   const int i = blockIdx.x / nj, j = (blockIdx.x % nj) * 32 + (threadIdx.x & 31);
@@ -66,9 +64,7 @@ __device__ __forceinline__ void prep_M_block(const void* Ps, const void* A, int 
       const int k = k0 + u;
       float b = 0.f;
       if (jv && k < ke) {
-        const size_t x = static_cast<size_t>(k) * r + j;
-        b = a_round ? __bfloat162float(__float2bfloat16_rn(static_cast<const float*>(A)[x]))
-                    : ld_f32(A, x, bf);
+        b = ld_f32(A, static_cast<size_t>(k) * r + j, bf);
       }
       av[u] = b;
     }
@@ -100,34 +96,27 @@ __device__ __forceinline__ void prep_M_block(const void* Ps, const void* A, int 
     lo += pl[x][c] + te;
   }
   two_sum_f(hi, lo, hi, lo);
-  const int idx = i * r + j;
-  if (M32) M32[idx] = hi + lo;
-  if (Mts) {
-    // -M as hi + mid + lo bf16 terms; the remainder stays a pair
-    float vh = -hi, vl = -lo;
-    for (int s = 0; s < kNumSplit; ++s) {
-      const __nv_bfloat16 b = __float2bfloat16_rn(vh);
-      Mts[(static_cast<size_t>(s) * r + j) * r + i] = b;
-      float t, te;
-      two_sum_f(vh - __bfloat162float(b), vl, t, te);
-      vh = t;
-      vl = te;
-    }
-  }
+  M32[i * r + j] = hi + lo;
 }
 
 __global__ void __launch_bounds__(256) k_prep_M(const void* Ps, const void* A, int d, int r,
-                                                bool bf, __nv_bfloat16* Mts, float* M32) {
-  prep_M_block(Ps, A, d, r, bf, false, Mts, M32);
+                                                bool bf, float* M32) {
+  prep_M_block(Ps, A, d, r, bf, M32);
 }
 
-// one grid row (blockIdx.y) per boundary of a SPEL batch
-__global__ void __launch_bounds__(256) k_prep_M_refresh(RefreshTable rt, const float* A, int d,
-                                                        int r) {
-  const int z = blockIdx.y;
-  if (z >= rt.n || rt.Mts[z] == nullptr) return;
-  prep_M_block(rt.Ps[z], A + static_cast<size_t>(z) * d * r, d, r, true, true, rt.Mts[z],
-               nullptr);
+// -M^T as three bf16 terms (the K-major B operand of the anchor fold) from
+// the fp32 M of a bf16 plan: term s holds the bf16 rounding of what the
+// terms before it left; each remainder is exact in fp32.
+__global__ void k_split_negMt(const float* __restrict__ M, int r, __nv_bfloat16* __restrict__ Mts) {
+  const int x = blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= r * r) return;
+  const int i = x / r, j = x % r;
+  float v = -M[x];
+  for (int t = 0; t < kNumSplit; ++t) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(v);
+    Mts[(static_cast<size_t>(t) * r + j) * r + i] = b;
+    v -= __bfloat162float(b);
+  }
 }
 
 __global__ void k_prep_At(const __nv_bfloat16* A, int d, int r, __nv_bfloat16* At) {
@@ -301,7 +290,6 @@ cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps
   const int T = 256;
   k_prep_At<<<blocks_for(static_cast<size_t>(d) * r, T), T, 0, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(A), d, r, p.At);
-  k_prep_M<<<r * ((r + 31) / 32), 256, 0, s>>>(Ps, A, d, r, true, p.Mts, nullptr);
   k_prep_Bcat<<<blocks_for(static_cast<size_t>(d) * 2 * r, T), T, 0, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(A), reinterpret_cast<const __nv_bfloat16*>(Pr), d, r,
       p.Bcat);
@@ -314,9 +302,8 @@ cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps
   return cudaGetLastError();
 }
 
-cudaError_t launch_prep_M_refresh(const RefreshTable& rt, const float* A, int d, int r,
-                                  cudaStream_t s) {
-  k_prep_M_refresh<<<dim3(r * ((r + 31) / 32), rt.n), 256, 0, s>>>(rt, A, d, r);
+cudaError_t launch_split_negMt(const float* M, int r, __nv_bfloat16* Mts, cudaStream_t s) {
+  k_split_negMt<<<(r * r + 255) / 256, 256, 0, s>>>(M, r, Mts);
   return cudaGetLastError();
 }
 
@@ -368,7 +355,7 @@ cudaError_t launch_prep_f32(const mapl_config& c, const void* A, const void* Ps,
   const size_t dr = static_cast<size_t>(d) * r;
   k_copy_f32<<<blocks_for(dr, T), T, 0, s>>>(reinterpret_cast<const float*>(A), p.A32, dr);
   k_prep_At32<<<blocks_for(dr, T), T, 0, s>>>(reinterpret_cast<const float*>(A), d, r, p.At32);
-  k_prep_M<<<r * ((r + 31) / 32), 256, 0, s>>>(Ps, A, d, r, false, nullptr, p.M32);
+  k_prep_M<<<r * ((r + 31) / 32), 256, 0, s>>>(Ps, A, d, r, false, p.M32);
   (void)Pr;   // the plan's P_recv copy is used in place (p.Pr32)
   if (!A_only) {
     if (c.G > 0) {

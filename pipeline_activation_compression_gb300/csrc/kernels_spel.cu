@@ -384,11 +384,6 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
     cudaMemcpyAsync(A, cur, sizeof(float) * w.dr * batch, cudaMemcpyDeviceToDevice, s);
     if (rt) k_refresh_AB<<<dim3(256, batch), 256, 0, s>>>(A, d, r, w.dr, *rt);
   }
-  if (rt) {
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return launch_prep_M_refresh(*rt, A, d, r, s);
-  }
   return cudaGetLastError();
 }
 

@@ -259,6 +259,8 @@ mapl_status mapl_payload_bytes(const mapl_config* cfg, int64_t* bytes_per_token)
   return MAPL_OK;
 }
 
+static mapl_status plan_M(mapl_plan pl, cudaStream_t stream);
+
 mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void* A,
                              const void* P_send, const void* P_recv, const void* codebooks,
                              cudaStream_t stream) {
@@ -298,6 +300,7 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   const size_t oPr = take(d * r * elt_size(*cfg));
   if (pl->tc) {
     oAt = take(d * r * 2);
+    oM32 = take(r * r * 4);
     oMts = take(static_cast<size_t>(kNumSplit) * r * r * 2);
     oBcat = take(d * 2 * r * 2);
     if (vq) oCb = take(ncode * pl->gd * 2);
@@ -321,6 +324,7 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   p.pool = pool;
   if (pl->tc) {
     p.At = reinterpret_cast<__nv_bfloat16*>(b + oAt);
+    p.M32 = reinterpret_cast<float*>(b + oM32);
     p.Mts = reinterpret_cast<__nv_bfloat16*>(b + oMts);
     p.Bcat = reinterpret_cast<__nv_bfloat16*>(b + oBcat);
     if (vq) p.Cb = reinterpret_cast<__nv_bfloat16*>(b + oCb);
@@ -345,8 +349,19 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   if (e == cudaSuccess)
     e = pl->tc ? launch_prep_bf16(*cfg, A, p.Ps, p.Pr, codebooks, p, false, stream)
                : launch_prep_f32(*cfg, A, p.Ps, p.Pr, codebooks, p, false, stream);
+  if (e == cudaSuccess && pl->tc) {
+    st = plan_M(pl, stream);
+    if (st != MAPL_OK) {
+      cudaStreamSynchronize(stream);
+      if (pl->blas) cublasDestroy(pl->blas);
+      cudaFree(pool);
+      delete pl;
+      return st;
+    }
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) {
+    if (pl->blas) cublasDestroy(pl->blas);
     cudaFree(pool);
     delete pl;
     return cuda_fail(e, "plan preparation");
@@ -355,6 +370,7 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
     st = geometry(pl);
     if (st == MAPL_OK) st = build_plan_maps(pl);
     if (st != MAPL_OK) {
+      if (pl->blas) cublasDestroy(pl->blas);
       cudaFree(pool);
       delete pl;
       return st;
@@ -364,15 +380,45 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   return MAPL_OK;
 }
 
-// T = E_emb A (cuBLAS, bf16 in, fp32 out) split into the [hi|mid|lo] table.
-static mapl_status embedding_table(mapl_plan pl, cudaStream_t stream) {
-  const mapl_config& c = pl->cfg;
+static mapl_status blas_on(mapl_plan pl, cudaStream_t stream) {
   if (!pl->blas && cublasCreate(&pl->blas) != CUBLAS_STATUS_SUCCESS) {
     pl->blas = nullptr;
     return fail(MAPL_ERR_CUDA, "cublasCreate failed");
   }
   if (cublasSetStream(pl->blas, stream) != CUBLAS_STATUS_SUCCESS)
     return fail(MAPL_ERR_CUDA, "cublasSetStream failed");
+  return MAPL_OK;
+}
+
+// bf16 plan: M = P_send A (r x r) from the plan's A^T and P_send copies, a
+// plain GEMM (cuBLAS, bf16 products exact, fp32 accumulation: M to about
+// 2^-24 relative, far inside what the fold's three bf16 terms carry into Z),
+// then -M^T split into the three bf16 terms of the anchor fold.
+static mapl_status plan_M(mapl_plan pl, cudaStream_t stream) {
+  mapl_status st = blas_on(pl, stream);
+  if (st != MAPL_OK) return st;
+  const mapl_config& c = pl->cfg;
+  const int r = static_cast<int>(c.r), d = static_cast<int>(c.d);
+  // column-major: M^T (r x r) = A^T P_send^T; the row-major A^T (r x d) is
+  // the column-major d x r A, read transposed; the row-major P_send (r x d)
+  // is the column-major d x r P_send^T.  The column-major M^T is the
+  // row-major M.
+  const float one = 1.f, zero = 0.f;
+  const cublasStatus_t bs =
+      cublasGemmEx(pl->blas, CUBLAS_OP_T, CUBLAS_OP_N, r, r, d, &one, pl->p.At, CUDA_R_16BF, d,
+                   pl->p.Ps, CUDA_R_16BF, d, &zero, pl->p.M32, CUDA_R_32F, r, CUBLAS_COMPUTE_32F,
+                   CUBLAS_GEMM_DEFAULT);
+  if (bs != CUBLAS_STATUS_SUCCESS) return fail(MAPL_ERR_CUDA, "cuBLAS GEMM failed (%d)", (int)bs);
+  const cudaError_t e = launch_split_negMt(pl->p.M32, r, pl->p.Mts, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "anchor fold operand");
+  return MAPL_OK;
+}
+
+// T = E_emb A (cuBLAS, bf16 in, fp32 out) split into the [hi|mid|lo] table.
+static mapl_status embedding_table(mapl_plan pl, cudaStream_t stream) {
+  const mapl_config& c = pl->cfg;
+  mapl_status bst = blas_on(pl, stream);
+  if (bst != MAPL_OK) return bst;
   // column-major: T^T (r x V) = A^T * E_emb^T, with the plan's row-major
   // A^T (r x d) read as the column-major d x r matrix A and transposed
   const float one = 1.f, zero = 0.f;
@@ -432,6 +478,10 @@ mapl_status mapl_plan_update_A(mapl_plan pl, const void* A, cudaStream_t stream)
   cudaError_t e = pl->tc ? launch_prep_bf16(pl->cfg, A, pl->p.Ps, pl->p.Pr, nullptr, pl->p, true, stream)
                          : launch_prep_f32(pl->cfg, A, pl->p.Ps, pl->p.Pr, nullptr, pl->p, true, stream);
   if (e != cudaSuccess) return cuda_fail(e, "update_A");
+  if (pl->tc) {
+    const mapl_status st = plan_M(pl, stream);
+    if (st != MAPL_OK) return st;
+  }
   if (pl->E_emb) return embedding_table(pl, stream);
   return MAPL_OK;
 }
@@ -924,8 +974,6 @@ mapl_status mapl_spel_step_refresh(float* A, const float* G, float* m, int64_t d
     if (st != MAPL_OK) return st;
     rt.At[b] = pl->p.At;
     rt.Bcat[b] = pl->p.Bcat;
-    rt.Mts[b] = pl->p.Mts;
-    rt.Ps[b] = pl->p.Ps;
   }
   if (!A || !G || !m || !coeffs || !workspace)
     return fail(MAPL_ERR_INVALID_ARG, "NULL pointer argument");
@@ -942,11 +990,12 @@ mapl_status mapl_spel_step_refresh(float* A, const float* G, float* m, int64_t d
   cudaError_t e = launch_spel(A, G, m, static_cast<int>(d), static_cast<int>(r), batch, lr, beta,
                               coeffs, n_lmo, n_retr, workspace, stream, &rt);
   if (e != cudaSuccess) return cuda_fail(e, "spel launch");
-  for (int b = 0; b < batch; ++b)
-    if (plans[b] && plans[b]->E_emb) {
-      st = embedding_table(plans[b], stream);
-      if (st != MAPL_OK) return st;
-    }
+  for (int b = 0; b < batch; ++b) {
+    if (!plans[b]) continue;
+    st = plan_M(plans[b], stream);   // M = P_send bf16(A) from the A^T just written
+    if (st == MAPL_OK && plans[b]->E_emb) st = embedding_table(plans[b], stream);
+    if (st != MAPL_OK) return st;
+  }
   return MAPL_OK;
 }
 

@@ -32,7 +32,7 @@ struct PlanDevice {
   // fp32 CUDA-core path
   float* A32 = nullptr;             // d x r
   float* At32 = nullptr;            // r x d     A^T
-  float* M32 = nullptr;             // r x r     M = P_send A
+  float* M32 = nullptr;             // r x r     M = P_send A (both paths)
   float* Pr32 = nullptr;            // r x d     P_recv
   float* C32 = nullptr;             // R x G x K x gd
   // both
@@ -130,21 +130,19 @@ constexpr size_t kSpelStaticScratchBytes = static_cast<size_t>(16) << 20;
 // Device address of that scratch on the current device (looked up once per
 // device with cudaGetSymbolAddress and cached).
 cudaError_t spel_static_scratch(void** out);
-// Plan operands refreshed from a SPEL step's new fp32 A (rounded to bf16),
-// per boundary of the batch; boundaries with At == nullptr are skipped.
+// Plan operands written by a SPEL step's last retraction product from the
+// new fp32 A (rounded to bf16), per boundary of the batch; boundaries with
+// At == nullptr are skipped.  M is formed afterwards by the host API.
 constexpr int kMaxRefresh = 16;
 struct RefreshTable {
   int n;
   __nv_bfloat16* At[kMaxRefresh];     // r x d
   __nv_bfloat16* Bcat[kMaxRefresh];   // d x 2r, columns [0, r) written
-  __nv_bfloat16* Mts[kMaxRefresh];    // S x r x r, -M^T terms
-  const void* Ps[kMaxRefresh];        // r x d bf16 P_send
 };
 cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int batch, float lr,
                         float beta, const float* coeffs, int n_lmo, int n_retr, void* ws,
                         cudaStream_t s, const RefreshTable* rt = nullptr);
-// M = P_send bf16(A) for every boundary of the table (one launch)
-cudaError_t launch_prep_M_refresh(const RefreshTable& rt, const float* A, int d, int r,
-                                  cudaStream_t s);
+// Mts = -M^T in kNumSplit bf16 terms from the fp32 r x r M of a bf16 plan.
+cudaError_t launch_split_negMt(const float* M, int r, __nv_bfloat16* Mts, cudaStream_t s);
 
 }  // namespace mapl

@@ -45,14 +45,19 @@ def parse():
 
 
 # ----------------------------------------------------------------- helpers
-def dist_setup(args):
+def dist_setup(args=None, backend: str = "nccl"):
+    """One process per GPU (torchrun env).  The codec shards by micro-batch:
+    every rank compresses and reconstructs its own tokens and no collective
+    touches the data path; the process group only carries the barrier and
+    the max-over-ranks of the timings."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if ws > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-        dist.init_process_group("nccl")
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group(backend)
     return ws, rank
 
 
@@ -67,9 +72,21 @@ def max_over_ranks(x: float, ws: int) -> float:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, ws: int, max_ms: float) -> float:
+    """Units all ranks processed in the timed region / the slowest rank's time."""
+    return units_per_rank * ws / (max_ms * 1e-3)
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank draws its own micro-batches (weak scaling: the work per rank
+    is fixed, no two ranks process the same tokens)."""
+    return rank
 
 
 class ClockSampler:
@@ -222,7 +239,7 @@ def run_ours(args, ws, rank):
     mapl.load_library()
     w = synth.WORKLOADS[args.workload]
     N = args.tokens or w.N
-    b = synth.make_boundary(w, seed=rank, n_tokens=N)
+    b = synth.make_boundary(w, seed=rank_seed(rank), n_tokens=N)
 
     def to_dev(a):
         a = np.ascontiguousarray(a)
@@ -350,8 +367,7 @@ def run_ours(args, ws, rank):
     peak, peak_kind = peaks()
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     step_bytes = comp_b + dec_b
-    tokens = N * K * ws
-    value = tokens / (total_ms * 1e-3)
+    value = whole_job_rate(N * K, ws, total_ms)
 
     # backward pass (gradient through the same projector, and dL/dA), timed
     # apart from the forward step: one call each per iteration, CUDA events
@@ -525,7 +541,7 @@ def run_ours(args, ws, rank):
                      "algorithmic_bytes_per_launch": dom_bytes,
                      "traffic": profiled_traffic(dom, w.name),
                      "step_frac": (step_bytes / (total_ms / K * 1e-3) / 1e9) / peak},
-        "e2e": {"value": N * Ke * ws / (e2e_ms * 1e-3), "unit": UNIT,
+        "e2e": {"value": whole_job_rate(N * Ke, ws, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(xh_host.numel() * 2 + 2 * t_host.numel() * 4
                                           + pay_h[0].numel() * pay_h[0].element_size()),
                 "d2h_bytes_per_step": int(out_h[0].numel() * 2
@@ -536,7 +552,7 @@ def run_ours(args, ws, rank):
                          "workload, 200 calls each, inputs L2-warm"),
         "spel": spel,
         "first_boundary": first,
-        "cuda_graph": {"value": N * ws / (graph_ms * 1e-3), "unit": UNIT,
+        "cuda_graph": {"value": whole_job_rate(N, ws, graph_ms), "unit": UNIT,
                        "ms_per_step": graph_ms, "steps": reps * nsets,
                        "note": "compress + decompress captured once per buffer set, replayed"},
         "gpu_launches": 2 * K,

@@ -241,6 +241,21 @@ mapl_status mapl_decompress_host(mapl_plan plan, const void* payload, const int3
  */
 mapl_status mapl_check(mapl_plan plan, cudaStream_t stream);
 
+/*
+ * Failure-detection self-test.  Every wait inside the codec kernels is
+ * bounded: a kernel that gives up sets the timeout bit of the plan's error
+ * word, unwinds and exits, so the context stays usable and mapl_check
+ * returns MAPL_ERR_TIMEOUT.  This call runs that same bounded wait in a
+ * one-warp kernel on an mbarrier that nothing arrives on, with a budget of
+ * `budget_ns` (1 us .. 2 s), and blocks until it has given up.  The give-up
+ * is recorded in the plan's error word exactly as a codec kernel records
+ * it (so the next mapl_check returns MAPL_ERR_TIMEOUT); *waited_ns receives
+ * the time the kernel waited.  Nothing else is launched or in flight.
+ * Errors: INVALID_ARG, CUDA.
+ */
+mapl_status mapl_selftest_bounded_wait(mapl_plan plan, int64_t budget_ns, int64_t* waited_ns,
+                                       cudaStream_t stream);
+
 void mapl_plan_destroy(mapl_plan plan);
 
 /* Bytes of device workspace mapl_spel_step needs for (d, r, batch). */

@@ -21,7 +21,7 @@ __all__ = [
     "mapl_compress_z32", "mapl_decompress", "mapl_check", "mapl_plan_destroy",
     "mapl_host_workspace_size", "mapl_compress_host", "mapl_decompress_host",
     "mapl_grad_compress", "mapl_grad_decompress", "mapl_grad_A",
-    "mapl_stream_subset", "mapl_plan_update_codes",
+    "mapl_stream_subset", "mapl_plan_update_codes", "mapl_selftest_bounded_wait",
     "mapl_spel_workspace_size", "mapl_spel_step", "mapl_spel_step_refresh",
     "mapl_spel_step_static", "mapl_last_error",
     "mapl_version",
@@ -77,6 +77,7 @@ def load_library():
         "mapl_compress_z32": [P, P, P, I64, P, P, P],
         "mapl_decompress": [P, P, P, I64, P, P, P],
         "mapl_check": [P, P],
+        "mapl_selftest_bounded_wait": [P, I64, ctypes.POINTER(I64), P],
         "mapl_host_workspace_size": [P, I64, ctypes.POINTER(SZ)],
         "mapl_grad_compress": [P, P, I64, P, P],
         "mapl_grad_decompress": [P, P, I64, P, P],
@@ -329,6 +330,15 @@ def mapl_plan_update_codes(plan: Plan, ids, codes, stream=None):
 def mapl_check(plan: Plan, stream=None):
     """Synchronise and raise MaplError if a kernel flagged a data error."""
     _check(load_library().mapl_check(plan.handle, _stream(stream)))
+
+
+def mapl_selftest_bounded_wait(plan: Plan, budget_ns: int, stream=None) -> int:
+    """Run the kernels' bounded wait on a barrier nothing completes; returns
+    the nanoseconds waited.  The plan's next mapl_check reports the timeout."""
+    out = ctypes.c_int64(0)
+    _check(load_library().mapl_selftest_bounded_wait(plan.handle, int(budget_ns),
+                                                     ctypes.byref(out), _stream(stream)))
+    return int(out.value)
 
 
 def mapl_plan_destroy(plan: Plan):

@@ -338,6 +338,34 @@ __global__ void k_update_codes(const int32_t* ids, int count, const void* codes,
   cnorm[id] = static_cast<float>(s);
 }
 
+// Self-test of the bounded wait every kernel uses: one warp waits on an
+// mbarrier that nothing arrives on, through the same mbar_wait, and reports
+// the give-up exactly as a codec kernel would (the error word's timeout bit).
+// Nothing is in flight while it waits, so giving up leaves nothing behind.
+__global__ void k_wait_selftest(uint64_t budget_ns, int* err, unsigned long long* waited) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint64_t t0 = global_ns();
+  const bool ok = mbar_wait(smem_u32(&bar), 0, &abort_flag, budget_ns);
+  const uint64_t t1 = global_ns();
+  if (threadIdx.x == 0) {
+    if (!ok) atomicOr(err, kErrTimeout);
+    *waited = t1 - t0;
+  }
+}
+
+cudaError_t launch_wait_selftest(uint64_t budget_ns, int* err, unsigned long long* waited,
+                                 cudaStream_t s) {
+  k_wait_selftest<<<1, 32, 0, s>>>(budget_ns, err, waited);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_update_codes(const mapl_config& c, const int32_t* ids, int count,
                                 const void* codes, PlanDevice& p, cudaStream_t s) {
   const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G), ncode = nb * c.K;

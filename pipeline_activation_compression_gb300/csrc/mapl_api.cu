@@ -904,6 +904,26 @@ mapl_status mapl_decompress_host(mapl_plan pl, const void* payload, const int32_
   return MAPL_OK;
 }
 
+mapl_status mapl_selftest_bounded_wait(mapl_plan pl, int64_t budget_ns, int64_t* waited_ns,
+                                       cudaStream_t stream) {
+  if (!pl || !waited_ns) return fail(MAPL_ERR_INVALID_ARG, "NULL argument");
+  if (budget_ns < 1000 || budget_ns > 2000000000LL)
+    return fail(MAPL_ERR_INVALID_ARG, "budget_ns must be in [1 us, 2 s]");
+  mapl_status st = check_device(pl);
+  if (st != MAPL_OK) return st;
+  unsigned long long* d = nullptr;
+  cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&d), sizeof(*d), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync");
+  unsigned long long h = 0;
+  e = launch_wait_selftest(static_cast<uint64_t>(budget_ns), pl->p.err, d, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&h, d, sizeof(h), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  cudaFreeAsync(d, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "bounded-wait self-test");
+  *waited_ns = static_cast<int64_t>(h);
+  return MAPL_OK;
+}
+
 mapl_status mapl_check(mapl_plan pl, cudaStream_t stream) {
   if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
   cudaError_t e = cudaStreamSynchronize(stream);

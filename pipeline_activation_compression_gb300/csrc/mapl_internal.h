@@ -92,6 +92,10 @@ cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps
 cudaError_t launch_prep_f32(const mapl_config& c, const void* A, const void* Ps, const void* Pr,
                             const void* C, PlanDevice& p, bool A_only, cudaStream_t s);
 
+// One warp waits (bounded) on an mbarrier nothing arrives on; sets the
+// timeout bit of `err` when it gives up and writes the time waited.
+cudaError_t launch_wait_selftest(uint64_t budget_ns, int* err, unsigned long long* waited,
+                                 cudaStream_t s);
 cudaError_t launch_update_codes(const mapl_config& c, const int32_t* ids, int count,
                                 const void* codes, PlanDevice& p, cudaStream_t s);
 

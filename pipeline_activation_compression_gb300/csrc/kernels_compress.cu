@@ -137,18 +137,6 @@ __device__ __forceinline__ void tmem_load_group(uint32_t taddr, float (&u)[GD]) 
   }
 }
 
-template <int GD>
-__device__ __forceinline__ void tmem_store_group(uint32_t taddr, const float (&u)[GD]) {
-#pragma unroll
-  for (int c = 0; c < GD; c += 16) {
-    float t[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) t[i] = u[c + i];
-    tmem_st16(taddr + c, t);
-  }
-  tmem_wait_st();
-}
-
 // Two-term bf16 split of the residual into the swizzled A operand of the
 // distance MMA: row `row` holds [hi (GD) | lo (GD)].
 template <int GD>
@@ -359,11 +347,14 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
 
   for (int b0 = 0; b0 < G && alive; b0 += geo.B) {
     const int b1g = b0 + geo.B < G ? b0 + geo.B : G;
+    // The residual of the group this warp owns in the batch (at most one:
+    // batches start at even groups and hold two) lives in registers through
+    // the rounds; Z's TMEM columns are only read here.
+    float u[GD];
     // round-0 operands of the groups this half owns
     for (int g = b0; g < b1g; ++g) {
       if ((g & 1) != h && G > 1) continue;
       if (G == 1 && h == 1) continue;
-      float u[GD];
       tmem_load_group<GD>(tz + g * GD, u);
       const int slot = g - b0;
       const float nu = write_operand<GD>(ubase + slot * kBlockBytes, row, u);
@@ -431,12 +422,8 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
         // of 2*GD exact products, fp32 rounding of ||c||^2 and the fma)
         const float eps = 2e-5f * nu * cm + 1.2e-7f * (cm * cm + 2.f * nu * cm + fabsf(B1));
         const bool need = (B2 - B1) <= 2.f * eps;
-        float u[GD];
-        bool have_u = false;
         if (owner && __any_sync(kFull, need)) {
           {
-            tmem_load_group<GD>(tz + g * GD, u);
-            have_u = true;
             // band of the candidates: the MMA-coarse band plus the error of
             // the fp32 CUDA-core dot products (32 exact products, fp32 sums)
             const float thr =
@@ -451,7 +438,6 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
         // 4. owner: record the index, update the residual, next operand
         if (store) idx_out[rho * G + g] = bad ? static_cast<uint8_t>(0) : static_cast<uint8_t>(K1);
         if (rho + 1 < R) {
-          if (!have_u) tmem_load_group<GD>(tz + g * GD, u);
 #pragma unroll
           for (int c = 0; c < GD / 8; ++c) {
             const uint4 w = code_chunk<GD>(stage, K1, c);
@@ -463,7 +449,6 @@ __device__ void epilogue_vq(const CompressArgs& a, const Geo& geo, Ctl* ctl, uin
               u[c * 8 + 2 * e + 1] -= f.y;
             }
           }
-          tmem_store_group<GD>(tz + g * GD, u);
           const float nn = write_operand<GD>(ubase + slot * kBlockBytes, row, u);
           ctl->nu[slot][suse[slot] & 1u][row] = nn;
           fence_async_shared();

@@ -371,13 +371,81 @@ struct CtlPt {
   int32_t ids[2][kTile];  // gather row ids of the tile in A buffer b
 };
 
+// One code row of book (rho, g) for index k, GD bf16 as GD/8 uint4 loads;
+// an index >= K is flagged and replaced by K - 1 (never read past the book).
+template <int GD>
+__device__ __forceinline__ void load_code(const DecompressArgs& a, const uint8_t* ip, int rho,
+                                          int g, uint4 (&w)[GD / 8]) {
+  int k = ip[rho * a.G + g];
+  if (k >= a.K) {
+    atomicOr(a.err, kErrBadIndex);
+    k = a.K - 1;
+  }
+  const uint4* cr =
+      reinterpret_cast<const uint4*>(a.Cb + (static_cast<size_t>(rho * a.G + g) * a.K + k) * GD);
+#pragma unroll
+  for (int c = 0; c < GD / 8; ++c) w[c] = __ldg(cr + c);
+}
+
+template <int GD>
+__device__ __forceinline__ void add_code(const uint4 (&w)[GD / 8], float (&acc)[GD]) {
+#pragma unroll
+  for (int c = 0; c < GD / 8; ++c) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w[c]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      acc[c * 8 + 2 * e] += f.x;
+      acc[c * 8 + 2 * e + 1] += f.y;
+    }
+  }
+}
+
+template <int GD>
+__device__ __forceinline__ void store_group(uint32_t abuf, int row, int g, const float (&acc)[GD]) {
+#pragma unroll
+  for (int c = 0; c < GD / 8; ++c) {
+    const int col = g * GD + c * 8;
+    uint4 v;
+    v.x = pack_bf16x2(acc[c * 8 + 0], acc[c * 8 + 1]);
+    v.y = pack_bf16x2(acc[c * 8 + 2], acc[c * 8 + 3]);
+    v.z = pack_bf16x2(acc[c * 8 + 4], acc[c * 8 + 5]);
+    v.w = pack_bf16x2(acc[c * 8 + 6], acc[c * 8 + 7]);
+    st_shared_v4(abuf + (col >> 6) * kBlockBytes + sw128_off(row, (col & 63) >> 3), v);
+  }
+}
+
 template <int GD>
 __device__ __forceinline__ void decode_row_pt(const DecompressArgs& a, uint32_t abuf, int row,
                                               int n, bool live) {
-  // Z_hat[n, g-block] = sum_rho C[rho][g][idx[n][rho][g]]  (fp32, then bf16);
-  // the loads of up to four rounds are issued before they are summed
-  const int G = a.G, R = a.R, K = a.K;
+  // Z_hat[n, g-block] = sum_rho C[rho][g][idx[n][rho][g]]  (fp32, rounds in
+  // order, then bf16).  With R <= 2 the lookups of two groups are in flight
+  // together; otherwise up to four rounds of one group at a time.
+  const int G = a.G, R = a.R;
   const uint8_t* ip = a.idx + static_cast<size_t>(n) * R * G;
+  if (R <= 2) {
+    for (int g = 0; g < G; g += 2) {
+      const int ng = g + 1 < G ? 2 : 1;
+      uint4 w[2][2][GD / 8];   // [group][round]
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int rho = 0; rho < 2; ++rho)
+          if (live && x < ng && rho < R) load_code<GD>(a, ip, rho, g + x, w[x][rho]);
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if (x >= ng) break;
+        float acc[GD];
+#pragma unroll
+        for (int i = 0; i < GD; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int rho = 0; rho < 2; ++rho)
+          if (live && rho < R) add_code<GD>(w[x][rho], acc);
+        store_group<GD>(abuf, row, g + x, acc);
+      }
+    }
+    return;
+  }
   for (int g = 0; g < G; ++g) {
     float acc[GD];
 #pragma unroll
@@ -386,46 +454,14 @@ __device__ __forceinline__ void decode_row_pt(const DecompressArgs& a, uint32_t 
       for (int r0 = 0; r0 < R; r0 += 4) {
         uint4 w[4][GD / 8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (r0 + j < R) {
-            int k = ip[(r0 + j) * G + g];
-            if (k >= K) {   // not a valid code: flag it, never read past the book
-              atomicOr(a.err, kErrBadIndex);
-              k = K - 1;
-            }
-            const uint4* cr = reinterpret_cast<const uint4*>(
-                a.Cb + (static_cast<size_t>((r0 + j) * G + g) * K + k) * GD);
+        for (int j = 0; j < 4; ++j)
+          if (r0 + j < R) load_code<GD>(a, ip, r0 + j, g, w[j]);
 #pragma unroll
-            for (int c = 0; c < GD / 8; ++c) w[j][c] = __ldg(cr + c);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (r0 + j < R) {
-#pragma unroll
-            for (int c = 0; c < GD / 8; ++c) {
-              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w[j][c]);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(h[e]);
-                acc[c * 8 + 2 * e] += f.x;
-                acc[c * 8 + 2 * e + 1] += f.y;
-              }
-            }
-          }
-        }
+        for (int j = 0; j < 4; ++j)
+          if (r0 + j < R) add_code<GD>(w[j], acc);
       }
     }
-#pragma unroll
-    for (int c = 0; c < GD / 8; ++c) {
-      const int col = g * GD + c * 8;
-      uint4 v;
-      v.x = pack_bf16x2(acc[c * 8 + 0], acc[c * 8 + 1]);
-      v.y = pack_bf16x2(acc[c * 8 + 2], acc[c * 8 + 3]);
-      v.z = pack_bf16x2(acc[c * 8 + 4], acc[c * 8 + 5]);
-      v.w = pack_bf16x2(acc[c * 8 + 6], acc[c * 8 + 7]);
-      st_shared_v4(abuf + (col >> 6) * kBlockBytes + sw128_off(row, (col & 63) >> 3), v);
-    }
+    store_group<GD>(abuf, row, g, acc);
   }
 }
 

@@ -108,10 +108,19 @@ VARIANTS = [
     ("vq_d1024_r128", dict(R=3, K=256, code_sigma=(0.99, 0.6, 0.35))),
     ("vq_d1024_r128", dict(R=1, K=128, code_sigma=(0.99,))),
     ("vq_d2048_r128", dict(R=3, K=64, code_sigma=(1.0, 0.7, 0.5))),
+    # four rounds, K = 192 (three 64-code blocks)
+    ("vq_d1024_r128", dict(R=4, K=192, code_sigma=(0.99, 0.7, 0.5, 0.35))),
+    # r = 64 with 16-wide groups (G = 4), r = 192 (G = 6), r = 256 with
+    # 16-wide groups (G = 16: eight batches of two groups)
+    ("vq_d1024_r128", dict(r=64, G=4, R=2, K=256, code_sigma=(0.99, 0.7))),
+    ("vq_d1024_r128", dict(r=192, G=6, R=2, K=128, code_sigma=(0.99, 0.7))),
+    ("vq_d2048_r256", dict(G=16, R=2, K=64, code_sigma=(1.0, 0.7))),
 ]
 
 
-@pytest.mark.parametrize("name,kw", VARIANTS, ids=["R3K256", "R1K128", "G8R3K64"])
+@pytest.mark.parametrize("name,kw", VARIANTS,
+                         ids=["R3K256", "R1K128", "G8R3K64", "R4K192", "r64G4", "r192G6",
+                              "r256G16"])
 def test_parity_vq_variants(name, kw):
     import dataclasses
     w = dataclasses.replace(synth.WORKLOADS[name], name=f"{name}_v", **kw)

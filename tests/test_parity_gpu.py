@@ -118,6 +118,25 @@ VARIANTS = [
 ]
 
 
+# The pages' own runs use groups of 2 dims (Table 8: 128 groups at r = 256,
+# K = 256): on the fp32 path, here with 8 groups of 2 dims at r = 16, and
+# one group of all 16 dims with a single round.
+F32_VARIANTS = [
+    dict(G=8, R=2, K=256, code_sigma=(0.5, 0.3)),
+    dict(G=1, R=1, K=64, code_sigma=(0.5,)),
+]
+
+
+@pytest.mark.parametrize("kw", F32_VARIANTS, ids=["gd2G8K256", "G1R1K64"])
+def test_parity_f32_group_widths(kw):
+    import dataclasses
+    w = dataclasses.replace(synth.WORKLOADS["tiny_d64_r16"], name="tiny_v", **kw)
+    b = synth.make_boundary(w, n_tokens=300)
+    plan = plan_for(w, b)
+    rep = check_outputs(w, b, *run(plan, w, b))
+    print(w, rep)
+
+
 @pytest.mark.parametrize("name,kw", VARIANTS,
                          ids=["R3K256", "R1K128", "G8R3K64", "R4K192", "r64G4", "r192G6",
                               "r256G16"])

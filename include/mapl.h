@@ -87,7 +87,9 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
                              const void* codebooks, cudaStream_t stream);
 
 /* Replace A (d x r, plan dtype) after a projector update and refresh M and
- * the operand layouts (§3.3: A_p changes every optimizer step). Async. */
+ * the operand layouts (§3.3: A_p changes every optimizer step).  bf16 plans
+ * form M with a cuBLAS GEMM on `stream` (the plan's handle is made at plan
+ * creation, so the call can be captured in a CUDA graph).  Async. */
 mapl_status mapl_plan_update_A(mapl_plan plan, const void* A, cudaStream_t stream);
 
 /*

@@ -35,15 +35,25 @@ def plan_for(w, b):
     return mapl.mapl_plan_create(cfg, to_dev(b["A"]), to_dev(b["P"]), to_dev(b["P_next"]), C)
 
 
+def _poisoned(shape, dtype):
+    if dtype == torch.uint8:
+        g = torch.Generator(device="cuda")
+        g.manual_seed(99)
+        return torch.randint(0, 256, shape, dtype=torch.uint8, device="cuda", generator=g)
+    return torch.full(shape, float("nan"), dtype=dtype, device="cuda")
+
+
 def run(plan, w, b, tids=None, check=True):
     X = to_dev(b["X"])
     t = torch.from_numpy(b["tids"] if tids is None else tids).cuda()
     N = X.shape[0]
-    payload = torch.empty(plan.payload_shape(N), dtype=plan.payload_dtype(), device="cuda")
+    # outputs start poisoned (NaN, or a random byte pattern for indices) so
+    # an element the kernels never write cannot pass as a stale result
+    payload = _poisoned(plan.payload_shape(N), plan.payload_dtype())
     mapl.mapl_compress(plan, X, t, to_dev(b["E"]), payload)
-    Z32 = torch.empty(N, w.r, dtype=torch.float32, device="cuda")
+    Z32 = _poisoned((N, w.r), torch.float32)
     mapl.mapl_compress_z32(plan, X, t, to_dev(b["E"]), Z32)
-    Xh = torch.empty(N, w.d, dtype=X.dtype, device="cuda")
+    Xh = _poisoned((N, w.d), X.dtype)
     mapl.mapl_decompress(plan, payload, t, to_dev(b["E_next"]), Xh)
     if check:
         mapl.mapl_check(plan)

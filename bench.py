@@ -318,15 +318,16 @@ def run_ours(args, ws, rank):
 
     # end to end through the public API's host-buffer calls: X and tids from
     # pinned host memory in, the payload out to the host and back, X_hat out
-    # to pinned host memory.  Consecutive steps rotate over four streams
-    # (each with its own device workspace and host outputs), so one step's
-    # download overlaps the next steps' uploads, as successive micro-batches
-    # of a pipeline would.  The host link (about 210 GB/s up, 190 down, 330
-    # both ways) bounds this number.
+    # to pinned host memory.  Consecutive steps rotate over six streams (each
+    # with its own device workspace and host outputs), so one step's download
+    # overlaps the next steps' uploads, as successive micro-batches of a
+    # pipeline would (2 / 4 / 6 / 8 streams measured 55 / 63 / 72 / 72 M
+    # tokens/s).  The host link (about 210 GB/s up, 190 down, 330 both ways)
+    # bounds this number.
     Ke = args.e2e_steps
     xh_host = torch.from_numpy(np.ascontiguousarray(b["X"]).view(np.int16)).view(torch.bfloat16).pin_memory()
     t_host = torch.from_numpy(b["tids"]).pin_memory()
-    NS = 4
+    NS = 6
     streams = [stream] + [torch.cuda.Stream() for _ in range(NS - 1)]
     wsz = mapl.mapl_host_workspace_size(plan, N)
     wsp = [torch.empty(wsz, dtype=torch.uint8, device="cuda") for _ in range(NS)]
@@ -547,7 +548,7 @@ def run_ours(args, ws, rank):
                 "d2h_bytes_per_step": int(out_h[0].numel() * 2
                                           + pay_h[0].numel() * pay_h[0].element_size()),
                 "api": "mapl_compress_host + mapl_decompress_host, steps rotating "
-                       "over four streams"},
+                       "over six streams"},
         "backward": dict(backward, note="gZ = dL/dX_hat A, dL/dX = gZ A^T, dL/dA; same "
                          "workload, 200 calls each, inputs L2-warm"),
         "spel": spel,

@@ -8,9 +8,13 @@
 //   Y   = A - lr Y
 //   repeat n_retr: same polynomial step                         eq. (7)
 //   A   = Y
-// The GEMMs are tiled 64 x 64 x 16 fp32 CUDA-core kernels (8 x 8 outputs
-// per thread) with sequential fp32 accumulation per output; r x r reductions over d use a fixed split-K
-// followed by an ordered sum, so results are run-to-run deterministic.
+// When d and r are multiples of 128, A^T G and the three products of each
+// polynomial step run on the tensor cores in emulated fp32
+// (kernels_spel_tc.cu); A H with its momentum epilogue, and every product of
+// other shapes, run in the tiled fp32 CUDA-core kernel below (32 x 32 output
+// tiles, sequential fp32 accumulation per output).  r x r reductions over d
+// use a fixed split-K followed by an ordered sum, so results are run-to-run
+// deterministic.
 #include "mapl_internal.h"
 
 namespace mapl {
@@ -268,6 +272,7 @@ struct Ws {
   float *Y0, *Y1, *S, *Q, *part, *nrm_part, *inv;
   long dr, rr;   // packed per-boundary strides of the d x r and r x r buffers
   int ks;
+  bool tc;       // the products of the step fit the tensor-core kernel
 };
 
 constexpr int kNormBlocks = 64;
@@ -279,6 +284,8 @@ Ws carve(void* ws, int d, int r, int batch) {
   w.dr = static_cast<long>(d) * r;
   w.rr = static_cast<long>(r) * r;
   w.ks = choose_ksplit(d);
+  w.tc = gemm3_supported(r, r, d, w.ks) && gemm3_supported(r, r, r, choose_ksplit_r(r, w.ks)) &&
+         gemm3_supported(d, r, r, 1);
   float* p = reinterpret_cast<float*>(ws);
   w.Y0 = p; p += al64(w.dr * batch);
   w.Y1 = p; p += al64(w.dr * batch);
@@ -288,33 +295,6 @@ Ws carve(void* ws, int d, int r, int batch) {
   w.nrm_part = p; p += al64(static_cast<size_t>(kNormBlocks) * batch);
   w.inv = p;
   return w;
-}
-
-// Y_out = Y_in (a I + b S + c S^2), S = Y_in^T Y_in; with rt the final
-// product also writes the refreshed plans' bf16 operands
-void pe_step(const float* Yin, float* Yout, const float* co, const Ws& w, int d, int r,
-             int batch, cudaStream_t s, const RefreshTable* rt = nullptr) {
-  EpiArgs none{};
-  k_sgemm<true, kStore, TM><<<gemm_grid(r, r, batch * w.ks), 64, 0, s>>>(
-      Yin, Yin, w.part, r, r, d, r, r, w.dr, w.dr, w.rr * w.ks, w.ks, none);
-  k_reduce<<<dim3((r * r + 255) / 256, batch), 256, 0, s>>>(w.part, w.S, r, w.ks, 0,
-                                                            w.rr * w.ks, w.rr);
-  // S^2 in split-K partials (a 4-aligned split of K = r for the plain A),
-  // then Q = a I + b S + c S^2 in the ordered reduction
-  const int kr = choose_ksplit_r(r, w.ks);
-  k_sgemm<false, kStore, TM><<<gemm_grid(r, r, batch * kr), 64, 0, s>>>(
-      w.S, w.S, w.part, r, r, r, r, r, w.rr, w.rr, w.rr * w.ks, kr, none);
-  k_reduce_poly<<<dim3((r * r + 255) / 256, batch), 256, 0, s>>>(
-      w.part, w.S, w.Q, r, kr, co[0], co[1], co[2], w.rr * w.ks, w.rr);
-  if (rt) {
-    EpiArgs re{};
-    re.rt = *rt;
-    k_sgemm<false, kRefresh, TM><<<gemm_grid(d, r, batch), 64, 0, s>>>(
-        Yin, w.Q, Yout, d, r, r, r, r, w.dr, w.rr, w.dr, 1, re);
-  } else {
-    k_sgemm<false, kStore, TM><<<gemm_grid(d, r, batch), 64, 0, s>>>(
-        Yin, w.Q, Yout, d, r, r, r, r, w.dr, w.rr, w.dr, 1, none);
-  }
 }
 
 // bf16 operands of the refreshed plans from an fp32 A (used when the step
@@ -329,6 +309,55 @@ __global__ void k_refresh_AB(const float* __restrict__ A, int d, int r, long sA,
     rt.At[z][static_cast<long>(j) * d + k] = v;
     rt.Bcat[z][static_cast<long>(k) * 2 * r + j] = v;
   }
+}
+
+// Y_out = Y_in (a I + b S + c S^2), S = Y_in^T Y_in; with rt the final
+// product also writes the refreshed plans' bf16 operands.  The three products
+// run on the tensor cores (launch_gemm3) when the shapes allow it, else on the
+// CUDA cores; the reductions and the polynomial are the same either way.
+cudaError_t pe_step(const float* Yin, float* Yout, const float* co, const Ws& w, int d, int r,
+                    int batch, cudaStream_t s, const RefreshTable* rt = nullptr) {
+  EpiArgs none{};
+  const int kr = choose_ksplit_r(r, w.ks);
+  const bool tc = w.tc;
+  cudaError_t e = cudaSuccess;
+  if (tc) {   // S partials: (Y^T)(Y^T)^T, both operands Y read with rows contiguous
+    e = launch_gemm3({Yin, r, w.dr, 1}, {Yin, r, w.dr, 1}, w.part, r, w.rr * w.ks, w.rr, r, r,
+                     d, batch, w.ks, s);
+    if (e != cudaSuccess) return e;
+  } else {
+    k_sgemm<true, kStore, TM><<<gemm_grid(r, r, batch * w.ks), 64, 0, s>>>(
+        Yin, Yin, w.part, r, r, d, r, r, w.dr, w.dr, w.rr * w.ks, w.ks, none);
+  }
+  k_reduce<<<dim3((r * r + 255) / 256, batch), 256, 0, s>>>(w.part, w.S, r, w.ks, 0,
+                                                            w.rr * w.ks, w.rr);
+  // S^2 in split-K partials (a 4-aligned split of K = r for the plain A),
+  // then Q = a I + b S + c S^2 in the ordered reduction
+  if (tc) {
+    e = launch_gemm3({w.S, r, w.rr, 0}, {w.S, r, w.rr, 1}, w.part, r, w.rr * w.ks, w.rr, r, r,
+                     r, batch, kr, s);
+    if (e != cudaSuccess) return e;
+  } else {
+    k_sgemm<false, kStore, TM><<<gemm_grid(r, r, batch * kr), 64, 0, s>>>(
+        w.S, w.S, w.part, r, r, r, r, r, w.rr, w.rr, w.rr * w.ks, kr, none);
+  }
+  k_reduce_poly<<<dim3((r * r + 255) / 256, batch), 256, 0, s>>>(
+      w.part, w.S, w.Q, r, kr, co[0], co[1], co[2], w.rr * w.ks, w.rr);
+  if (tc) {   // Y Q: Q read with rows contiguous (its transpose's rows)
+    e = launch_gemm3({Yin, r, w.dr, 0}, {w.Q, r, w.rr, 1}, Yout, r, w.dr, 0, d, r, r, batch, 1,
+                     s);
+    if (e != cudaSuccess) return e;
+    if (rt) k_refresh_AB<<<dim3(256, batch), 256, 0, s>>>(Yout, d, r, w.dr, *rt);
+  } else if (rt) {
+    EpiArgs re{};
+    re.rt = *rt;
+    k_sgemm<false, kRefresh, TM><<<gemm_grid(d, r, batch), 64, 0, s>>>(
+        Yin, w.Q, Yout, d, r, r, r, r, w.dr, w.rr, w.dr, 1, re);
+  } else {
+    k_sgemm<false, kStore, TM><<<gemm_grid(d, r, batch), 64, 0, s>>>(
+        Yin, w.Q, Yout, d, r, r, r, r, w.dr, w.rr, w.dr, 1, none);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -347,8 +376,15 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
   const Ws w = carve(ws, d, r, batch);
   EpiArgs none{};
   // H = sym(A^T G)
-  k_sgemm<true, kStore, TM><<<gemm_grid(r, r, batch * w.ks), 64, 0, s>>>(
-      A, G, w.part, r, r, d, r, r, w.dr, w.dr, w.rr * w.ks, w.ks, none);
+  cudaError_t e = cudaSuccess;
+  if (w.tc) {
+    e = launch_gemm3({A, r, w.dr, 1}, {G, r, w.dr, 1}, w.part, r, w.rr * w.ks, w.rr, r, r, d,
+                     batch, w.ks, s);
+    if (e != cudaSuccess) return e;
+  } else {
+    k_sgemm<true, kStore, TM><<<gemm_grid(r, r, batch * w.ks), 64, 0, s>>>(
+        A, G, w.part, r, r, d, r, r, w.dr, w.dr, w.rr * w.ks, w.ks, none);
+  }
   k_reduce<<<dim3((r * r + 255) / 256, batch), 256, 0, s>>>(w.part, w.S, r, w.ks, 1,
                                                             w.rr * w.ks, w.rr);
   // m = beta m + (1 - beta)(G - A H)
@@ -368,7 +404,8 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
   float* cur = w.Y0;
   float* nxt = w.Y1;
   for (int t = 0; t < n_lmo; ++t) {
-    pe_step(cur, nxt, coeffs + 3 * t, w, d, r, batch, s);
+    e = pe_step(cur, nxt, coeffs + 3 * t, w, d, r, batch, s);
+    if (e != cudaSuccess) return e;
     float* tmp = cur; cur = nxt; nxt = tmp;
   }
   // retraction input A - lr D
@@ -377,7 +414,8 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
   for (int t = 0; t < n_retr; ++t) {
     const bool last = t == n_retr - 1;
     float* out = last ? A : nxt;
-    pe_step(cur, out, coeffs + 3 * (n_lmo + t), w, d, r, batch, s, last ? rt : nullptr);
+    e = pe_step(cur, out, coeffs + 3 * (n_lmo + t), w, d, r, batch, s, last ? rt : nullptr);
+    if (e != cudaSuccess) return e;
     float* tmp = cur; cur = out; nxt = tmp;
   }
   if (n_retr == 0) {

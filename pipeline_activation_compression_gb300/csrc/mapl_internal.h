@@ -147,6 +147,22 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
                         float beta, const float* coeffs, int n_lmo, int n_retr, void* ws,
                         cudaStream_t s, const RefreshTable* rt = nullptr);
 // Mts = -M^T in kNumSplit bf16 terms from the fp32 r x r M of a bf16 plan.
+// Batched fp32 product on the tensor cores (3-term bf16 split, six term
+// products, fp32 accumulation): C[z] + ks * sS = opA[z] * opB[z]^T over split
+// ks of K.  An operand holds `rows x K` values, element (row, k) at
+// p[row * ld + k], or at p[k * ld + row] when rows_contig.  Needs M, N
+// multiples of 128 and K a multiple of 64 * ksplit (gemm3_supported).
+struct Gemm3Operand {
+  const float* p;
+  long ld;
+  long batch_stride;
+  int rows_contig;
+};
+bool gemm3_supported(int M, int N, int K, int ksplit);
+cudaError_t launch_gemm3(const Gemm3Operand& a, const Gemm3Operand& b, float* C, long ldc,
+                         long sC, long sS, int M, int N, int K, int batch, int ksplit,
+                         cudaStream_t s);
+
 cudaError_t launch_split_negMt(const float* M, int r, __nv_bfloat16* Mts, cudaStream_t s);
 
 }  // namespace mapl

@@ -24,7 +24,8 @@ def workspace(d, r, batch):
 
 
 @pytest.mark.parametrize("d,r,batch,n_lmo,n_retr", [
-    (256, 64, 2, 5, 5), (1024, 256, 3, 5, 5), (2048, 256, 3, 5, 7), (96, 20, 1, 3, 2)])
+    (256, 64, 2, 5, 5), (1024, 256, 3, 5, 5), (2048, 256, 3, 5, 7), (96, 20, 1, 3, 2),
+    (384, 128, 2, 2, 1), (2176, 128, 1, 1, 1), (640, 256, 1, 0, 2)])
 def test_one_step_parity(d, r, batch, n_lmo, n_retr):
     w = synth.SpelWorkload(f"t{d}", d, r, batch)
     s = synth.make_spel(w)

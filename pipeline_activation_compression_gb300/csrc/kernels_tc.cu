@@ -621,22 +621,27 @@ __global__ void __launch_bounds__(kPtThreads, 1)
       }
       ctl->ids[ab][bt] = t;
       named_bar_sync(kPtBuildBar, 128);
-      if (bt == 0) {
-        // Z_hat (non-VQ payload) and the anchor rows E'[tids] by TMA
+      if (bt < 32) {
+        // Z_hat (non-VQ payload) and the anchor rows E'[tids] by TMA.  Each
+        // lane of the first builder warp issues one four-row gather per
+        // K-block (one thread issuing all of them held the build back);
+        // afull completes only after lane 0's arrivals below, so the lanes'
+        // copies may land in any order around its expect_tx.
         const uint32_t fb = smem_u32(&ctl->afull[ab]);
-        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nzb) * kBlockBytes *
-                                      ((a.vq ? 0u : 1u) + (a.anchor ? 1u : 0u)));
-        if (!a.vq)
-          for (int kb = 0; kb < nzb; ++kb)
-            tma_load_2d(abuf + kb * kBlockBytes, &tmZ, kb * 64, tile * kTile, fb);
-        const int32_t* ids = ctl->ids[ab];
+        if (bt == 0) {
+          mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nzb) * kBlockBytes *
+                                        ((a.vq ? 0u : 1u) + (a.anchor ? 1u : 0u)));
+          if (!a.vq)
+            for (int kb = 0; kb < nzb; ++kb)
+              tma_load_2d(abuf + kb * kBlockBytes, &tmZ, kb * 64, tile * kTile, fb);
+          last_ab = ab;
+          last_use = ause;
+        }
+        const int32_t* ids = ctl->ids[ab] + 4 * bt;
         if (a.anchor)
           for (int kb = 0; kb < nzb; ++kb)
-            for (int q4 = 0; q4 < kTile / 4; ++q4)
-              tma_gather4(abuf + (nzb + kb) * kBlockBytes + q4 * 512, &tmE, kb * 64, ids[4 * q4],
-                          ids[4 * q4 + 1], ids[4 * q4 + 2], ids[4 * q4 + 3], fb);
-        last_ab = ab;
-        last_use = ause;
+            tma_gather4(abuf + (nzb + kb) * kBlockBytes + bt * 512, &tmE, kb * 64, ids[0], ids[1],
+                        ids[2], ids[3], fb);
       }
       if (a.vq) {
         if constexpr (GD > 0) decode_row_pt<GD>(a, abuf, bt, n, live);

@@ -175,7 +175,7 @@ def test_parity_full_size_sampled(name):
 
 
 # ------------------------------------------------------------------ edge cases
-@pytest.mark.parametrize("n", [1, 127, 128, 129, 255])
+@pytest.mark.parametrize("n", [1, 127, 128, 129, 255, 256, 257, 384])
 @pytest.mark.parametrize("name", ["vq_d1024_r128", "proj_d1024_r128", "tiny_d64_r16"])
 def test_ragged_sizes(name, n):
     w = synth.WORKLOADS[name]

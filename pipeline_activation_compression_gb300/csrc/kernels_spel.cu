@@ -16,6 +16,7 @@
 // use a fixed split-K followed by an ordered sum, so results are run-to-run
 // deterministic.
 #include "mapl_internal.h"
+#include "pdl.cuh"
 
 namespace mapl {
 
@@ -46,6 +47,7 @@ __global__ void __launch_bounds__(64)
     k_sgemm(const float* __restrict__ A, const float* __restrict__ B, float* __restrict__ C,
             int M, int N, int K, int lda, int ldb, long sA, long sB, long sC, int ksplit,
             EpiArgs e) {
+  pdl_enter();
   constexpr int MT = TM / 8;          // outputs per thread per dimension
   constexpr int V4 = TM / 16;         // float4 loads per thread per operand tile
   constexpr int R4 = TM / 4;          // float4s in a TM-wide row
@@ -179,6 +181,7 @@ __global__ void __launch_bounds__(64)
 __global__ void k_reduce_poly(const float* __restrict__ part, const float* __restrict__ S,
                               float* __restrict__ Q, int n, int ksplit, float a, float b,
                               float c, long sP, long sO) {
+  pdl_enter();
   const int z = blockIdx.y;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n * n) return;
@@ -192,6 +195,7 @@ __global__ void k_reduce_poly(const float* __restrict__ part, const float* __res
 // out = sum of `ksplit` partials (ordered); optionally symmetrised.
 __global__ void k_reduce(const float* __restrict__ part, float* __restrict__ out, int n,
                          int ksplit, int sym, long sP, long sO) {
+  pdl_enter();
   const int z = blockIdx.y;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n * n) return;
@@ -210,6 +214,7 @@ __global__ void k_reduce(const float* __restrict__ part, float* __restrict__ out
 // per-block partial sums of squares, then an ordered final sum
 __global__ void k_sumsq_partial(const float* __restrict__ x, long n, float* part, long sX,
                                 int nblk) {
+  pdl_enter();
   __shared__ float red[256];
   const int z = blockIdx.y;
   const float* p = x + z * sX;
@@ -225,6 +230,7 @@ __global__ void k_sumsq_partial(const float* __restrict__ x, long n, float* part
 }
 
 __global__ void k_sumsq_final(const float* part, int nblk, float* inv) {
+  pdl_enter();
   const int z = blockIdx.x;
   if (threadIdx.x != 0) return;
   float s = 0.f;
@@ -235,6 +241,7 @@ __global__ void k_sumsq_final(const float* part, int nblk, float* inv) {
 // y = alpha_z * x (alpha from a per-batch array) or y = A - lr * x
 __global__ void k_scale(const float* __restrict__ x, const float* __restrict__ inv, float* y,
                         long n, long sX) {
+  pdl_enter();
   const int z = blockIdx.y;
   const float a = inv[z];
   for (long i = blockIdx.x * 256L + threadIdx.x; i < n; i += 256L * gridDim.x)
@@ -243,6 +250,7 @@ __global__ void k_scale(const float* __restrict__ x, const float* __restrict__ i
 
 __global__ void k_axpy(const float* __restrict__ A, const float* __restrict__ D, float lr,
                        float* y, long n, long sX) {
+  pdl_enter();
   const int z = blockIdx.y;
   for (long i = blockIdx.x * 256L + threadIdx.x; i < n; i += 256L * gridDim.x)
     y[z * sX + i] = A[z * sX + i] - lr * D[z * sX + i];
@@ -300,6 +308,7 @@ Ws carve(void* ws, int d, int r, int batch) {
 // bf16 operands of the refreshed plans from an fp32 A (used when the step
 // has no retraction product to carry them)
 __global__ void k_refresh_AB(const float* __restrict__ A, int d, int r, long sA, RefreshTable rt) {
+  pdl_enter();
   const int z = blockIdx.y;
   if (z >= rt.n || rt.At[z] == nullptr) return;
   for (long x = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x;
@@ -326,11 +335,12 @@ cudaError_t pe_step(const float* Yin, float* Yout, const float* co, const Ws& w,
                      d, batch, w.ks, s);
     if (e != cudaSuccess) return e;
   } else {
-    k_sgemm<true, kStore, TM><<<gemm_grid(r, r, batch * w.ks), 64, 0, s>>>(
-        Yin, Yin, w.part, r, r, d, r, r, w.dr, w.dr, w.rr * w.ks, w.ks, none);
+    if ((e = launch_chained(k_sgemm<true, kStore, TM>, gemm_grid(r, r, batch * w.ks), dim3(64), 0,
+        s, Yin, Yin, w.part, r, r, d, r, r, w.dr, w.dr, w.rr * w.ks, w.ks,
+        none)) != cudaSuccess) return e;
   }
-  k_reduce<<<dim3((r * r + 255) / 256, batch), 256, 0, s>>>(w.part, w.S, r, w.ks, 0,
-                                                            w.rr * w.ks, w.rr);
+  if ((e = launch_chained(k_reduce, dim3((r * r + 255) / 256, batch), dim3(256), 0, s, w.part, w.S,
+      r, w.ks, 0, w.rr * w.ks, w.rr)) != cudaSuccess) return e;
   // S^2 in split-K partials (a 4-aligned split of K = r for the plain A),
   // then Q = a I + b S + c S^2 in the ordered reduction
   if (tc) {
@@ -338,24 +348,26 @@ cudaError_t pe_step(const float* Yin, float* Yout, const float* co, const Ws& w,
                      r, batch, kr, s);
     if (e != cudaSuccess) return e;
   } else {
-    k_sgemm<false, kStore, TM><<<gemm_grid(r, r, batch * kr), 64, 0, s>>>(
-        w.S, w.S, w.part, r, r, r, r, r, w.rr, w.rr, w.rr * w.ks, kr, none);
+    if ((e = launch_chained(k_sgemm<false, kStore, TM>, gemm_grid(r, r, batch * kr), dim3(64), 0,
+        s, w.S, w.S, w.part, r, r, r, r, r, w.rr, w.rr, w.rr * w.ks, kr,
+        none)) != cudaSuccess) return e;
   }
-  k_reduce_poly<<<dim3((r * r + 255) / 256, batch), 256, 0, s>>>(
-      w.part, w.S, w.Q, r, kr, co[0], co[1], co[2], w.rr * w.ks, w.rr);
+  if ((e = launch_chained(k_reduce_poly, dim3((r * r + 255) / 256, batch), dim3(256), 0, s, w.part,
+      w.S, w.Q, r, kr, co[0], co[1], co[2], w.rr * w.ks, w.rr)) != cudaSuccess) return e;
   if (tc) {   // Y Q: Q read with rows contiguous (its transpose's rows)
     e = launch_gemm3({Yin, r, w.dr, 0}, {w.Q, r, w.rr, 1}, Yout, r, w.dr, 0, d, r, r, batch, 1,
                      s);
     if (e != cudaSuccess) return e;
-    if (rt) k_refresh_AB<<<dim3(256, batch), 256, 0, s>>>(Yout, d, r, w.dr, *rt);
+    if (rt && (e = launch_chained(k_refresh_AB, dim3(256, batch), dim3(256), 0, s, Yout, d, r,
+        w.dr, *rt)) != cudaSuccess) return e;
   } else if (rt) {
     EpiArgs re{};
     re.rt = *rt;
-    k_sgemm<false, kRefresh, TM><<<gemm_grid(d, r, batch), 64, 0, s>>>(
-        Yin, w.Q, Yout, d, r, r, r, r, w.dr, w.rr, w.dr, 1, re);
+    if ((e = launch_chained(k_sgemm<false, kRefresh, TM>, gemm_grid(d, r, batch), dim3(64), 0, s,
+        Yin, w.Q, Yout, d, r, r, r, r, w.dr, w.rr, w.dr, 1, re)) != cudaSuccess) return e;
   } else {
-    k_sgemm<false, kStore, TM><<<gemm_grid(d, r, batch), 64, 0, s>>>(
-        Yin, w.Q, Yout, d, r, r, r, r, w.dr, w.rr, w.dr, 1, none);
+    if ((e = launch_chained(k_sgemm<false, kStore, TM>, gemm_grid(d, r, batch), dim3(64), 0, s,
+        Yin, w.Q, Yout, d, r, r, r, r, w.dr, w.rr, w.dr, 1, none)) != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
@@ -382,11 +394,12 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
                      batch, w.ks, s);
     if (e != cudaSuccess) return e;
   } else {
-    k_sgemm<true, kStore, TM><<<gemm_grid(r, r, batch * w.ks), 64, 0, s>>>(
-        A, G, w.part, r, r, d, r, r, w.dr, w.dr, w.rr * w.ks, w.ks, none);
+    if ((e = launch_chained(k_sgemm<true, kStore, TM>, gemm_grid(r, r, batch * w.ks), dim3(64), 0,
+        s, A, G, w.part, r, r, d, r, r, w.dr, w.dr, w.rr * w.ks, w.ks,
+        none)) != cudaSuccess) return e;
   }
-  k_reduce<<<dim3((r * r + 255) / 256, batch), 256, 0, s>>>(w.part, w.S, r, w.ks, 1,
-                                                            w.rr * w.ks, w.rr);
+  if ((e = launch_chained(k_reduce, dim3((r * r + 255) / 256, batch), dim3(256), 0, s, w.part, w.S,
+      r, w.ks, 1, w.rr * w.ks, w.rr)) != cudaSuccess) return e;
   // m = beta m + (1 - beta)(G - A H)
   EpiArgs mo{};
   mo.G = G;
@@ -394,13 +407,15 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
   mo.sG = w.dr;
   mo.sm = w.dr;
   mo.beta = beta;
-  k_sgemm<false, kMomentum, TM><<<gemm_grid(d, r, batch), 64, 0, s>>>(A, w.S, nullptr, d, r, r, r,
-                                                                   r, w.dr, w.rr, 0, 1, mo);
+  if ((e = launch_chained(k_sgemm<false, kMomentum, TM>, gemm_grid(d, r, batch), dim3(64), 0, s, A,
+      w.S, nullptr, d, r, r, r, r, w.dr, w.rr, 0, 1, mo)) != cudaSuccess) return e;
   // Y = m / (||m||_F + 1e-7)
-  k_sumsq_partial<<<dim3(kNormBlocks, batch), 256, 0, s>>>(m, w.dr, w.nrm_part, w.dr,
-                                                           kNormBlocks);
-  k_sumsq_final<<<batch, 32, 0, s>>>(w.nrm_part, kNormBlocks, w.inv);
-  k_scale<<<dim3(256, batch), 256, 0, s>>>(m, w.inv, w.Y0, w.dr, w.dr);
+  if ((e = launch_chained(k_sumsq_partial, dim3(kNormBlocks, batch), dim3(256), 0, s, m, w.dr,
+      w.nrm_part, w.dr, kNormBlocks)) != cudaSuccess) return e;
+  if ((e = launch_chained(k_sumsq_final, batch, dim3(32), 0, s, w.nrm_part, kNormBlocks,
+      w.inv)) != cudaSuccess) return e;
+  if ((e = launch_chained(k_scale, dim3(256, batch), dim3(256), 0, s, m, w.inv, w.Y0, w.dr,
+      w.dr)) != cudaSuccess) return e;
   float* cur = w.Y0;
   float* nxt = w.Y1;
   for (int t = 0; t < n_lmo; ++t) {
@@ -409,7 +424,8 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
     float* tmp = cur; cur = nxt; nxt = tmp;
   }
   // retraction input A - lr D
-  k_axpy<<<dim3(256, batch), 256, 0, s>>>(A, cur, lr, nxt, w.dr, w.dr);
+  if ((e = launch_chained(k_axpy, dim3(256, batch), dim3(256), 0, s, A, cur, lr, nxt, w.dr,
+      w.dr)) != cudaSuccess) return e;
   { float* tmp = cur; cur = nxt; nxt = tmp; }
   for (int t = 0; t < n_retr; ++t) {
     const bool last = t == n_retr - 1;
@@ -420,7 +436,8 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
   }
   if (n_retr == 0) {
     cudaMemcpyAsync(A, cur, sizeof(float) * w.dr * batch, cudaMemcpyDeviceToDevice, s);
-    if (rt) k_refresh_AB<<<dim3(256, batch), 256, 0, s>>>(A, d, r, w.dr, *rt);
+    if (rt && (e = launch_chained(k_refresh_AB, dim3(256, batch), dim3(256), 0, s, A, d, r, w.dr,
+        *rt)) != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

@@ -21,6 +21,7 @@
 // p[k * ld + row], i.e. the transpose of a row-major matrix).
 #include "mapl_internal.h"
 #include "ptx.cuh"
+#include "pdl.cuh"
 
 namespace mapl {
 
@@ -161,6 +162,7 @@ __device__ __forceinline__ void stash_tile(const GemmOp& op, const float4 (&v)[4
 __global__ void __launch_bounds__(kGThreads, 1)
     k_gemm3(GemmOp A, GemmOp B, float* __restrict__ C, long ldc, long sC, long sS, int K,
             int ksplit, uint64_t budget_ns) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t mma_done[2];
   __shared__ uint32_t tmem_base;
@@ -290,8 +292,8 @@ cudaError_t launch_gemm3(const Gemm3Operand& a, const Gemm3Operand& b, float* C,
   const GemmOp gb{b.p, b.ld, b.batch_stride, b.rows_contig};
   const dim3 grid(static_cast<unsigned>(N / 128), static_cast<unsigned>(M / 128),
                   static_cast<unsigned>(batch * ksplit));
-  k_gemm3<<<grid, kGThreads, kGSmem, s>>>(ga, gb, C, ldc, sC, sS, K, ksplit, kDefaultTimeoutNs);
-  return cudaGetLastError();
+  return launch_chained(k_gemm3, grid, dim3(kGThreads), kGSmem, s, ga, gb, C, ldc, sC, sS, K,
+                        ksplit, kDefaultTimeoutNs);
 }
 
 }  // namespace mapl

@@ -11,7 +11,7 @@
 // The three dropped products (mid.lo, lo.mid, lo.lo) are below 2^-24 of the
 // leading term, the size of fp32 rounding itself.
 //
-// One CTA computes a 128 x 128 tile of C[z] = opA[z] (M x K) * opB[z]^T
+// One CTA computes a 128 x 128 (or 128 x 64) tile of C[z] = opA[z] (M x K) * opB[z]^T
 // (opB: N x K) over a K range (split-K writes partial tiles).  Sixteen warps
 // load and split the fp32 operand tiles (64 K-columns per step) into two
 // shared-memory buffers while thread 0 issues the MMAs of the other buffer;
@@ -86,26 +86,32 @@ __device__ __forceinline__ float sel4(const float4& v, int j) {
   return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
 }
 
-// Global -> registers: rows [r0, r0 + 128) x K-columns [k0, k0 + 64) of an
-// operand, 4 float4 per thread (512 threads).
+// Global -> registers: rows [r0, r0 + ROWS) x K-columns [k0, k0 + 64) of an
+// operand (ROWS = 128 or 64), ROWS / 32 float4 per thread (512 threads).
 //  K contiguous: float4 i of thread t holds row (t >> 4) + 32 i, columns
 //    4 (t & 15) .. + 3 (a half-warp reads one 256-byte row).
-//  rows contiguous: float4 2 i + e holds K-column 2 kp + e, rows 4 rq .. + 3,
-//    rq = (lane & 7) | ((warp & 3) << 3), kp = (lane >> 3) | ((warp >> 2) << 2)
-//    | (i << 4) (a warp reads four 128-byte row segments per load).
+//  rows contiguous, ROWS = 128: float4 2 i + e holds K-column 2 kp + e + 32 i,
+//    rows 4 rq .. + 3, rq = (lane & 7) | ((warp & 3) << 3),
+//    kp = (lane >> 3) | ((warp >> 2) << 2) (a warp reads four 128-byte row
+//    segments per load); ROWS = 64: float4 e holds K-column 2 kp + e,
+//    rq = (lane & 7) | ((warp & 1) << 3), kp = (lane >> 3) | ((warp >> 1) << 2).
+template <int ROWS>
 __device__ __forceinline__ void fetch_tile(const GemmOp& op, const float* base, int r0, int k0,
-                                           int tid, float4 (&v)[4]) {
+                                           int tid, float4 (&v)[ROWS / 32]) {
   if (!op.rows_contig) {
     const float* p = base + static_cast<long>(r0 + (tid >> 4)) * op.ld + k0 + 4 * (tid & 15);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const float4*>(p + 32L * i * op.ld);
+    for (int i = 0; i < ROWS / 32; ++i)
+      v[i] = *reinterpret_cast<const float4*>(p + 32L * i * op.ld);
   } else {
     const int lane = tid & 31, warp = tid >> 5;
-    const int rq = (lane & 7) | ((warp & 3) << 3);
-    const int kp = (lane >> 3) | ((warp >> 2) << 2);
+    const int rq = ROWS == 128 ? ((lane & 7) | ((warp & 3) << 3))
+                               : ((lane & 7) | ((warp & 1) << 3));
+    const int kp = ROWS == 128 ? ((lane >> 3) | ((warp >> 2) << 2))
+                               : ((lane >> 3) | ((warp >> 1) << 2));
     const float* p = base + static_cast<long>(k0 + 2 * kp) * op.ld + r0 + 4 * rq;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < ROWS / 64; ++i) {
       v[2 * i] = *reinterpret_cast<const float4*>(p + 32L * i * op.ld);
       v[2 * i + 1] = *reinterpret_cast<const float4*>(p + (32L * i + 1) * op.ld);
     }
@@ -117,12 +123,13 @@ __device__ __forceinline__ void fetch_tile(const GemmOp& op, const float* base, 
 // row r at r * 128 bytes).  Both layouts store without bank conflicts: in the
 // rows-contiguous one, the eight lanes that share a K pair write their four
 // rows in a rotated order so that they hit eight different 16-byte chunks.
-__device__ __forceinline__ void stash_tile(const GemmOp& op, const float4 (&v)[4], uint32_t t0,
-                                           int tid) {
+template <int ROWS>
+__device__ __forceinline__ void stash_tile(const GemmOp& op, const float4 (&v)[ROWS / 32],
+                                           uint32_t t0, int tid) {
   if (!op.rows_contig) {
     const int q = tid & 15;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < ROWS / 32; ++i) {
       const int row = (tid >> 4) + 32 * i;
       uint32_t h01, m01, l01, h23, m23, l23;
       split_pair(v[i].x, v[i].y, h01, m01, l01);
@@ -135,12 +142,15 @@ __device__ __forceinline__ void stash_tile(const GemmOp& op, const float4 (&v)[4
     }
   } else {
     const int lane = tid & 31, warp = tid >> 5;
-    const int rq = (lane & 7) | ((warp & 3) << 3);
+    const int rq = ROWS == 128 ? ((lane & 7) | ((warp & 3) << 3))
+                               : ((lane & 7) | ((warp & 1) << 3));
     const int rot = (lane & 7) >> 1;
     const uint32_t kbyte = static_cast<uint32_t>(lane >> 3) * 4u;   // (2 kp mod 8) * 2 bytes
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint32_t chunk = static_cast<uint32_t>((warp >> 2) | (i << 2));   // k >> 3
+    for (int i = 0; i < ROWS / 64; ++i) {
+      // k >> 3 of K-column 2 kp + e (+ 32 i)
+      const uint32_t chunk = ROWS == 128 ? static_cast<uint32_t>((warp >> 2) | (i << 2))
+                                         : static_cast<uint32_t>(warp >> 1);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int jj = (j + rot) & 3;
@@ -155,10 +165,12 @@ __device__ __forceinline__ void stash_tile(const GemmOp& op, const float4 (&v)[4
   }
 }
 
-// C[z] (+ ks * sS) = opA[z] * opB[z]^T over split ks of K, fp32.
-// grid: (N / 128, M / 128, batch * ksplit); C row-major with leading
+// C[z] (+ ks * sS) = opA[z] * opB[z]^T over split ks of K, fp32, in
+// 128 x TN output tiles (TN = 128, or 64 to give a small product twice the
+// CTAs).  grid: (N / TN, M / 128, batch * ksplit); C row-major with leading
 // dimension ldc and batch stride sC.  Every wait is bounded; a CTA that gives
 // up writes NaN over its tile, so the failure reaches the caller's result.
+template <int TN>
 __global__ void __launch_bounds__(kGThreads, 1)
     k_gemm3(GemmOp A, GemmOp B, float* __restrict__ C, long ldc, long sC, long sS, int K,
             int ksplit, uint64_t budget_ns) {
@@ -170,7 +182,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
   const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int z = blockIdx.z / ksplit, ks = blockIdx.z % ksplit;
-  const int m0 = blockIdx.y * 128, n0 = blockIdx.x * 128;
+  const int m0 = blockIdx.y * 128, n0 = blockIdx.x * TN;
   const int kbeg = static_cast<int>(static_cast<long>(K) * ks / ksplit);
   const int kend = static_cast<int>(static_cast<long>(K) * (ks + 1) / ksplit);
   const int nkb = (kend - kbeg) / 64;
@@ -183,31 +195,31 @@ __global__ void __launch_bounds__(kGThreads, 1)
     abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(smem_u32(&tmem_base), 128);
+  if (warp == 0) tmem_alloc(smem_u32(&tmem_base), TN);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tacc = tmem_base;
-  constexpr uint32_t idesc = idesc_bf16(128, 128);
+  constexpr uint32_t idesc = idesc_bf16(128, TN);
   bool ok = true;
   int issued = 0;
-  float4 va[4], vb[4];
+  float4 va[4], vb[TN / 32];
 
   for (int kb = 0; kb < nkb; ++kb) {
     const int b = kb & 1;
     const uint32_t buf = sbase + static_cast<uint32_t>(b) * kGBuf;
     const int k0 = kbeg + kb * 64;
     // the loads do not touch shared memory, so they start before the wait
-    fetch_tile(A, pa, m0, k0, tid, va);
-    fetch_tile(B, pb, n0, k0, tid, vb);
+    fetch_tile<128>(A, pa, m0, k0, tid, va);
+    fetch_tile<TN>(B, pb, n0, k0, tid, vb);
     // the MMAs that read this buffer two steps ago have completed (one
     // thread waits; the barrier releases the rest)
     if (kb >= 2 && tid == 0)
       ok = mbar_wait(smem_u32(&mma_done[b]), ((kb >> 1) - 1) & 1, &abort_flag, budget_ns);
     ok = __syncthreads_and(ok) != 0;
     if (!ok) break;
-    stash_tile(A, va, buf, tid);
-    stash_tile(B, vb, buf + 3u * kGTile, tid);
+    stash_tile<128>(A, va, buf, tid);
+    stash_tile<TN>(B, vb, buf + 3u * kGTile, tid);
     fence_async_shared();
     __syncthreads();
     if (tid == 0) {
@@ -236,7 +248,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     ok = __syncthreads_and(ok && fin) != 0;
   }
   tc_fence_after();
-  if (nkb > 0) {
+  if (nkb > 0 && 32 * (warp >> 2) < TN) {
     // warp w reads TMEM lanes 32 (w & 3) .. + 31 (its lane quarter) and
     // accumulator columns 32 (w >> 2) .. + 31, and stages them row-major in
     // the (now idle) first operand buffer; rows then leave by bulk copies.
@@ -258,10 +270,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tacc, 128);
+  if (warp == 0) tmem_dealloc(tacc, TN);
   if (nkb > 0 && tid < 128) {
     bulk_store(C + z * sC + ks * sS + static_cast<long>(m0 + tid) * ldc + n0,
-               sbase + static_cast<uint32_t>(tid) * kGRowPitch, 512u);
+               sbase + static_cast<uint32_t>(tid) * kGRowPitch, 4u * TN);
     bulk_commit();
     bulk_wait<0>();
   }
@@ -284,15 +296,23 @@ cudaError_t launch_gemm3(const Gemm3Operand& a, const Gemm3Operand& b, float* C,
   if (!al16(a.p) || !al16(b.p) || !al16(C) || ((a.ld | a.batch_stride | b.ld | b.batch_stride |
                                                  ldc | sC | sS) & 3) != 0)
     return cudaErrorInvalidValue;
-  const cudaError_t e =
-      cudaFuncSetAttribute(k_gemm3, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // 128 x 64 tiles when 128 x 128 tiles would leave more than half of the
+  // SMs idle (the chain inside one CTA, not the tensor pipe, sets the time)
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long ctas128 = static_cast<long>(N / 128) * (M / 128) * batch * ksplit;
+  const bool narrow = 2 * ctas128 <= sms;
+  auto kern = narrow ? k_gemm3<64> : k_gemm3<128>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kGSmem));
   if (e != cudaSuccess) return e;
   const GemmOp ga{a.p, a.ld, a.batch_stride, a.rows_contig};
   const GemmOp gb{b.p, b.ld, b.batch_stride, b.rows_contig};
-  const dim3 grid(static_cast<unsigned>(N / 128), static_cast<unsigned>(M / 128),
+  const dim3 grid(static_cast<unsigned>(N / (narrow ? 64 : 128)), static_cast<unsigned>(M / 128),
                   static_cast<unsigned>(batch * ksplit));
-  return launch_chained(k_gemm3, grid, dim3(kGThreads), kGSmem, s, ga, gb, C, ldc, sC, sS, K,
+  return launch_chained(kern, grid, dim3(kGThreads), kGSmem, s, ga, gb, C, ldc, sC, sS, K,
                         ksplit, kDefaultTimeoutNs);
 }
 

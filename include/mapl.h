@@ -278,7 +278,11 @@ mapl_status mapl_spel_workspace_size(int64_t d, int64_t r, int32_t batch, size_t
  *   workspace  device scratch of at least mapl_spel_workspace_size bytes,
  *              owned by the caller, 256-byte aligned.
  * Requirements: r % 4 == 0, d % 4 == 0, r <= d, 1 <= n_lmo + n_retr <= 32.
- * Async.
+ * Async.  The step's kernels are launched as programmatic dependent launches
+ * (each waits for the stream's earlier work before it reads anything); a
+ * kernel that the caller launches next with programmatic stream
+ * serialization must itself wait (cudaGridDependencySynchronize) before it
+ * reads A or m.  Ordinary launches, copies and events are ordered as usual.
  */
 mapl_status mapl_spel_step(float* A, const float* G, float* m, int64_t d, int64_t r,
                            int32_t batch, float lr, float beta, const float* coeffs,

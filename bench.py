@@ -316,6 +316,21 @@ def run_ours(args, ws, rank):
     graph_ms = max_over_ranks(g0.elapsed_time(g1), ws) / (reps * nsets)
     mapl.mapl_check(plan)
 
+    # the device's plain write rate on the same rotating X_hat buffers: a
+    # fill of N x d bf16 (no reads), the floor under decompress, whose
+    # traffic is almost all X_hat writes
+    for k in range(2 * nsets):
+        Xh[k % nsets].fill_(0)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nf = 10 * nsets
+    f0.record(stream)
+    for k in range(nf):
+        Xh[k % nsets].fill_(0)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    fill_ms = f0.elapsed_time(f1) / nf
+
     # end to end through the public API's host-buffer calls: X and tids from
     # pinned host memory in, the payload out to the host and back, X_hat out
     # to pinned host memory.  Consecutive steps rotate over six streams (each
@@ -536,7 +551,13 @@ def run_ours(args, ws, rank):
                    "step": "mapl_compress + mapl_decompress on one stream"},
         "kernels": {"mapl_compress_us": comp_avg * 1e3, "mapl_decompress_us": dec_avg * 1e3,
                     "step_GBps": step_bytes / (total_ms / K * 1e-3) / 1e9,
-                    "unique_token_rows": U},
+                    "unique_token_rows": U,
+                    "x_hat_fill_us": fill_ms * 1e3,
+                    "x_hat_fill_GBps": N * w.d * 2 / (fill_ms * 1e-3) / 1e9,
+                    "decompress_vs_fill": fill_ms / dec_avg,
+                    "fill_note": "torch fill_ of the same rotating X_hat buffers (writes "
+                                 "only), timed after the step loop: the device's plain write "
+                                 "rate, the floor under decompress"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "algorithmic_bytes_per_launch": dom_bytes,

@@ -49,7 +49,7 @@ def gpu_residuals(Z32, C, idx):
     return out
 
 
-def check_vq_indices(idx_gpu, Z32_gpu, Z_oracle, C, rel_tie=1e-6, max_mismatch_frac=1e-3):
+def check_vq_indices(idx_gpu, Z32_gpu, Z_oracle, C, rel_tie=1e-6):
     """Compare GPU VQ indices with the oracle.
 
     1. Internal exactness: every GPU index is the exact (fp64) nearest code
@@ -59,8 +59,11 @@ def check_vq_indices(idx_gpu, Z32_gpu, Z_oracle, C, rel_tie=1e-6, max_mismatch_f
        oracle's, the disagreement must be a near tie certified by the size of
        the GPU's residual error delta = ||v_gpu - v_oracle||:
          D(k_gpu) - D(k_oracle) <= 2 delta (||v - c_gpu|| + ||v - c_oracle||) + 2 delta^2.
+    3. Every mismatch must also carry the oracle's own near-tie flag
+       (gap < rel_tie * ||v||^2): indices are bit-exact elsewhere.
     Returns a dict of counts (mismatches, of which inside the literal
-    rel_tie * ||v||^2 flag, and the largest certified-band ratio).
+    rel_tie * ||v||^2 flag, and the largest certified-band ratio); the
+    counts are printed as a diagnostic.
     """
     idx_gpu = np.asarray(idx_gpu).astype(np.int64)
     Cd = synth.widen(C)
@@ -107,6 +110,9 @@ def check_vq_indices(idx_gpu, Z32_gpu, Z_oracle, C, rel_tie=1e-6, max_mismatch_f
             f"index mismatch outside the certified near-tie band at n={n} rho={rho} g={g}: "
             f"gap {gap:.3g} > band {band:.3g} (delta {delta:.3g})")
     total = idx_gpu.size
-    assert len(mism) <= max(2, max_mismatch_frac * total), f"{len(mism)} mismatches of {total}"
-    return dict(total=int(total), mismatches=int(len(mism)), literal_flagged=int(in_flag),
-                unflagged=int(len(mism) - in_flag), worst_band_ratio=float(worst))
+    rep = dict(total=int(total), mismatches=int(len(mism)), literal_flagged=int(in_flag),
+               unflagged=int(len(mism) - in_flag), worst_band_ratio=float(worst))
+    print(f"VQ parity: {rep}")
+    # bit-exact except where the oracle itself flags a near tie
+    assert rep["unflagged"] == 0, f"{rep['unflagged']} unflagged index mismatches of {total}"
+    return rep

@@ -208,6 +208,68 @@ def pin_rvq_given(o):
         assert np.array_equal(a[k], b[k])
 
 
+def pin_rvq_given_diverged(o):
+    """§3.5 residual rounds, conditioned on another encoder's round-0 choice.
+
+    Hand-built one-dimensional case (G = 1, gd = 1, R = 2), values exact in
+    binary.  z = 0; round-0 codes {0, 1}: the nearest is code 0, but the other
+    encoder took code 1, so the residual carried into round 1 is 0 - 1 = -1.
+    Round-1 codes {-1, 0, 5}: from -1 the nearest is code 0 (distance 0, next
+    best code 1 at distance 1), whereas from the unconditioned residual 0 it
+    would be code 1.  A second group (z = 2, codes {2, 7} then {0, 3}) is
+    given its own nearest choices and must be unaffected.
+    """
+    Z = np.array([[0.0, 2.0]])
+    C = np.zeros((2, 2, 3, 1))
+    C[0, 0, :, 0] = [0.0, 1.0, 9.0]
+    C[1, 0, :, 0] = [-1.0, 0.0, 5.0]
+    C[0, 1, :, 0] = [2.0, 7.0, 8.0]
+    C[1, 1, :, 0] = [0.0, 3.0, 4.0]
+    given = np.array([[[1, 0], [0, 0]]])
+    res = o.rvq_encode_given(Z, C, given)
+    # round 0 is still the oracle's own decision from z
+    assert res["idx"][0, 0, 0] == 0 and res["gap"][0, 0, 0] == 1.0
+    assert res["vnorm2"][0, 0, 0] == 0.0
+    # round 1 starts from the residual the given choice left: -1
+    assert res["idx"][0, 1, 0] == 0
+    assert res["gap"][0, 1, 0] == 1.0
+    assert res["vnorm2"][0, 1, 0] == 1.0
+    assert res["residual"][0, 0] == 0.0
+    # untouched group: z = 2 -> code 0 (exact), residual 0 -> code 0 (exact)
+    assert res["idx"][0, 0, 1] == 0 and res["idx"][0, 1, 1] == 0
+    assert res["gap"][0, 0, 1] == 25.0 and res["gap"][0, 1, 1] == 9.0
+    assert res["residual"][0, 1] == 0.0
+    # without conditioning the same input follows its own choice instead
+    own = o.rvq_encode(Z, C)
+    assert own["idx"][0, 1, 0] == 1 and own["residual"][0, 0] == 0.0
+
+
+def pin_rvq_tie_flag_norm(o):
+    """The near-tie flag compares the best-to-second gap with rel_tie times the
+    squared norm of the vector quantised in that round (the group's own
+    residual), not its norm and not the whole token's.
+
+    Group 0 holds v = (3, 4), ||v||^2 = 25; group 1 holds (30, 40), whose
+    norm would dominate a whole-token reading.  Code 0 of each book is v
+    itself and code 1 is v + (delta, 0), so the gap is delta^2: 0.9e-6 * 25
+    must be flagged and 1.1e-6 * 25 must not be.
+    """
+    for frac, want in ((0.9, True), (1.1, False)):
+        delta = np.sqrt(frac * 1e-6 * 25.0)
+        Z = np.array([[3.0, 4.0, 30.0, 40.0]])
+        C = np.zeros((1, 2, 2, 2))
+        C[0, 0, 0] = [3.0, 4.0]
+        C[0, 0, 1] = [3.0 + delta, 4.0]
+        C[0, 1, 0] = [30.0, 40.0]
+        C[0, 1, 1] = [-30.0, -40.0]
+        res = o.rvq_encode(Z, C)
+        assert res["vnorm2"][0, 0, 0] == 25.0
+        assert res["idx"][0, 0, 0] == 0
+        assert abs(res["gap"][0, 0, 0] - delta ** 2) < 1e-12
+        assert bool(res["flag"][0, 0, 0]) is want
+        assert not res["flag"][0, 0, 1]
+
+
 # ----------------------------------------------------------------- §3.3 SPEL
 def pin_tangent(o):
     """eq. (4) maps onto the tangent space of St(d,r) at A, {V : sym(A^T V) = 0};

@@ -23,7 +23,10 @@ MUTANTS = {
     "rvq_last_tie": ("k = np.argmin(D, axis=1)", "k = D.shape[1] - 1 - np.argmin(D[:, ::-1], axis=1)"),
     "rvq_residual_sign": ("u[:, cols] = v - C[rho, g][take]", "u[:, cols] = v + C[rho, g][take]"),
     "rvq_no_residual": ("u[:, cols] = v - C[rho, g][take]", "u[:, cols] = v"),
-    "rvq_wrong_round_book": ("k, d1, d2 = _nearest(v, C[rho, g])", "k, d1, d2 = _nearest(v, C[0, g])"),
+    "rvq_given_ignored": ("take = k if idx_given is None else np.asarray(idx_given)[:, rho, g].astype(np.int64)", "take = k"),
+    "rvq_flag_sqrt_norm": ("flag = gap < rel_tie * vn", "flag = gap < rel_tie * np.sqrt(vn)"),
+    "rvq_flag_whole_token_norm": ('vn[:, rho, g] = np.einsum("nj,nj->n", v, v)', 'vn[:, rho, g] = np.einsum("nj,nj->n", u, u)'),
+    "rvq_wrong_round_book":("k, d1, d2 = _nearest(v, C[rho, g])", "k, d1, d2 = _nearest(v, C[0, g])"),
     "decode_one_round": ("for rho in range(R):\n        for g in range(G):\n            Zh", "for rho in range(1):\n        for g in range(G):\n            Zh"),
     "tangent_no_sym": ("return g - A @ sym(A.T @ g)", "return g - A @ (A.T @ g)"),
     "tangent_sign": ("return g - A @ sym(A.T @ g)", "return g + A @ sym(A.T @ g)"),

@@ -324,9 +324,10 @@ mapl_status mapl_spel_step_refresh(float* A, const float* G, float* m, int64_t d
  * r = 256, batch = 3 fits; d = 2048, r = 256, batch = 3 does not), otherwise
  * MAPL_ERR_UNSUPPORTED is returned and nothing runs.  The call allocates
  * nothing (no cudaMalloc, cudaFree or allocating library routine).
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *  - Every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress), so the address stays right after a device
+ *    reset.  The first call on a device also loads the library's device
+ *    code there; make that first call before any stream capture.
  *  - All calls share the one array: calls whose work overlaps on the GPU
  *    (different streams, or several threads) race on it and must be
  *    serialised by the caller.  Nothing in the array needs to start at zero;

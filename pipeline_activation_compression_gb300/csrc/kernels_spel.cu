@@ -435,7 +435,8 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
     float* tmp = cur; cur = out; nxt = tmp;
   }
   if (n_retr == 0) {
-    cudaMemcpyAsync(A, cur, sizeof(float) * w.dr * batch, cudaMemcpyDeviceToDevice, s);
+    if ((e = cudaMemcpyAsync(A, cur, sizeof(float) * w.dr * batch, cudaMemcpyDeviceToDevice,
+                             s)) != cudaSuccess) return e;
     if (rt && (e = launch_chained(k_refresh_AB, dim3(256, batch), dim3(256), 0, s, A, d, r, w.dr,
         *rt)) != cudaSuccess) return e;
   }
@@ -450,36 +451,25 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
 // The scratch lives in this file-scope device array, reserved on every GPU
 // that loads the library for as long as the process runs.  Host code cannot
 // hand the array's name to a kernel (in host code it is only a stand-in, not
-// a device address); its device address is looked up once per device with
-// cudaGetSymbolAddress, with that device current, and cached here.
+// a device address); its device address is looked up with
+// cudaGetSymbolAddress on every call, with the caller's device current.  No
+// address is cached: after a device reset or a primary-context teardown the
+// module is loaded again and a remembered address would point at freed
+// memory.  The lookup itself is a table read once the module is loaded.
 // ---------------------------------------------------------------------------
-#include <mutex>
-
 namespace mapl {
 
 namespace {
 
 __device__ __align__(256) unsigned char g_spel_scratch[kSpelStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void* g_scratch_addr[kMaxDevices] = {};
-
 }  // namespace
 
 cudaError_t spel_static_scratch(void** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_spel_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_spel_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

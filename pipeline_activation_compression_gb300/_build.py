@@ -18,8 +18,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmapl.so")
-SOURCES = ["mapl_api.cu", "kernels_compress.cu", "kernels_tc.cu", "kernels_simt.cu",
-           "kernels_spel.cu", "kernels_spel_tc.cu", "kernels_grad.cu"]
+SOURCES = ["mapl_api.cu", "kernels_compress.cu", "kernels_compress_pipe.cu", "kernels_tc.cu",
+           "kernels_simt.cu", "kernels_spel.cu", "kernels_spel_tc.cu", "kernels_grad.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", os.path.join(ROOT, "include")]

@@ -32,6 +32,10 @@ struct mapl_plan_s {
   uint32_t d_stage = 0, d_smem = 0, d_abytes = 0, d_nc = 0;
   bool d_stream = false;
   int d_nab = 0;                      // > 0: persistent kernel with d_nab A buffers
+  // pipelined compress kernel (shapes it supports), else the ring kernel above
+  bool c_pipe = false;
+  int p_nx = 0, p_nb = 0, p_ncb = 0;
+  uint32_t p_bstage = 0, p_cstage = 0, p_smem = 0;
   // projector gradient: cuBLAS handle and scratch, made on first use:
   // [P_send as fp32, r x d | S^T, r x r fp32 | E[tids], g_rows x r bf16]
   cublasHandle_t blas = nullptr;
@@ -156,6 +160,29 @@ mapl_status geometry(mapl_plan_s* pl) {
     pl->c_nstage = ns;
     pl->c_stage = st;
     pl->c_smem = ns * st + extra;
+  }
+  // pipelined compress: deep X ring (HBM), shallow B ring (A^T and -M^T
+  // blocks from L2), codebook ring
+  pl->c_pipe = compress_pipe_supported(static_cast<int>(c.r), pl->vq, pl->gd, c.G);
+  if (pl->c_pipe) {
+    const uint32_t fixed = compress_pipe_ctl_bytes() + 64 + slack;
+    const uint32_t bst = static_cast<uint32_t>(c.r) * 128u;
+    const uint32_t cst = pl->vq ? ((static_cast<uint32_t>(c.K * pl->gd) * 2u + 1023u) & ~1023u) : 0u;
+    const int ncb = pl->vq ? 4 : 0;   // two codebook stages per epilogue warp set
+    const int nb = bst > 16384u ? 3 : 4;
+    const uint32_t used = fixed + nb * bst + ncb * cst;
+    int nx = used < kSmemMax ? static_cast<int>((kSmemMax - used) / 16384u) : 0;
+    if (nx > 12) nx = 12;
+    if (nx >= 3) {
+      pl->p_nx = nx;
+      pl->p_nb = nb;
+      pl->p_ncb = ncb;
+      pl->p_bstage = bst;
+      pl->p_cstage = cst;
+      pl->p_smem = used + nx * 16384u;
+    } else {
+      pl->c_pipe = false;
+    }
   }
   const uint32_t ctl = decompress_ctl_bytes() + 64;
   // decompress.  r <= 256: persistent kernel, one CTA per SM, the A operand
@@ -605,6 +632,21 @@ static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* t
   a.nstage = pl->c_nstage;
   a.stage_bytes = pl->c_stage;
   a.timeout_ns = pl->timeout_ns;
+  if (pl->c_pipe) {
+    // one contiguous range of about N / grid rows per CTA, at least 64 rows
+    a.nstage = pl->p_nx;
+    a.stage_bytes = 16384u;
+    a.nbstage = pl->p_nb;
+    a.bstage_bytes = pl->p_bstage;
+    a.ncb = pl->p_ncb;
+    a.cstage_bytes = pl->p_cstage;
+    const int64_t want = (N + 63) / 64;
+    const int grid = static_cast<int>(want < pl->num_sms ? want : pl->num_sms);
+    e = launch_compress_pipe(tmX, pl->tmAt, emb ? pl->tmMt_emb : pl->tmMt, pl->tmC, tmE, a,
+                             pl->p_smem, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "compress launch");
+    return MAPL_OK;
+  }
   const int ntiles = static_cast<int>((N + kTile - 1) / kTile);
   const int grid = ntiles < pl->num_sms ? ntiles : pl->num_sms;
   e = launch_compress_tc(tmX, pl->tmAt, emb ? pl->tmMt_emb : pl->tmMt, pl->tmC, tmE, a,

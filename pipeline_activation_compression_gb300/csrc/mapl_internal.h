@@ -57,8 +57,12 @@ struct CompressArgs {
   int anchor;                       // 0: no anchor term (backward pass: gZ = dX_hat A)
   int re;                           // columns of the anchor table E (multiple of 64)
   int nsplit;                       // bf16 terms of -M (re x r) in the folded anchor
-  int nstage;
+  int nstage;                       // X ring stages (pipelined kernel) / ring stages
   uint32_t stage_bytes;
+  int nbstage;                      // pipelined kernel: B ring stages (A^T, -M^T blocks)
+  uint32_t bstage_bytes;            //   r x 128 bytes
+  int ncb;                          //   codebook ring stages (VQ)
+  uint32_t cstage_bytes;            //   K x gd x 2 bytes rounded up to 1024
   uint64_t timeout_ns;
 };
 
@@ -83,6 +87,10 @@ struct DecompressArgs {
 };
 
 uint32_t compress_ctl_bytes();      // control block of the compress kernel
+uint32_t compress_pipe_ctl_bytes(); // control block of the pipelined compress kernel
+// Shapes the pipelined compress kernel handles: without VQ r <= 256; with
+// VQ r in {64, 128}, group width 16 or 32, an even number of groups.
+bool compress_pipe_supported(int r, bool vq, int gd, int G);
 uint32_t decompress_ctl_bytes();    // control block of the decompress kernel
 uint32_t decompress_pt_ctl_bytes(); // control block + drain staging of the persistent kernel
 
@@ -103,6 +111,10 @@ cudaError_t launch_compress_tc(const CUtensorMap& tmX, const CUtensorMap& tmAt,
                                const CUtensorMap& tmMt, const CUtensorMap& tmC,
                                const CUtensorMap& tmE, const CompressArgs& a,
                                uint32_t smem_bytes, int grid, cudaStream_t s);
+cudaError_t launch_compress_pipe(const CUtensorMap& tmX, const CUtensorMap& tmAt,
+                                 const CUtensorMap& tmMt, const CUtensorMap& tmC,
+                                 const CUtensorMap& tmE, const CompressArgs& a,
+                                 uint32_t smem_bytes, int grid, cudaStream_t s);
 cudaError_t launch_decompress_pt(const CUtensorMap& tmB, const CUtensorMap& tmZ,
                                  const CUtensorMap& tmE, const CUtensorMap& tmXh,
                                  const DecompressArgs& a, uint32_t smem_bytes, int grid,
@@ -131,8 +143,8 @@ size_t spel_workspace_bytes(int64_t d, int64_t r, int32_t batch);
 
 // Size of the fixed device scratch behind mapl_spel_step_static (16 MiB).
 constexpr size_t kSpelStaticScratchBytes = static_cast<size_t>(16) << 20;
-// Device address of that scratch on the current device (looked up once per
-// device with cudaGetSymbolAddress and cached).
+// Device address of that scratch on the current device (cudaGetSymbolAddress
+// on every call, never cached).
 cudaError_t spel_static_scratch(void** out);
 // Plan operands written by a SPEL step's last retraction product from the
 // new fp32 A (rounded to bf16), per boundary of the batch; boundaries with

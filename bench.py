@@ -41,6 +41,8 @@ def parse():
     p.add_argument("--tokens", type=int, default=0,
                    help="tokens per step (default: the workload's micro-batch); for profiling")
     p.add_argument("--skip-cpu", action="store_true", help="skip the CPU-baseline timing")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="skip the timing of the other boundary workloads")
     return p.parse_args()
 
 
@@ -90,52 +92,71 @@ def rank_seed(rank: int) -> int:
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled during the timed region.
 
-    def __init__(self, enabled=True):
-        self.proc = None
-        self.path = None
-        if enabled:
-            try:
-                import tempfile
-                fd, self.path = tempfile.mkstemp(prefix="mapl_clocks_", suffix=".csv")
-                self.f = os.fdopen(fd, "w")
-                self.proc = subprocess.Popen(
-                    ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                     "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
-            except Exception:
-                self.proc = None
+    A background thread polls NVML (through ctypes on libnvidia-ml, read-only
+    queries) every millisecond, and one sample is taken when sampling starts
+    and one when it stops, so even a region of a few milliseconds is covered.
+    Falls back to nvidia-smi polling if NVML cannot be loaded."""
+    # clocks-event reason bits of NVML
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, enabled=True, dev_index=0):
+        import threading
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.nvml = None
+        self.thread = None
+        self.stop_flag = threading.Event()
+        if not enabled:
+            return
+        try:
+            import ctypes
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(dev_index), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            self.nvml, self.h, self.ct = lib, h, ctypes
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+        except Exception:
+            self.nvml = None
+            return
+        self._sample()
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+
+    def _sample(self):
+        ct, lib = self.ct, self.nvml
+        clk = ct.c_uint()
+        if lib.nvmlDeviceGetClockInfo(self.h, ct.c_int(1), ct.byref(clk)) == 0:   # NVML_CLOCK_SM
+            self.samples.append(float(clk.value))
+        r = ct.c_ulonglong()
+        if self.reasons_fn(self.h, ct.byref(r)) == 0:
+            for nm, bit in self.BITS.items():
+                if r.value & bit:
+                    self.reasons.add(nm)
+
+    def _loop(self):
+        while not self.stop_flag.wait(0.001):
+            self._sample()
 
     def stop(self, dev_index: int):
-        if self.proc is None:
+        if self.nvml is None:
             return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.f.close()
-        sms, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9 or not f[0].isdigit() or int(f[0]) != dev_index:
-                continue
-            try:
-                sms.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        if not sms:
+        self.stop_flag.set()
+        self.thread.join(timeout=5)
+        self._sample()
+        if not self.samples:
             return None
-        return {"sm_mhz": float(np.median(sms)), "sm_max_mhz": mx, "samples": len(sms),
-                "reasons": sorted(reasons)}
+        return {"sm_mhz": float(np.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "samples": len(self.samples), "reasons": sorted(self.reasons),
+                "source": "NVML, 1 ms polling plus the region's first and last moment"}
 
 
 def peaks():
@@ -147,7 +168,23 @@ def peaks():
     return 6800.0, "fallback"
 
 
-KERNEL_SOURCES = {"mapl_compress": "kernels_compress.cu", "mapl_decompress": "kernels_tc.cu"}
+def tensor_peak():
+    """Dense bf16 tensor peak in TFLOP/s for a kernel timed alone (burst)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def algorithmic_flops(w):
+    """Algorithmic flops per token: compress 2dr (X A) + 2r^2 (anchor fold)
+    + 2 r K R (VQ distances); decompress 4dr (the K = 2r reconstruction)."""
+    comp = 2 * w.d * w.r + 2 * w.r * w.r + (2 * w.r * w.K * w.R if w.vq else 0)
+    return float(comp), float(4 * w.d * w.r)
+
+
+KERNEL_SOURCES = {"mapl_compress": "kernels_compress_pipe.cu", "mapl_decompress": "kernels_tc.cu"}
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -190,6 +227,79 @@ def algorithmic_bytes(w, tids: np.ndarray):
     return float(comp), float(decomp), U
 
 
+# ------------------------------------------------- the other workloads
+SWEEP = ("proj_d1024_r64", "proj_d1024_r128", "proj_d1024_r256", "proj_d1024_r512",
+         "vq_d2048_r128", "vq_d2048_r256")
+
+
+def sweep_workloads(mapl, synth, stream, iters=100):
+    """Compress and decompress of the pages' other boundary workloads, each
+    at its full micro-batch, timed apart with CUDA events over rotating
+    input/output buffer sets larger than L2: tokens/s, algorithmic GB/s and
+    TFLOP/s, and the fraction of the roofline max(bytes / HBM peak, flops /
+    bf16 tensor peak) each kernel reaches."""
+    import torch
+    hbm, hbm_kind = peaks()
+    tc, tc_kind = tensor_peak()
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    out = {}
+    for name in SWEEP:
+        w = synth.WORKLOADS[name]
+        b = synth.make_boundary(w)
+        N = w.N
+
+        def dev(a):
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+            return torch.from_numpy(a).cuda()
+
+        cfg = mapl.make_config(w.d, w.r, w.V, w.G, w.R, w.K, mapl.MAPL_BF16)
+        plan = mapl.mapl_plan_create(cfg, dev(b["A"]), dev(b["P"]), dev(b["P_next"]),
+                                     dev(b["C"]) if w.vq else None)
+        E, En, t = dev(b["E"]), dev(b["E_next"]), dev(b["tids"])
+        x0 = dev(b["X"])
+        nsets = max(3, int(np.ceil(2 * l2 / (x0.numel() * 2))) + 1)
+        Xs = [x0] + [x0.clone() for _ in range(nsets - 1)]
+        Xh = [torch.empty(N, w.d, dtype=torch.bfloat16, device="cuda") for _ in range(nsets)]
+        pay = [torch.empty(plan.payload_shape(N), dtype=plan.payload_dtype(), device="cuda")
+               for _ in range(nsets)]
+        for i in range(5):
+            mapl.mapl_compress(plan, Xs[i % nsets], t, E, pay[i % nsets], stream)
+            mapl.mapl_decompress(plan, pay[i % nsets], t, En, Xh[i % nsets], stream)
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * iters + 1)]
+        ev[0].record(stream)
+        for i in range(iters):
+            k = i % nsets
+            mapl.mapl_compress(plan, Xs[k], t, E, pay[k], stream)
+            ev[2 * i + 1].record(stream)
+            mapl.mapl_decompress(plan, pay[k], t, En, Xh[k], stream)
+            ev[2 * i + 2].record(stream)
+        torch.cuda.synchronize()
+        mapl.mapl_check(plan)
+        c_ms = float(np.mean([ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(iters)]))
+        d_ms = float(np.mean([ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(iters)]))
+        cb, db, U = algorithmic_bytes(w, b["tids"])
+        cf, df = algorithmic_flops(w)
+        entry = {"tokens": N, "tokens_per_s": N / ((c_ms + d_ms) * 1e-3)}
+        for kname, ms, by, fl in (("compress", c_ms, cb, cf * N), ("decompress", d_ms, db, df * N)):
+            t_hbm = by / (hbm * 1e9)
+            t_tc = fl / (tc * 1e12)
+            entry[kname] = {"us": ms * 1e3, "GBps": by / (ms * 1e-3) / 1e9,
+                            "TFLOPs": fl / (ms * 1e-3) / 1e12,
+                            "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                            "frac": max(t_hbm, t_tc) / (ms * 1e-3)}
+        out[name] = entry
+        plan.destroy()
+        del Xs, Xh, pay
+        torch.cuda.empty_cache()
+    out["note"] = (f"roofline = max(algorithmic bytes / {hbm:.0f} GB/s ({hbm_kind}), algorithmic "
+                   f"flops / {tc:.0f} TFLOP/s bf16 ({tc_kind})); {iters} calls each, rotating "
+                   "buffer sets larger than L2")
+    return out
+
+
 # ------------------------------------------------------------- CPU oracle
 def oracle_step(b, w, rows):
     import oracle
@@ -226,6 +336,44 @@ def time_oracle(b, w, tokens: int, budget_s: float):
         el = time.perf_counter() - t0
         if el >= budget_s:
             return done / el, done, el
+
+
+def _oracle_worker(job):
+    """One CPU-baseline process: its own sample of the workload, then the
+    oracle on random chunks of it for `budget` seconds (BLAS on one thread:
+    the parent sets the thread-count variables before spawning)."""
+    name, seed, tokens, budget = job
+    from pipeline_activation_compression_gb300 import synth
+    w = synth.WORKLOADS[name]
+    b = synth.make_boundary(w, seed=seed, n_tokens=4 * tokens)
+    rate, done, el = time_oracle(b, w, tokens, budget)
+    return done, el
+
+
+def cpu_baseline(name: str, budget_s: float = 10.0, tokens: int = 256):
+    """The oracle as it stands on the host cores: one process per core, each
+    single-threaded, timed together (tokens/s summed over the processes), and
+    one process alone (the 1-thread figure)."""
+    import multiprocessing as mp
+    keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in keys}
+    for k in keys:
+        os.environ[k] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        n = cpu_threads()
+        with ctx.Pool(n) as pool:
+            res = pool.map(_oracle_worker, [(name, 100 + i, tokens, budget_s) for i in range(n)])
+            one = pool.map(_oracle_worker, [(name, 99, tokens, budget_s / 2)])
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    total = sum(d / e for d, e in res)
+    done = sum(d for d, _ in res)
+    return total, n, done, one[0][0] / one[0][1]
 
 
 # --------------------------------------------------------------- our arm
@@ -275,7 +423,7 @@ def run_ours(args, ws, rank):
 
     K = args.steps
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K + 1)]
-    clocks = ClockSampler(enabled=(rank == 0 and not args.no_clocks))
+    clocks = ClockSampler(enabled=(rank == 0 and not args.no_clocks), dev_index=dev)
     barrier(ws)
     torch.cuda.synchronize()
     ev[0].record(stream)
@@ -537,8 +685,10 @@ def run_ours(args, ws, rank):
                          "X_hat = Z_hat A^T + E_emb[t]; update_A includes the E_emb A table")
         plan_e.destroy()
 
-    # CPU baseline: the oracle as it stands, bounded sample
-    cps, done, el = (0.0, 0, 0.0) if args.skip_cpu else time_oracle(b, w, min(1024, N), 10.0)
+    workloads = {} if args.no_sweep else sweep_workloads(mapl, synth, stream)
+
+    # CPU baseline: the oracle as it stands, bounded sample on every host core
+    cps, ncores, done, cps1 = (0.0, 0, 0, 0.0) if args.skip_cpu else cpu_baseline(w.name)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
@@ -574,14 +724,16 @@ def run_ours(args, ws, rank):
                          "workload, 200 calls each, inputs L2-warm"),
         "spel": spel,
         "first_boundary": first,
+        "workloads": workloads,
         "cuda_graph": {"value": whole_job_rate(N, ws, graph_ms), "unit": UNIT,
                        "ms_per_step": graph_ms, "steps": reps * nsets,
                        "note": "compress + decompress captured once per buffer set, replayed"},
         "gpu_launches": 2 * K,
-        "cpu_baseline": {"value": cps, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                         "sample": f"{done} tokens of {w.name} in chunks of 1024 random rows, "
-                                   f"{el:.1f} s (numpy fp64; BLAS threads for the GEMMs, "
-                                   f"VQ search single-threaded)"},
+        "cpu_baseline": {"value": cps, "unit": UNIT, "cores": ncores, "kind": "oracle",
+                         "one_thread_value": cps1,
+                         "sample": f"{done} tokens of {w.name} in chunks of 256 random rows: "
+                                   f"{ncores} single-threaded processes for 10 s each, rates "
+                                   f"summed (numpy fp64), and one process alone for 5 s"},
     }
     if clk is not None:
         res["clocks"] = clk

@@ -540,10 +540,11 @@ def run_ours(args, ws, rank):
     gX = torch.empty(N, w.d, dtype=torch.bfloat16, device="cuda")
     Zb = torch.empty(N, w.r, dtype=torch.bfloat16, device="cuda")
     dA = torch.empty(w.d, w.r, dtype=torch.float32, device="cuda")
+    gws = torch.empty(mapl.mapl_grad_workspace_size(plan, N), dtype=torch.uint8, device="cuda")
     bw_calls = [
         ("grad_compress_us", lambda: mapl.mapl_grad_compress(plan, gxh, gZ, stream)),
         ("grad_decompress_us", lambda: mapl.mapl_grad_decompress(plan, gZ, gX, stream)),
-        ("grad_A_us", lambda: mapl.mapl_grad_A(plan, x0, t, E, gZ, gxh, Zb, dA, stream)),
+        ("grad_A_us", lambda: mapl.mapl_grad_A(plan, x0, t, E, gZ, gxh, Zb, dA, gws, stream)),
     ]
     backward = {}
     for key, fn in bw_calls:

@@ -190,12 +190,20 @@ mapl_status mapl_plan_update_codes(mapl_plan plan, const int32_t* ids, int32_t c
  *   dA = X_res^T gZ + gX_hat^T Z,  X_res = X - E_send[tids] P_send
  *   X, gX_hat N x d; gZ, Z N x r (bf16; Z as the pipeline has it, e.g. the
  *   decoded payload); tids N; E_send V x r;  dA  d x r fp32 out.
- *   Computed as X^T gZ + gX_hat^T Z - P_send^T (E_send[tids]^T gZ): plain
- *   GEMMs in cuBLAS (bf16 in, fp32 accumulation) after the library gathers
- *   E_send[tids].  The first call on a plan, and a call with a larger N than
- *   any before, creates the plan's cuBLAS handle / grows its scratch
- *   (N x r bf16 + r x d + r x r fp32): it synchronises `stream` and cannot
- *   be captured in a CUDA graph; later calls can.
+ *   Computed as X^T gZ + gX_hat^T Z - P_send^T (E_send[tids]^T gZ) on the
+ *   tensor cores (bf16 in, fp32 accumulation) in one cooperative launch
+ *   (one CTA per SM; preceded by a 4-byte memset of the workspace's grid
+ *   barrier), split over token ranges whose partial sums go to `workspace`
+ *   and are then added in a fixed order, so the result is the same on every
+ *   call (with an embedding-anchor plan, the last term is E_emb[tids]^T gZ
+ *   and E_send may be NULL).  Token ids outside [0, V) contribute no anchor
+ *   term and set MAPL_ERR_BAD_TOKEN in the plan's error word.
+ *   workspace  device, 256-byte aligned, at least
+ *              mapl_grad_workspace_size(plan, N) bytes, owned by the caller,
+ *              not read before it is written; calls that overlap on the GPU
+ *              need workspaces of their own.  The call allocates nothing.
+ * mapl_grad_workspace_size  bytes of workspace mapl_grad_A needs for N tokens
+ *   (about 30 MiB at d = 1024, r = 128 on 152 SMs).
  * Async on `stream`.
  */
 mapl_status mapl_grad_compress(mapl_plan plan, const void* gX_hat, int64_t N, void* gZ,
@@ -204,9 +212,12 @@ mapl_status mapl_grad_compress(mapl_plan plan, const void* gX_hat, int64_t N, vo
 mapl_status mapl_grad_decompress(mapl_plan plan, const void* gZ, int64_t N, void* gX,
                                  cudaStream_t stream);
 
+mapl_status mapl_grad_workspace_size(mapl_plan plan, int64_t N, size_t* bytes);
+
 mapl_status mapl_grad_A(mapl_plan plan, const void* X, const int32_t* tids, const void* E_send,
                         const void* gZ, const void* gX_hat, const void* Z, int64_t N,
-                        float* dA, cudaStream_t stream);
+                        float* dA, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
 
 /*
  * Host-buffer forms of mapl_compress / mapl_decompress, for callers whose

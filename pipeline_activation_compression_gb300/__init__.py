@@ -20,7 +20,7 @@ __all__ = [
     "mapl_payload_bytes", "mapl_compress",
     "mapl_compress_z32", "mapl_decompress", "mapl_check", "mapl_plan_destroy",
     "mapl_host_workspace_size", "mapl_compress_host", "mapl_decompress_host",
-    "mapl_grad_compress", "mapl_grad_decompress", "mapl_grad_A",
+    "mapl_grad_compress", "mapl_grad_decompress", "mapl_grad_workspace_size", "mapl_grad_A",
     "mapl_stream_subset", "mapl_plan_update_codes", "mapl_selftest_bounded_wait",
     "mapl_spel_workspace_size", "mapl_spel_step", "mapl_spel_step_refresh",
     "mapl_spel_step_static", "mapl_last_error",
@@ -81,7 +81,8 @@ def load_library():
         "mapl_host_workspace_size": [P, I64, ctypes.POINTER(SZ)],
         "mapl_grad_compress": [P, P, I64, P, P],
         "mapl_grad_decompress": [P, P, I64, P, P],
-        "mapl_grad_A": [P, P, P, P, P, P, P, I64, P, P],
+        "mapl_grad_workspace_size": [P, I64, ctypes.POINTER(SZ)],
+        "mapl_grad_A": [P, P, P, P, P, P, P, I64, P, P, SZ, P],
         "mapl_stream_subset": [I64, I64, ctypes.c_uint64, I64, P, ctypes.POINTER(I32)],
         "mapl_plan_update_codes": [P, P, I32, P, P],
         "mapl_compress_host": [P, P, P, I64, P, P, P, SZ, P],
@@ -298,14 +299,28 @@ def mapl_grad_decompress(plan: Plan, gZ, gX, stream=None):
     return gX
 
 
-def mapl_grad_A(plan: Plan, X, tids, E_send, gZ, gX_hat, Z, dA, stream=None):
-    """dA = (X - E_send[tids] P_send)^T gZ + gX_hat^T Z, fp32 d x r."""
+def mapl_grad_workspace_size(plan: Plan, N: int) -> int:
+    """Bytes of device workspace mapl_grad_A needs for N tokens."""
+    n = ctypes.c_size_t(0)
+    _check(load_library().mapl_grad_workspace_size(plan.handle, int(N), ctypes.byref(n)))
+    return int(n.value)
+
+
+def mapl_grad_A(plan: Plan, X, tids, E_send, gZ, gX_hat, Z, dA, workspace=None, stream=None):
+    """dA = (X - E_send[tids] P_send)^T gZ + gX_hat^T Z, fp32 d x r.  The
+    workspace (a device tensor of at least mapl_grad_workspace_size bytes) is
+    the caller's; without one a tensor of that size is made for the call."""
     import torch
+    N = int(X.shape[0])
+    if workspace is None:
+        workspace = torch.empty(mapl_grad_workspace_size(plan, N), dtype=torch.uint8,
+                                device=X.device)
     _check(load_library().mapl_grad_A(
         plan.handle, _ptr(X, torch.bfloat16, "X"), _ptr(tids, torch.int32, "tids"),
         _ptr(E_send, torch.bfloat16, "E_send"), _ptr(gZ, torch.bfloat16, "gZ"),
         _ptr(gX_hat, torch.bfloat16, "gX_hat"), _ptr(Z, torch.bfloat16, "Z"),
-        int(X.shape[0]), _ptr(dA, torch.float32, "dA"), _stream(stream)))
+        N, _ptr(dA, torch.float32, "dA"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
     return dA
 
 

@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmapl.so")
 SOURCES = ["mapl_api.cu", "kernels_compress.cu", "kernels_compress_pipe.cu", "kernels_tc.cu",
-           "kernels_simt.cu", "kernels_spel.cu", "kernels_spel_tc.cu", "kernels_grad.cu"]
+           "kernels_simt.cu", "kernels_spel.cu", "kernels_spel_tc.cu", "kernels_grad.cu",
+           "kernels_grad_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", os.path.join(ROOT, "include")]
@@ -63,7 +64,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
     tmp = LIB + ".tmp"
-    # cuBLAS serves the two plain GEMMs of the projector gradient only
+    # cuBLAS serves two plan-time products only: M = P_send A of a bf16 plan and
+    # the first-boundary table E_emb A
     cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-lcublas",
            "-Xlinker", "-rpath=" + os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(_nvcc()))),
                                                 "lib64")]

@@ -36,11 +36,9 @@ struct mapl_plan_s {
   bool c_pipe = false;
   int p_nx = 0, p_nb = 0, p_ncb = 0;
   uint32_t p_bstage = 0, p_cstage = 0, p_smem = 0;
-  // projector gradient: cuBLAS handle and scratch, made on first use:
-  // [P_send as fp32, r x d | S^T, r x r fp32 | E[tids], g_rows x r bf16]
+  // cuBLAS handle for the plan-time products (M = P_send A and the
+  // first-boundary table E_emb A), made on first use
   cublasHandle_t blas = nullptr;
-  void* gws = nullptr;
-  int64_t g_rows = 0, g_cols = 0;
   // sender anchor: E_send[tids] P_send (re = r, three -M terms), or with
   // mapl_plan_set_embedding_anchor the first-boundary E_emb[tids] (re = 3r,
   // one term): table [hi|mid|lo] of E_emb A and -[I; I; I]
@@ -101,6 +99,24 @@ bool make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D bf16 tensor map viewing a row-major (outer x inner) matrix as
+// {64 elements, outer rows, inner / 64 atoms}: one box of {64, box_outer,
+// box_atoms} lands in shared memory as box_atoms consecutive 128-byte
+// swizzled atoms of box_outer rows (atoms past the matrix read zeros).
+bool make_tmap_atoms(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
+                     uint32_t box_outer, uint32_t box_atoms) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, outer, inner / 64};
+  cuuint64_t strides[2] = {inner * 2, 128};
+  cuuint32_t box[3] = {64, box_outer, box_atoms};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -569,7 +585,6 @@ mapl_status mapl_stream_subset(int64_t total, int64_t per_batch, uint64_t seed, 
 void mapl_plan_destroy(mapl_plan pl) {
   if (!pl) return;
   if (pl->blas) cublasDestroy(pl->blas);
-  if (pl->gws) cudaFree(pl->gws);
   if (pl->emb_pool) cudaFree(pl->emb_pool);
   if (pl->p.pool) cudaFree(pl->p.pool);
   delete pl;
@@ -760,94 +775,122 @@ mapl_status mapl_grad_decompress(mapl_plan pl, const void* gZ, int64_t N, void* 
   return decompress_common(pl, gZ, nullptr, N, nullptr, gX, stream, false);
 }
 
-mapl_status mapl_grad_A(mapl_plan pl, const void* X, const int32_t* tids, const void* E_send,
-                        const void* gZ, const void* gX_hat, const void* Z, int64_t N, float* dA,
-                        cudaStream_t stream) {
-  if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
-  const bool emb = pl->E_emb != nullptr;   // first-boundary anchor: E_send is not read
-  if (!X || !tids || (!E_send && !emb) || !gZ || !gX_hat || !Z || !dA)
-    return fail(MAPL_ERR_INVALID_ARG, "NULL tensor pointer");
+namespace {
+
+// Token splits, tiles and K block of the projector gradient for N tokens.
+struct GradGeom {
+  int nX, nE, S, W, nM, kb, nstage;
+  bool fold;
+  uint32_t smem;
+  size_t ws_bar, ws_partials, ws_fold, ws_T, ws_total;
+};
+
+// Column tiles of W = 256 (128 when r = 512, so that the r / 128 M blocks of
+// 128 x W fp32 accumulators fit TMEM's 512 columns), 32-token blocks, as many
+// ring stages as shared memory holds, and S token splits per tile so that
+// the grid is at most one CTA per SM.
+GradGeom grad_geom(const mapl_plan_s* pl, int64_t N) {
+  const mapl_config& c = pl->cfg;
+  GradGeom g{};
+  const bool emb = pl->E_emb != nullptr;
+  g.fold = !emb && c.r <= 128;
+  g.W = c.r <= 256 ? 256 : 128;
+  g.nM = static_cast<int>((c.r + 127) / 128);
+  g.nX = static_cast<int>((c.d + g.W - 1) / g.W);
+  g.nE = emb ? g.nX : (g.fold ? 0 : static_cast<int>((c.r + g.W - 1) / g.W));
+  g.kb = 32;
+  const uint32_t st = grad_stage_bytes(static_cast<int>(c.r), g.W, g.kb);
+  int ns = static_cast<int>((kSmemMax - 2048u - grad_ctl_bytes() - grad_fring_bytes(g.kb)) / st);
+  if (ns > kGradMaxStages) ns = kGradMaxStages;
+  g.nstage = ns;
+  g.smem = ns * st + grad_fring_bytes(g.kb) + 1024u + grad_ctl_bytes() + 64u;
+  const int64_t nkb = (N + g.kb - 1) / g.kb;
+  int S = pl->num_sms / (g.nX + g.nE);
+  if (S < 1) S = 1;
+  if (S > nkb) S = static_cast<int>(nkb);
+  g.S = S;
+  g.ws_bar = 256;
+  g.ws_partials = up256(static_cast<size_t>(g.nX + g.nE) * S * g.W * c.r * sizeof(float));
+  g.ws_fold = g.fold ? up256(static_cast<size_t>(g.nX) * S * c.r * c.r * sizeof(float)) : 0;
+  g.ws_T = up256(static_cast<size_t>(c.r) * c.r * sizeof(float));
+  g.ws_total = g.ws_bar + g.ws_partials + g.ws_fold + g.ws_T;
+  return g;
+}
+
+}  // namespace
+
+mapl_status mapl_grad_workspace_size(mapl_plan pl, int64_t N, size_t* bytes) {
+  if (!pl || !bytes) return fail(MAPL_ERR_INVALID_ARG, "NULL argument");
   if (N < 1 || N > 0x7fffffffLL) return fail(MAPL_ERR_INVALID_ARG, "N must be in [1, 2^31)");
   if (!pl->tc) return fail(MAPL_ERR_UNSUPPORTED, "gradient calls need a bf16 (tensor-core) plan");
-  if (!emb && !aligned16(E_send)) return fail(MAPL_ERR_INVALID_ARG, "E_send must be 16-byte aligned");
+  *bytes = grad_geom(pl, N).ws_total;
+  return MAPL_OK;
+}
+
+mapl_status mapl_grad_A(mapl_plan pl, const void* X, const int32_t* tids, const void* E_send,
+                        const void* gZ, const void* gX_hat, const void* Z, int64_t N, float* dA,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
+  const bool emb = pl->E_emb != nullptr;   // first-boundary anchor: E_send is not read
+  if (!X || !tids || (!E_send && !emb) || !gZ || !gX_hat || !Z || !dA || !workspace)
+    return fail(MAPL_ERR_INVALID_ARG, "NULL pointer argument");
+  if (N < 1 || N > 0x7fffffffLL) return fail(MAPL_ERR_INVALID_ARG, "N must be in [1, 2^31)");
+  if (!pl->tc) return fail(MAPL_ERR_UNSUPPORTED, "gradient calls need a bf16 (tensor-core) plan");
+  if (!aligned16(X) || !aligned16(gZ) || !aligned16(gX_hat) || !aligned16(Z) || !aligned16(dA) ||
+      (!emb && !aligned16(E_send)) || (reinterpret_cast<uintptr_t>(tids) & 3u))
+    return fail(MAPL_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned (tids 4-byte)");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(MAPL_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   mapl_status st = check_device(pl);
   if (st != MAPL_OK) return st;
   const mapl_config& c = pl->cfg;
-  const size_t r = static_cast<size_t>(c.r), d = static_cast<size_t>(c.d);
-  const size_t oP = 0, oT = up256(r * d * 4), oEg = oT + up256(r * r * 4);
-  const int64_t gcols = emb ? c.d : c.r;   // columns of the gathered anchor rows
-  cudaError_t e;
-  if (!pl->blas) {
-    if (cublasCreate(&pl->blas) != CUBLAS_STATUS_SUCCESS) {
-      pl->blas = nullptr;
-      return fail(MAPL_ERR_CUDA, "cublasCreate failed");
-    }
-  }
-  if (!pl->gws || pl->g_rows < N || pl->g_cols < gcols) {
-    // scratch sized for N gathered anchor rows; P_send is widened once per buffer
-    e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-    if (pl->gws) cudaFree(pl->gws);
-    pl->gws = nullptr;
-    pl->g_rows = 0;
-    e = cudaMalloc(&pl->gws, oEg + up256(static_cast<size_t>(N) * gcols * 2));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(gradient scratch)");
-    pl->g_rows = N;
-    pl->g_cols = gcols;
-    e = launch_widen(reinterpret_cast<const __nv_bfloat16*>(pl->p.Ps), r * d,
-                     reinterpret_cast<float*>(static_cast<char*>(pl->gws) + oP), stream);
-    if (e != cudaSuccess) return cuda_fail(e, "widen P_send");
-  }
-  char* ws = static_cast<char*>(pl->gws);
-  float* P32 = reinterpret_cast<float*>(ws + oP);
-  float* T = reinterpret_cast<float*>(ws + oT);
-  __nv_bfloat16* Eg = reinterpret_cast<__nv_bfloat16*>(ws + oEg);
-  e = launch_gather_rows(tids, reinterpret_cast<const __nv_bfloat16*>(emb ? pl->E_emb : E_send),
-                         static_cast<int>(N), static_cast<int>(c.V), static_cast<int>(gcols), Eg,
-                         stream);
-  if (e != cudaSuccess) return cuda_fail(e, "gather E[tids]");
-  if (cublasSetStream(pl->blas, stream) != CUBLAS_STATUS_SUCCESS)
-    return fail(MAPL_ERR_CUDA, "cublasSetStream failed");
-  if (emb) {
-    // Z = (X - E_emb[tids]) A, X_hat = Z_hat A^T + E_emb[tids]:
-    //   dA^T (r x d) = gZ^T X - gZ^T E_emb[tids] + Z^T gX_hat
-    const int m = static_cast<int>(r), n = static_cast<int>(d), k = static_cast<int>(N);
-    const float one = 1.f, zero = 0.f, minus = -1.f;
-    cublasStatus_t bs = cublasGemmEx(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, n, k, &one, gZ,
-                                     CUDA_R_16BF, m, X, CUDA_R_16BF, n, &zero, dA, CUDA_R_32F, m,
-                                     CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-    if (bs == CUBLAS_STATUS_SUCCESS)
-      bs = cublasGemmEx(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, n, k, &minus, gZ, CUDA_R_16BF, m,
-                        Eg, CUDA_R_16BF, n, &one, dA, CUDA_R_32F, m, CUBLAS_COMPUTE_32F,
-                        CUBLAS_GEMM_DEFAULT);
-    if (bs == CUBLAS_STATUS_SUCCESS)
-      bs = cublasGemmEx(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, n, k, &one, Z, CUDA_R_16BF, m,
-                        gX_hat, CUDA_R_16BF, n, &one, dA, CUDA_R_32F, m, CUBLAS_COMPUTE_32F,
-                        CUBLAS_GEMM_DEFAULT);
-    if (bs != CUBLAS_STATUS_SUCCESS) return fail(MAPL_ERR_CUDA, "cuBLAS GEMM failed (%d)", (int)bs);
-    return MAPL_OK;
-  }
-  // Everything column-major (the row-major tensors read transposed):
-  //   dA^T (r x d)  = gZ^T X + Z^T gX_hat - (E[tids]^T gZ)^T P
-  //   T = S^T (r x r) = gZ^T E[tids]
-  const int m = static_cast<int>(r), n = static_cast<int>(d), k = static_cast<int>(N);
-  const float one = 1.f, zero = 0.f, minus = -1.f;
-  cublasStatus_t bs = cublasGemmEx(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, n, k, &one, gZ,
-                                   CUDA_R_16BF, m, X, CUDA_R_16BF, n, &zero, dA, CUDA_R_32F, m,
-                                   CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-  if (bs == CUBLAS_STATUS_SUCCESS)
-    bs = cublasGemmEx(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, n, k, &one, Z, CUDA_R_16BF, m,
-                      gX_hat, CUDA_R_16BF, n, &one, dA, CUDA_R_32F, m, CUBLAS_COMPUTE_32F,
-                      CUBLAS_GEMM_DEFAULT);
-  if (bs == CUBLAS_STATUS_SUCCESS)
-    bs = cublasGemmEx(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, m, k, &one, gZ, CUDA_R_16BF, m, Eg,
-                      CUDA_R_16BF, m, &zero, T, CUDA_R_32F, m, CUBLAS_COMPUTE_32F,
-                      CUBLAS_GEMM_DEFAULT);
-  // dA^T -= T P, with P (r x d row-major) read as the column-major d x r P^T
-  if (bs == CUBLAS_STATUS_SUCCESS)
-    bs = cublasSgemm(pl->blas, CUBLAS_OP_N, CUBLAS_OP_T, m, n, m, &minus, T, m, P32, n, &one, dA,
-                     m);
-  if (bs != CUBLAS_STATUS_SUCCESS) return fail(MAPL_ERR_CUDA, "cuBLAS GEMM failed (%d)", (int)bs);
+  const GradGeom g = grad_geom(pl, N);
+  if (workspace_bytes < g.ws_total)
+    return fail(MAPL_ERR_INVALID_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                g.ws_total);
+  // MN-major slabs: boxes of 64 elements x kb tokens x the slab's 64-element
+  // atoms (W / 64 of X and dL/dX_hat, 2 per 128 rows of r of gZ and Z); the
+  // anchor table of an E tile by four-row gathers of one 64-element segment
+  const uint32_t kb = static_cast<uint32_t>(g.kb);
+  const uint32_t nB = static_cast<uint32_t>(g.W / 64), nA = static_cast<uint32_t>(2 * g.nM);
+  CUtensorMap tmX, tmGX, tmGZ, tmZ, tmE;
+  if (!make_tmap_atoms(&tmX, X, c.d, static_cast<uint64_t>(N), kb, nB) ||
+      !make_tmap_atoms(&tmGX, gX_hat, c.d, static_cast<uint64_t>(N), kb, nB) ||
+      !make_tmap_atoms(&tmGZ, gZ, c.r, static_cast<uint64_t>(N), kb, nA) ||
+      !make_tmap_atoms(&tmZ, Z, c.r, static_cast<uint64_t>(N), kb, nA))
+    return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (gradient operands)");
+  const void* table = emb ? pl->E_emb : E_send;
+  const uint64_t tcols = emb ? static_cast<uint64_t>(c.d) : static_cast<uint64_t>(c.r);
+  if (!make_tmap(&tmE, table, tcols, static_cast<uint64_t>(c.V), 64, 1))
+    return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (anchor table)");
+  char* wsb = static_cast<char*>(workspace);
+  GradArgs a{};
+  a.tids = tids;
+  a.E = static_cast<const __nv_bfloat16*>(E_send);
+  a.P = reinterpret_cast<const __nv_bfloat16*>(pl->p.Ps);
+  a.err = pl->p.err;
+  a.bar = reinterpret_cast<unsigned int*>(wsb);
+  a.ws = reinterpret_cast<float*>(wsb + g.ws_bar);
+  a.wsT = reinterpret_cast<float*>(wsb + g.ws_bar + g.ws_partials);
+  a.T = reinterpret_cast<float*>(wsb + g.ws_bar + g.ws_partials + g.ws_fold);
+  a.dA = dA;
+  a.N = static_cast<int>(N);
+  a.d = static_cast<int>(c.d);
+  a.r = static_cast<int>(c.r);
+  a.V = static_cast<int>(c.V);
+  a.S = g.S;
+  a.nX = g.nX;
+  a.nE = g.nE;
+  a.W = g.W;
+  a.nM = g.nM;
+  a.kb = g.kb;
+  a.nstage = g.nstage;
+  a.emb = emb ? 1 : 0;
+  a.fold = g.fold ? 1 : 0;
+  a.timeout_ns = pl->timeout_ns;
+  const cudaError_t e =
+      launch_grad_A(tmX, tmGX, tmGZ, tmZ, tmE, a, (g.nX + g.nE) * g.S, g.smem, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gradient launch");
   return MAPL_OK;
 }
 

@@ -119,11 +119,33 @@ cudaError_t launch_decompress_pt(const CUtensorMap& tmB, const CUtensorMap& tmZ,
                                  const CUtensorMap& tmE, const CUtensorMap& tmXh,
                                  const DecompressArgs& a, uint32_t smem_bytes, int grid,
                                  cudaStream_t s);
-// Projector-gradient helpers: Eg[n] = E[tids[n]] (N x r), and a bf16 -> fp32
-// copy.
-cudaError_t launch_gather_rows(const int32_t* tids, const __nv_bfloat16* E, int N, int V, int r,
-                               __nv_bfloat16* Eg, cudaStream_t s);
-cudaError_t launch_widen(const __nv_bfloat16* a, size_t n, float* b, cudaStream_t s);
+// Projector gradient on the tensor cores (kernels_grad_tc.cu).  Output
+// tiles: nX of 128 rows of d (X^T gZ + gXh^T Z) and nE of 128 rows of the
+// anchor table's columns (E[tids]^T gZ), each split into S token ranges of
+// whole K blocks of kb tokens; partials in ws, (nX + nE) x S x 128 x r fp32.
+struct GradArgs {
+  const int32_t* tids;
+  const __nv_bfloat16* E;           // E_send (V x r), factored anchor
+  const __nv_bfloat16* P;           // P_send (r x d), factored anchor
+  int* err;
+  unsigned int* bar;                // grid-barrier counter, zeroed before the launch
+  float* ws;                        // column-tile partials, (nX + nE) x S x W x r
+  float* wsT;                       // folded anchor partials, nX x S x r x r (fold only)
+  float* T;                         // E[tids]^T gZ, r x r (factored anchor)
+  float* dA;
+  int N, d, r, V;
+  int S, nX, nE, W, nM, kb, nstage;
+  int emb;                          // first-boundary anchor: E tiles over d, subtracted
+  int fold;                         // factored anchor folded into the X tiles (r <= 128)
+  uint64_t timeout_ns;
+};
+constexpr int kGradMaxStages = 8;
+uint32_t grad_stage_bytes(int r, int W, int kb);
+uint32_t grad_fring_bytes(int kb);   // the folded-gather ring, whole
+uint32_t grad_ctl_bytes();
+cudaError_t launch_grad_A(const CUtensorMap& tmX, const CUtensorMap& tmGX, const CUtensorMap& tmGZ,
+                          const CUtensorMap& tmZ, const CUtensorMap& tmE, const GradArgs& a,
+                          int grid, uint32_t smem, cudaStream_t s);
 // First-boundary anchor: T (V x r fp32) -> [hi | mid | lo] bf16 (V x 3r), and
 // the r x 3r operand -[I; I; I]^T.
 cudaError_t launch_split3(const float* T, size_t V, int r, __nv_bfloat16* Tb, cudaStream_t s);

@@ -95,3 +95,37 @@ def test_backward_full_size():
     dA_or = oracle.grad_A_given(W(b["X"]), b["tids"], W(b["E"]), W(b["P"]), W(gZ), W(gxh), W(Z))
     assert rel_frob(dA, dA_or) <= TOL_F32
     assert np.isfinite(dA).all()
+
+
+@pytest.mark.parametrize("name,n", [("vq_d1024_r128", 3001), ("proj_d1024_r256", 1000)])
+def test_grad_A_same_bits_every_call_and_bad_ids(name, n):
+    """Two calls give the same bits (the split sums are added in a fixed
+    order), and token ids outside [0, V) set MAPL_ERR_BAD_TOKEN and contribute
+    no anchor term: the oracle's result with those tokens' anchor rows zero."""
+    w = synth.WORKLOADS[name]
+    b = synth.make_boundary(w, seed=8, n_tokens=n)
+    gxh = synth.make_boundary_grad(w, seed=8, n_tokens=n)
+    plan = _plan(w, b)
+    tids = b["tids"].copy()
+    bad = np.array([0, 5, n // 2, n - 1])
+    tids[bad] = np.array([-1, w.V, w.V + 7, -(2 ** 31)], dtype=tids.dtype)
+    X, t, E = to_dev(b["X"]), torch.from_numpy(tids).cuda(), to_dev(b["E"])
+    gXh, Z = to_dev(gxh), to_dev(b["X"][:, : w.r])
+    gZ = torch.empty(n, w.r, dtype=torch.bfloat16, device="cuda")
+    mapl.mapl_grad_compress(plan, gXh, gZ)
+    ws = torch.empty(mapl.mapl_grad_workspace_size(plan, n), dtype=torch.uint8, device="cuda")
+    dA1 = torch.empty(w.d, w.r, dtype=torch.float32, device="cuda")
+    dA2 = torch.empty_like(dA1)
+    mapl.mapl_grad_A(plan, X, t, E, gZ, gXh, Z, dA1, ws)
+    mapl.mapl_grad_A(plan, X, t, E, gZ, gXh, Z, dA2, ws)
+    torch.cuda.synchronize()
+    with pytest.raises(mapl.MaplError) as ei:
+        mapl.mapl_check(plan)
+    assert ei.value.name == "MAPL_ERR_BAD_TOKEN"
+    assert torch.equal(dA1, dA2)
+    Wd = synth.widen
+    E0 = np.vstack([Wd(b["E"]), np.zeros((1, w.r))])   # row V: the zero anchor
+    t0 = np.where((tids < 0) | (tids >= w.V), w.V, tids)
+    dA_or = oracle.grad_A_given(Wd(b["X"]), t0, E0, Wd(b["P"]), Wd(to_host(gZ)), Wd(gxh),
+                                Wd(b["X"][:, : w.r]))
+    assert rel_frob(dA1.cpu().numpy(), dA_or) <= TOL_F32

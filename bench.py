@@ -464,20 +464,22 @@ def run_ours(args, ws, rank):
     graph_ms = max_over_ranks(g0.elapsed_time(g1), ws) / (reps * nsets)
     mapl.mapl_check(plan)
 
-    # the device's plain write rate on the same rotating X_hat buffers: a
-    # fill of N x d bf16 (no reads), the floor under decompress, whose
-    # traffic is almost all X_hat writes
-    for k in range(2 * nsets):
-        Xh[k % nsets].fill_(0)
-    torch.cuda.synchronize()
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    nf = 10 * nsets
-    f0.record(stream)
-    for k in range(nf):
-        Xh[k % nsets].fill_(0)
-    f1.record(stream)
-    torch.cuda.synchronize()
-    fill_ms = f0.elapsed_time(f1) / nf
+    # the device's write ceiling on the same rotating X_hat buffers: the
+    # library's store-only probe (no reads) by each of its store paths, the
+    # best taken; decompress's traffic is almost all X_hat writes
+    probe_ms = {}
+    for mode in (0, 1, 2):
+        for k in range(2 * nsets):
+            mapl.mapl_store_probe(Xh[k % nsets], mode, stream)
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nf = 10 * nsets
+        f0.record(stream)
+        for k in range(nf):
+            mapl.mapl_store_probe(Xh[k % nsets], mode, stream)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        probe_ms[mode] = f0.elapsed_time(f1) / nf
 
     # end to end through the public API's host-buffer calls: X and tids from
     # pinned host memory in, the payload out to the host and back, X_hat out
@@ -532,6 +534,8 @@ def run_ours(args, ws, rank):
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     step_bytes = comp_b + dec_b
     value = whole_job_rate(N * K, ws, total_ms)
+    write_ceiling = max(xbytes / (v * 1e-3) / 1e9 for v in probe_ms.values())
+    step_floor_us = (comp_b / (peak * 1e9) + dec_b / (write_ceiling * 1e9)) * 1e6
 
     # backward pass (gradient through the same projector, and dL/dA), timed
     # apart from the forward step: one call each per iteration, CUDA events
@@ -546,6 +550,14 @@ def run_ours(args, ws, rank):
         ("grad_decompress_us", lambda: mapl.mapl_grad_decompress(plan, gZ, gX, stream)),
         ("grad_A_us", lambda: mapl.mapl_grad_A(plan, x0, t, E, gZ, gxh, Zb, dA, gws, stream)),
     ]
+    if w.vq:
+        # MCVQ of the gradient with codebooks of its own (§3.5)
+        mapl.mapl_plan_set_grad_codebooks(plan, to_dev(synth.make_grad_codebooks(w)), stream)
+        gpay = torch.empty(plan.payload_shape(N), dtype=torch.uint8, device="cuda")
+        bw_calls += [
+            ("grad_compress_vq_us", lambda: mapl.mapl_grad_compress_vq(plan, gxh, gpay, stream)),
+            ("grad_decompress_vq_us", lambda: mapl.mapl_grad_decompress_vq(plan, gpay, gX, stream)),
+        ]
     backward = {}
     for key, fn in bw_calls:
         for _ in range(5):
@@ -635,6 +647,31 @@ def run_ours(args, ws, rank):
                     "step with the projector broadcast to 3 bf16 plans, separate vs fused")
     mapl.mapl_check(plan)
 
+    # streaming codebook sync (§3.5, App. F): each micro-batch overwrites the
+    # same seeded subset of codes on both ends; one fifth of the R x G x K
+    # codes per micro-batch (Table 8), timed per mapl_plan_update_codes call
+    stream_sync = {}
+    if w.vq:
+        total = w.R * w.G * w.K
+        per = max(1, total // 5)
+        ids_h = mapl.mapl_stream_subset(total, per, 1234, 0)
+        cnt = int(ids_h.size)
+        ids_d = torch.from_numpy(ids_h).cuda()
+        codes_d = to_dev(np.ascontiguousarray(b["C"].reshape(total, w.gd)[ids_h]))
+        for _ in range(3):
+            mapl.mapl_plan_update_codes(plan, ids_d, codes_d, stream)
+        torch.cuda.synchronize()
+        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        u0.record(stream)
+        for _ in range(50):
+            mapl.mapl_plan_update_codes(plan, ids_d, codes_d, stream)
+        u1.record(stream)
+        torch.cuda.synchronize()
+        mapl.mapl_check(plan)
+        stream_sync = {"plan_update_codes_us": u0.elapsed_time(u1) / 50 * 1e3, "codes_per_call": cnt,
+                       "note": "one fifth of the R x G x K codes per micro-batch (the same "
+                               "values written back, so the plan is unchanged)"}
+
     # first-boundary anchor (the full token embedding E_emb, V x d): the same
     # workload with X = E_emb[tids] + signal, compress and decompress timed
     # apart with CUDA events over rotating buffer sets
@@ -703,12 +740,21 @@ def run_ours(args, ws, rank):
         "kernels": {"mapl_compress_us": comp_avg * 1e3, "mapl_decompress_us": dec_avg * 1e3,
                     "step_GBps": step_bytes / (total_ms / K * 1e-3) / 1e9,
                     "unique_token_rows": U,
-                    "x_hat_fill_us": fill_ms * 1e3,
-                    "x_hat_fill_GBps": N * w.d * 2 / (fill_ms * 1e-3) / 1e9,
-                    "decompress_vs_fill": fill_ms / dec_avg,
-                    "fill_note": "torch fill_ of the same rotating X_hat buffers (writes "
-                                 "only), timed after the step loop: the device's plain write "
-                                 "rate, the floor under decompress"},
+                    "write_probe_GBps": {k: xbytes / (v * 1e-3) / 1e9 for k, v in
+                                         (("st_v4", probe_ms[0]), ("st_cs_v4", probe_ms[1]),
+                                          ("bulk_copy", probe_ms[2]))},
+                    "write_ceiling_GBps": write_ceiling,
+                    "decompress_GBps": dec_b / (dec_avg * 1e-3) / 1e9,
+                    "decompress_frac_write_ceiling": dec_b / (dec_avg * 1e-3) / 1e9 / write_ceiling,
+                    "decompress_frac_copy_peak": dec_b / (dec_avg * 1e-3) / 1e9 / peak,
+                    "step_floor_us": step_floor_us,
+                    "step_frac_of_floor": step_floor_us / (total_ms / K * 1e3),
+                    "write_note": "mapl_store_probe (the library's store-only kernels: "
+                                  "16-byte stores, streaming stores, bulk async copies) over "
+                                  "the same rotating X_hat buffers, timed after the step loop; "
+                                  "the best is the write ceiling.  step_floor_us: compress's "
+                                  "bytes at the HBM copy peak plus decompress's at the write "
+                                  "ceiling"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "algorithmic_bytes_per_launch": dom_bytes,
@@ -721,10 +767,12 @@ def run_ours(args, ws, rank):
                                           + pay_h[0].numel() * pay_h[0].element_size()),
                 "api": "mapl_compress_host + mapl_decompress_host, steps rotating "
                        "over six streams"},
-        "backward": dict(backward, note="gZ = dL/dX_hat A, dL/dX = gZ A^T, dL/dA; same "
-                         "workload, 200 calls each, inputs L2-warm"),
+        "backward": dict(backward, note="gZ = dL/dX_hat A, dL/dX = gZ A^T, dL/dA; the "
+                         "_vq calls quantise gZ with gradient codebooks (indices out, decoded "
+                         "in); same workload, 200 calls each, inputs L2-warm"),
         "spel": spel,
         "first_boundary": first,
+        "codebook_stream": stream_sync,
         "workloads": workloads,
         "cuda_graph": {"value": whole_job_rate(N, ws, graph_ms), "unit": UNIT,
                        "ms_per_step": graph_ms, "steps": reps * nsets,

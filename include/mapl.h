@@ -165,9 +165,12 @@ mapl_status mapl_decompress(mapl_plan plan, const void* payload, const int32_t* 
  *   (per_batch, or fewer for the last block of an epoch) to `ids`.  Both ends
  *   compute the same subset, so only the code values need to travel.
  * mapl_plan_update_codes: codes ids[i] (device int32) take the values
- *   codes[i * gd .. +gd) (device, plan dtype); their ||c||^2 and every book's
+ *   codes[i * gd .. +gd) (device, plan dtype, 16-byte aligned); their ||c||^2 and every book's
  *   max ||c|| are refreshed.  An id outside [0, R*G*K) sets the error word
- *   (mapl_check reports MAPL_ERR_INVALID_ARG) and is skipped.  Async.
+ *   (mapl_check reports MAPL_ERR_INVALID_ARG) and is skipped.  One launch
+ *   (its last block recomputes the maxima through a counter the plan keeps),
+ *   so calls on the same plan must not overlap on the GPU, as with every
+ *   call that writes the plan.  Async.
  */
 mapl_status mapl_stream_subset(int64_t total, int64_t per_batch, uint64_t seed, int64_t step,
                                int32_t* ids, int32_t* count);
@@ -213,6 +216,31 @@ mapl_status mapl_grad_decompress(mapl_plan plan, const void* gZ, int64_t N, void
                                  cudaStream_t stream);
 
 mapl_status mapl_grad_workspace_size(mapl_plan plan, int64_t N, size_t* bytes);
+
+/*
+ * MCVQ of backward gradients (MAPL §3.5: the multi-codebook quantiser
+ * compresses both forward activations and backward gradients).  The
+ * gradient has a distribution of its own, so it gets codebooks of its own:
+ *   mapl_plan_set_grad_codebooks  R x G x K x gd bf16 codebooks (device,
+ *     16-byte aligned), copied into the plan with their squared norms and
+ *     per-book maxima; a later call replaces them.  The first call allocates
+ *     their plan storage (R*G*K*(2 gd + 4) bytes).
+ *   mapl_grad_compress_vq    gZ = dL/dX_hat A (no anchor term), quantised
+ *     round by round with the gradient codebooks exactly as mapl_compress
+ *     quantises Z (same kernel, same exact-nearest-code rule): payload
+ *     N x (R*G) uint8, round-major then group.
+ *   mapl_grad_decompress_vq  dL/dX = gZ_hat A^T, gZ_hat the sum over rounds of
+ *     the payload's codes in the gradient codebooks; N x d bf16.
+ * bf16 VQ plans only (UNSUPPORTED otherwise); the two codec calls return
+ * INVALID_ARG until mapl_plan_set_grad_codebooks has been called.  Async.
+ */
+mapl_status mapl_plan_set_grad_codebooks(mapl_plan plan, const void* codebooks, cudaStream_t stream);
+
+mapl_status mapl_grad_compress_vq(mapl_plan plan, const void* gX_hat, int64_t N, void* payload,
+                                  cudaStream_t stream);
+
+mapl_status mapl_grad_decompress_vq(mapl_plan plan, const void* payload, int64_t N, void* gX,
+                                    cudaStream_t stream);
 
 mapl_status mapl_grad_A(mapl_plan plan, const void* X, const int32_t* tids, const void* E_send,
                         const void* gZ, const void* gX_hat, const void* Z, int64_t N,
@@ -268,6 +296,19 @@ mapl_status mapl_check(mapl_plan plan, cudaStream_t stream);
  */
 mapl_status mapl_selftest_bounded_wait(mapl_plan plan, int64_t budget_ns, int64_t* waited_ns,
                                        cudaStream_t stream);
+
+/*
+ * Device write-rate probe (measurement only, no plan): writes `bytes` zero
+ * bytes over `dst` (device, 16-byte aligned; bytes a multiple of 16) with
+ * nothing read.  mode 0: 16-byte st.global from a grid-stride loop of four
+ * 512-thread CTAs per SM; mode 1: the same with the streaming (evict-first)
+ * hint; mode 2: bulk asynchronous copies (cp.async.bulk, the copy path of
+ * the decompress kernel's TMA-store drain) of a zeroed 32 KB shared-memory
+ * buffer, one CTA per SM over a contiguous range.  Timed on decompress's
+ * own output buffers it gives the write ceiling decompress is held to.
+ * Errors: INVALID_ARG, CUDA.
+ */
+mapl_status mapl_store_probe(void* dst, size_t bytes, int32_t mode, cudaStream_t stream);
 
 void mapl_plan_destroy(mapl_plan plan);
 

@@ -21,7 +21,9 @@ __all__ = [
     "mapl_compress_z32", "mapl_decompress", "mapl_check", "mapl_plan_destroy",
     "mapl_host_workspace_size", "mapl_compress_host", "mapl_decompress_host",
     "mapl_grad_compress", "mapl_grad_decompress", "mapl_grad_workspace_size", "mapl_grad_A",
+    "mapl_plan_set_grad_codebooks", "mapl_grad_compress_vq", "mapl_grad_decompress_vq",
     "mapl_stream_subset", "mapl_plan_update_codes", "mapl_selftest_bounded_wait",
+    "mapl_store_probe",
     "mapl_spel_workspace_size", "mapl_spel_step", "mapl_spel_step_refresh",
     "mapl_spel_step_static", "mapl_last_error",
     "mapl_version",
@@ -78,10 +80,14 @@ def load_library():
         "mapl_decompress": [P, P, P, I64, P, P, P],
         "mapl_check": [P, P],
         "mapl_selftest_bounded_wait": [P, I64, ctypes.POINTER(I64), P],
+        "mapl_store_probe": [P, SZ, I32, P],
         "mapl_host_workspace_size": [P, I64, ctypes.POINTER(SZ)],
         "mapl_grad_compress": [P, P, I64, P, P],
         "mapl_grad_decompress": [P, P, I64, P, P],
         "mapl_grad_workspace_size": [P, I64, ctypes.POINTER(SZ)],
+        "mapl_plan_set_grad_codebooks": [P, P, P],
+        "mapl_grad_compress_vq": [P, P, I64, P, P],
+        "mapl_grad_decompress_vq": [P, P, I64, P, P],
         "mapl_grad_A": [P, P, P, P, P, P, P, I64, P, P, SZ, P],
         "mapl_stream_subset": [I64, I64, ctypes.c_uint64, I64, P, ctypes.POINTER(I32)],
         "mapl_plan_update_codes": [P, P, I32, P, P],
@@ -299,6 +305,33 @@ def mapl_grad_decompress(plan: Plan, gZ, gX, stream=None):
     return gX
 
 
+def mapl_plan_set_grad_codebooks(plan: Plan, codebooks, stream=None):
+    """Gradient codebooks (R x G x K x gd bf16 device tensor) for the MCVQ of
+    backward gradients."""
+    import torch
+    _check(load_library().mapl_plan_set_grad_codebooks(
+        plan.handle, _ptr(codebooks, torch.bfloat16, "codebooks"), _stream(stream)))
+
+
+def mapl_grad_compress_vq(plan: Plan, gX_hat, payload, stream=None):
+    """payload (N x R*G uint8) = the gradient codebooks' RVQ of gZ = gX_hat A."""
+    import torch
+    _check(load_library().mapl_grad_compress_vq(
+        plan.handle, _ptr(gX_hat, torch.bfloat16, "gX_hat"), int(gX_hat.shape[0]),
+        _ptr(payload, torch.uint8, "payload"), _stream(stream)))
+    return payload
+
+
+def mapl_grad_decompress_vq(plan: Plan, payload, gX, stream=None):
+    """gX (N x d bf16) = gZ_hat A^T, gZ_hat decoded from the payload with the
+    gradient codebooks."""
+    import torch
+    _check(load_library().mapl_grad_decompress_vq(
+        plan.handle, _ptr(payload, torch.uint8, "payload"), int(payload.shape[0]),
+        _ptr(gX, torch.bfloat16, "gX"), _stream(stream)))
+    return gX
+
+
 def mapl_grad_workspace_size(plan: Plan, N: int) -> int:
     """Bytes of device workspace mapl_grad_A needs for N tokens."""
     n = ctypes.c_size_t(0)
@@ -345,6 +378,14 @@ def mapl_plan_update_codes(plan: Plan, ids, codes, stream=None):
 def mapl_check(plan: Plan, stream=None):
     """Synchronise and raise MaplError if a kernel flagged a data error."""
     _check(load_library().mapl_check(plan.handle, _stream(stream)))
+
+
+def mapl_store_probe(dst, mode: int = 0, stream=None) -> None:
+    """Write zeros over the device tensor `dst` (no reads) by store path
+    `mode` (0: 16-byte stores, 1: streaming stores, 2: bulk async copies):
+    the write-rate probe."""
+    _check(load_library().mapl_store_probe(_ptr(dst), dst.numel() * dst.element_size(),
+                                           int(mode), _stream(stream)))
 
 
 def mapl_selftest_bounded_wait(plan: Plan, budget_ns: int, stream=None) -> int:

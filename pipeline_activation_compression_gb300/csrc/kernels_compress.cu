@@ -782,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           epilogue_vq<GD>(a, geo, ctl, tbase, ubase, cn_s, base + nst * sb, cbsb, tile, zb, q,
                           h, lane, dcnt, pcnt, suse, alive);
         const int n = tile * kTile + q * 32 + lane;
-        if (alive && h == 0 && n < a.N) {
+        if (alive && h == 0 && n < a.N && a.anchor) {   // no token ids without the anchor
           const int t = a.tids[n];
           if (t < 0 || t >= a.V) atomicOr(a.err, kErrBadToken);
         }

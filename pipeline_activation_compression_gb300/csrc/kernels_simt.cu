@@ -161,12 +161,20 @@ __global__ void k_prep_codes(const void* C, int nbooks, int K, int gd, bool bf,
   cnorm[idx] = static_cast<float>(s);
 }
 
+// max_k ||c_k|| of each book, rounded up: one warp per book (the maximum of
+// the fp32 norms is exact in any order; the square root is taken in fp64).
+__device__ __forceinline__ void book_max_warp(const float* cnorm, int b, int K, int lane,
+                                              float* cmax) {
+  float m = 0.f;
+  for (int k = lane; k < K; k += 32) m = fmaxf(m, __ldcg(cnorm + static_cast<size_t>(b) * K + k));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) cmax[b] = static_cast<float>(sqrt(static_cast<double>(m)) * (1.0 + 1e-6));
+}
+
 __global__ void k_prep_cmax(const float* cnorm, int nbooks, int K, float* cmax) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= nbooks) return;
-  double m = 0.0;
-  for (int k = 0; k < K; ++k) m = fmax(m, static_cast<double>(cnorm[static_cast<size_t>(b) * K + k]));
-  cmax[b] = static_cast<float>(sqrt(m) * (1.0 + 1e-6));
+  const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (b < nbooks) book_max_warp(cnorm, b, K, threadIdx.x & 31, cmax);
 }
 
 inline unsigned blocks_for(size_t n, int t) { return static_cast<unsigned>((n + t - 1) / t); }
@@ -297,8 +305,19 @@ cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps
     const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G);
     k_prep_codes<<<blocks_for(static_cast<size_t>(nb) * c.K, T), T, 0, s>>>(
         C, nb, c.K, gd, true, p.Cb, nullptr, p.cnorm);
-    k_prep_cmax<<<blocks_for(nb, 64), 64, 0, s>>>(p.cnorm, nb, c.K, p.cmax);
+    k_prep_cmax<<<blocks_for(static_cast<size_t>(nb) * 32, 256), 256, 0, s>>>(p.cnorm, nb, c.K, p.cmax);
   }
+  return cudaGetLastError();
+}
+
+// A bf16 codebook set (R x G x K x gd) copied into plan storage with its
+// squared norms and per-book maxima (the gradient codebooks of §3.5).
+cudaError_t launch_prep_books_bf16(const mapl_config& c, const void* C, __nv_bfloat16* Cb,
+                                   float* cnorm, float* cmax, cudaStream_t s) {
+  const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G);
+  k_prep_codes<<<blocks_for(static_cast<size_t>(nb) * c.K, 256), 256, 0, s>>>(C, nb, c.K, gd, true,
+                                                                              Cb, nullptr, cnorm);
+  k_prep_cmax<<<blocks_for(static_cast<size_t>(nb) * 32, 256), 256, 0, s>>>(cnorm, nb, c.K, cmax);
   return cudaGetLastError();
 }
 
@@ -307,36 +326,81 @@ cudaError_t launch_split_negMt(const float* M, int r, __nv_bfloat16* Mts, cudaSt
   return cudaGetLastError();
 }
 
-// Streaming codebook update (§3.5, App. F): code ids[i] (flat over R x G x
-// K) takes the values codes[i] (gd entries, plan dtype); its squared norm is
-// recomputed.  One thread per updated code; ids outside the table set the
-// error word and are skipped.
-__global__ void k_update_codes(const int32_t* ids, int count, const void* codes, int gd,
-                               int ncode, bool bf, __nv_bfloat16* Cb, float* C32, float* cnorm,
-                               int* err) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= count) return;
-  const int id = ids[i];
+// One updated code: its values are read first (16-byte loads for bf16 rows
+// of 16 or 32 values, all in flight together), then written to the plan's
+// table, and ||c||^2 is formed from the registers in fp64.
+__device__ __forceinline__ void update_one_code(int id, int i, const void* __restrict__ codes,
+                                                int gd, int ncode, bool bf,
+                                                __nv_bfloat16* __restrict__ Cb,
+                                                float* __restrict__ C32, float* __restrict__ cnorm,
+                                                int* err) {
   if (id < 0 || id >= ncode) {
     atomicOr(err, kErrBadIndex);
     return;
   }
   double s = 0.0;
-  for (int j = 0; j < gd; ++j) {
-    const size_t src = static_cast<size_t>(i) * gd + j, dst = static_cast<size_t>(id) * gd + j;
-    if (bf) {
-      const __nv_bfloat16 v = reinterpret_cast<const __nv_bfloat16*>(codes)[src];
-      Cb[dst] = v;
-      const double x = static_cast<double>(__bfloat162float(v));
-      s = fma(x, x, s);
-    } else {
-      const float v = reinterpret_cast<const float*>(codes)[src];
-      C32[dst] = v;
-      s = fma(static_cast<double>(v), static_cast<double>(v), s);
+  if (bf && (gd == 16 || gd == 32)) {
+    const uint4* src = reinterpret_cast<const uint4*>(codes) + static_cast<size_t>(i) * (gd / 8);
+    uint4* dst = reinterpret_cast<uint4*>(Cb) + static_cast<size_t>(id) * (gd / 8);
+    uint4 w[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (c < gd / 8) w[c] = __ldg(src + c);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (c < gd / 8) {
+        dst[c] = w[c];
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w[c]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(h[e]);
+          s = fma(static_cast<double>(f.x), static_cast<double>(f.x), s);
+          s = fma(static_cast<double>(f.y), static_cast<double>(f.y), s);
+        }
+      }
+  } else {
+    for (int j = 0; j < gd; ++j) {
+      const size_t src = static_cast<size_t>(i) * gd + j, dst = static_cast<size_t>(id) * gd + j;
+      if (bf) {
+        const __nv_bfloat16 v = reinterpret_cast<const __nv_bfloat16*>(codes)[src];
+        Cb[dst] = v;
+        const double x = static_cast<double>(__bfloat162float(v));
+        s = fma(x, x, s);
+      } else {
+        const float v = reinterpret_cast<const float*>(codes)[src];
+        C32[dst] = v;
+        s = fma(static_cast<double>(v), static_cast<double>(v), s);
+      }
     }
   }
   cnorm[id] = static_cast<float>(s);
 }
+
+// Streaming codebook update (§3.5, App. F): code ids[i] (flat over R x G x
+// K) takes the values codes[i] (gd entries, plan dtype); its squared norm is
+// recomputed.  One thread per updated code; ids outside the table set the
+// error word and are skipped.  The last block to finish (a counter in the
+// plan, left at zero) recomputes every book's max ||c||, one warp per book,
+// so an update is one launch.
+__global__ void __launch_bounds__(128) k_update_codes(const int32_t* ids, int count,
+                                                      const void* codes, int gd, int ncode,
+                                                      bool bf, __nv_bfloat16* Cb, float* C32,
+                                                      float* cnorm, int* err, int nbooks, int K,
+                                                      float* cmax, unsigned int* ctr) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < count) update_one_code(ids[i], i, codes, gd, ncode, bf, Cb, C32, cnorm, err);
+  __shared__ bool last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(ctr, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int b = threadIdx.x >> 5; b < nbooks; b += blockDim.x >> 5)
+    book_max_warp(cnorm, b, K, threadIdx.x & 31, cmax);
+  if (threadIdx.x == 0) *ctr = 0u;
+}
+
 
 // Self-test of the bounded wait every kernel uses: one warp waits on an
 // mbarrier that nothing arrives on, through the same mbar_wait, and reports
@@ -371,8 +435,7 @@ cudaError_t launch_update_codes(const mapl_config& c, const int32_t* ids, int co
   const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G), ncode = nb * c.K;
   const bool bf = c.dtype == MAPL_BF16;
   k_update_codes<<<blocks_for(static_cast<size_t>(count), 128), 128, 0, s>>>(
-      ids, count, codes, gd, ncode, bf, p.Cb, p.C32, p.cnorm, p.err);
-  k_prep_cmax<<<blocks_for(nb, 64), 64, 0, s>>>(p.cnorm, nb, c.K, p.cmax);
+      ids, count, codes, gd, ncode, bf, p.Cb, p.C32, p.cnorm, p.err, nb, c.K, p.cmax, p.upd_ctr);
   return cudaGetLastError();
 }
 
@@ -390,7 +453,7 @@ cudaError_t launch_prep_f32(const mapl_config& c, const void* A, const void* Ps,
       const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G);
       k_prep_codes<<<blocks_for(static_cast<size_t>(nb) * c.K, T), T, 0, s>>>(
           C, nb, c.K, gd, false, nullptr, p.C32, p.cnorm);
-      k_prep_cmax<<<blocks_for(nb, 64), 64, 0, s>>>(p.cnorm, nb, c.K, p.cmax);
+      k_prep_cmax<<<blocks_for(static_cast<size_t>(nb) * 32, 256), 256, 0, s>>>(p.cnorm, nb, c.K, p.cmax);
     }
   }
   return cudaGetLastError();
@@ -419,6 +482,67 @@ cudaError_t launch_decompress_f32(const mapl_config& c, const PlanDevice& p, con
   k_decompress_f32<<<grid, kWarpsPerBlock * 32, smem, s>>>(
       in, tids, p.At32, p.Pr32, E, p.C32, Xh, p.err, static_cast<int>(N), static_cast<int>(c.d),
       r, static_cast<int>(c.V), c.G, c.R, c.K, gd, c.G > 0 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+// Write-rate probe: zeros over [dst, dst + 16 n16) with nothing read.
+// Modes 0/1: 16-byte stores from a grid-stride loop, four stores in flight
+// per thread (1: the streaming, evict-first hint).  Mode 2: bulk
+// asynchronous copies of a zeroed 32 KB shared-memory buffer, one CTA per
+// SM over a contiguous range, the copy path of the TMA store drain.
+namespace {
+
+template <bool kStream>
+__global__ void __launch_bounds__(512) k_store_probe(uint4* __restrict__ dst, size_t n16) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (kStream) __stcs(dst + i + k * stride, z);
+      else dst[i + k * stride] = z;
+    }
+  }
+  for (; i < n16; i += stride) {
+    if (kStream) __stcs(dst + i, z);
+    else dst[i] = z;
+  }
+}
+
+constexpr uint32_t kBulkBytes = 32768;
+
+__global__ void __launch_bounds__(128) k_store_probe_bulk(uint8_t* __restrict__ dst, size_t n16) {
+  __shared__ __align__(128) uint4 buf[kBulkBytes / 16];
+  for (int i = threadIdx.x; i < static_cast<int>(kBulkBytes / 16); i += blockDim.x)
+    buf[i] = make_uint4(0u, 0u, 0u, 0u);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  const size_t b0 = n16 * blockIdx.x / gridDim.x * 16, b1 = n16 * (blockIdx.x + 1) / gridDim.x * 16;
+  const uint32_t src = static_cast<uint32_t>(__cvta_generic_to_shared(buf));
+  for (size_t o = b0; o < b1; o += kBulkBytes) {
+    const uint32_t n = b1 - o < kBulkBytes ? static_cast<uint32_t>(b1 - o) : kBulkBytes;
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst + o),
+                 "r"(src), "r"(n)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 8;" ::: "memory");
+  }
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+}  // namespace
+
+cudaError_t launch_store_probe(void* dst, size_t bytes, int mode, int num_sms, cudaStream_t s) {
+  const size_t n16 = bytes / 16;
+  if (mode == 2) {
+    k_store_probe_bulk<<<num_sms, 128, 0, s>>>(static_cast<uint8_t*>(dst), n16);
+  } else if (mode == 1) {
+    k_store_probe<true><<<4 * num_sms, 512, 0, s>>>(static_cast<uint4*>(dst), n16);
+  } else {
+    k_store_probe<false><<<4 * num_sms, 512, 0, s>>>(static_cast<uint4*>(dst), n16);
+  }
   return cudaGetLastError();
 }
 

@@ -48,6 +48,13 @@ struct mapl_plan_s {
   float* emb_T = nullptr;
   __nv_bfloat16* emb_tab = nullptr;
   CUtensorMap tmMt_emb{};
+  // gradient codebooks (MCVQ of backward gradients): [Cb R x G x K x gd bf16
+  // | cnorm | cmax] in one allocation, and their tensor map
+  void* gpool = nullptr;
+  __nv_bfloat16* Cb_g = nullptr;
+  float* cnorm_g = nullptr;
+  float* cmax_g = nullptr;
+  CUtensorMap tmC_g{};
 };
 
 namespace {
@@ -355,7 +362,7 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   }
   const size_t ocn = take((ncode > 0 ? ncode : 1) * 4);
   const size_t ocm = take((nb > 0 ? nb : 1) * 4);
-  const size_t oerr = take(4);
+  const size_t oerr = take(8);   // the error word, then the codebook-update counter
   void* pool = nullptr;
   e = cudaMalloc(&pool, off);
   if (e != cudaSuccess) {
@@ -383,8 +390,9 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   p.cnorm = reinterpret_cast<float*>(b + ocn);
   p.cmax = reinterpret_cast<float*>(b + ocm);
   p.err = reinterpret_cast<int*>(b + oerr);
+  p.upd_ctr = reinterpret_cast<unsigned int*>(b + oerr + 4);
 
-  e = cudaMemsetAsync(p.err, 0, 4, stream);
+  e = cudaMemsetAsync(p.err, 0, 8, stream);   // the error word and the update counter
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(p.Ps, P_send, d * r * elt_size(*cfg), cudaMemcpyDeviceToDevice, stream);
   if (e == cudaSuccess)
@@ -536,6 +544,8 @@ mapl_status mapl_plan_update_codes(mapl_plan pl, const int32_t* ids, int32_t cou
   if (count < 0) return fail(MAPL_ERR_INVALID_ARG, "count must be >= 0");
   if (count == 0) return MAPL_OK;
   if (!ids || !codes) return fail(MAPL_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(codes) || (reinterpret_cast<uintptr_t>(ids) & 3u))
+    return fail(MAPL_ERR_INVALID_ARG, "codes must be 16-byte aligned (ids 4-byte)");
   mapl_status st = check_device(pl);
   if (st != MAPL_OK) return st;
   cudaError_t e = launch_update_codes(pl->cfg, ids, count, codes, pl->p, stream);
@@ -586,13 +596,16 @@ void mapl_plan_destroy(mapl_plan pl) {
   if (!pl) return;
   if (pl->blas) cublasDestroy(pl->blas);
   if (pl->emb_pool) cudaFree(pl->emb_pool);
+  if (pl->gpool) cudaFree(pl->gpool);
   if (pl->p.pool) cudaFree(pl->p.pool);
   delete pl;
 }
 
+// grad_books: quantise with the plan's gradient codebooks (MCVQ of the
+// backward gradient) instead of the forward ones.
 static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* tids, int64_t N,
                                    const void* E, void* out, int mode, cudaStream_t stream,
-                                   bool anchor = true) {
+                                   bool anchor = true, bool grad_books = false) {
   if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
   const bool own_table = pl->E_emb != nullptr;   // E_send is not read
   if (!X || !out || (anchor && (!tids || (!E && !own_table))))
@@ -629,9 +642,9 @@ static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* t
   a.E = reinterpret_cast<const __nv_bfloat16*>(E);
   a.re = pl->re;
   a.nsplit = pl->nsplit;
-  a.Cb = pl->p.Cb;
-  a.cnorm = pl->p.cnorm;
-  a.cmax = pl->p.cmax;
+  a.Cb = grad_books ? pl->Cb_g : pl->p.Cb;
+  a.cnorm = grad_books ? pl->cnorm_g : pl->p.cnorm;
+  a.cmax = grad_books ? pl->cmax_g : pl->p.cmax;
   a.out = out;
   a.err = pl->p.err;
   a.N = static_cast<int>(N);
@@ -657,15 +670,15 @@ static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* t
     a.cstage_bytes = pl->p_cstage;
     const int64_t want = (N + 63) / 64;
     const int grid = static_cast<int>(want < pl->num_sms ? want : pl->num_sms);
-    e = launch_compress_pipe(tmX, pl->tmAt, emb ? pl->tmMt_emb : pl->tmMt, pl->tmC, tmE, a,
-                             pl->p_smem, grid, stream);
+    e = launch_compress_pipe(tmX, pl->tmAt, emb ? pl->tmMt_emb : pl->tmMt,
+                             grad_books ? pl->tmC_g : pl->tmC, tmE, a, pl->p_smem, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "compress launch");
     return MAPL_OK;
   }
   const int ntiles = static_cast<int>((N + kTile - 1) / kTile);
   const int grid = ntiles < pl->num_sms ? ntiles : pl->num_sms;
-  e = launch_compress_tc(tmX, pl->tmAt, emb ? pl->tmMt_emb : pl->tmMt, pl->tmC, tmE, a,
-                         pl->c_smem, grid, stream);
+  e = launch_compress_tc(tmX, pl->tmAt, emb ? pl->tmMt_emb : pl->tmMt,
+                         grad_books ? pl->tmC_g : pl->tmC, tmE, a, pl->c_smem, grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "compress launch");
   return MAPL_OK;
 }
@@ -682,11 +695,12 @@ mapl_status mapl_compress_z32(mapl_plan pl, const void* X, const int32_t* tids, 
   return compress_common(pl, X, tids, N, E_send, Z, kModeZ32, stream);
 }
 
-// anchor == false: the payload is a bf16 N x r tensor (never VQ indices) and
-// the E' term is left out (backward pass, dX = gZ A^T).
+// anchor == false: the E' term is left out (backward pass, dX = gZ A^T) and
+// the payload is a bf16 N x r tensor, or (grad_books) VQ indices into the
+// plan's gradient codebooks.
 static mapl_status decompress_common(mapl_plan pl, const void* payload, const int32_t* tids,
                                      int64_t N, const void* E_recv, void* X_hat,
-                                     cudaStream_t stream, bool anchor) {
+                                     cudaStream_t stream, bool anchor, bool grad_books = false) {
   if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
   // first-boundary anchor: X_hat = Z_hat A^T + E_emb[tids], E_recv not read
   const bool emb = anchor && pl->E_emb != nullptr;
@@ -702,7 +716,7 @@ static mapl_status decompress_common(mapl_plan pl, const void* payload, const in
   cudaError_t e;
   if (!anchor && !pl->tc)
     return fail(MAPL_ERR_UNSUPPORTED, "gradient calls need a bf16 (tensor-core) plan");
-  const bool vq = anchor && pl->vq;
+  const bool vq = anchor ? pl->vq : grad_books;
   if (!pl->tc) {
     e = launch_decompress_f32(c, pl->p, payload, tids, N, reinterpret_cast<const float*>(E_recv),
                               reinterpret_cast<float*>(X_hat), stream);
@@ -719,7 +733,7 @@ static mapl_status decompress_common(mapl_plan pl, const void* payload, const in
   DecompressArgs a{};
   a.tids = tids;
   a.E = reinterpret_cast<const __nv_bfloat16*>(E_recv);
-  a.Cb = pl->p.Cb;
+  a.Cb = grad_books ? pl->Cb_g : pl->p.Cb;
   a.idx = vq ? reinterpret_cast<const uint8_t*>(payload) : nullptr;
   a.Xh = reinterpret_cast<__nv_bfloat16*>(X_hat);
   a.err = pl->p.err;
@@ -773,6 +787,53 @@ mapl_status mapl_grad_compress(mapl_plan pl, const void* gX_hat, int64_t N, void
 mapl_status mapl_grad_decompress(mapl_plan pl, const void* gZ, int64_t N, void* gX,
                                  cudaStream_t stream) {
   return decompress_common(pl, gZ, nullptr, N, nullptr, gX, stream, false);
+}
+
+mapl_status mapl_plan_set_grad_codebooks(mapl_plan pl, const void* codebooks, cudaStream_t stream) {
+  if (!pl || !codebooks) return fail(MAPL_ERR_INVALID_ARG, "NULL argument");
+  if (!pl->vq || !pl->tc)
+    return fail(MAPL_ERR_UNSUPPORTED, "gradient codebooks need a bf16 VQ plan");
+  if (!aligned16(codebooks)) return fail(MAPL_ERR_INVALID_ARG, "codebooks must be 16-byte aligned");
+  mapl_status st = check_device(pl);
+  if (st != MAPL_OK) return st;
+  const mapl_config& c = pl->cfg;
+  const size_t nb = static_cast<size_t>(c.R) * c.G, ncode = nb * c.K;
+  const size_t ocn = up256(ncode * pl->gd * sizeof(__nv_bfloat16));
+  const size_t ocm = ocn + up256(ncode * sizeof(float));
+  if (!pl->gpool) {
+    cudaError_t e = cudaMalloc(&pl->gpool, ocm + up256(nb * sizeof(float)));
+    if (e != cudaSuccess) {
+      pl->gpool = nullptr;
+      return cuda_fail(e, "cudaMalloc(gradient codebooks)");
+    }
+    char* b = static_cast<char*>(pl->gpool);
+    pl->Cb_g = reinterpret_cast<__nv_bfloat16*>(b);
+    pl->cnorm_g = reinterpret_cast<float*>(b + ocn);
+    pl->cmax_g = reinterpret_cast<float*>(b + ocm);
+    const CUtensorMapSwizzle swz =
+        pl->gd == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    if (!make_tmap(&pl->tmC_g, pl->Cb_g, static_cast<uint64_t>(pl->gd), ncode,
+                   static_cast<uint32_t>(pl->gd), static_cast<uint32_t>(c.K), swz))
+      return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (gradient codebooks)");
+  }
+  const cudaError_t e = launch_prep_books_bf16(c, codebooks, pl->Cb_g, pl->cnorm_g, pl->cmax_g,
+                                               stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gradient codebook prep");
+  return MAPL_OK;
+}
+
+mapl_status mapl_grad_compress_vq(mapl_plan pl, const void* gX_hat, int64_t N, void* payload,
+                                  cudaStream_t stream) {
+  if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
+  if (!pl->gpool) return fail(MAPL_ERR_INVALID_ARG, "no gradient codebooks (mapl_plan_set_grad_codebooks)");
+  return compress_common(pl, gX_hat, nullptr, N, nullptr, payload, kModeVQ, stream, false, true);
+}
+
+mapl_status mapl_grad_decompress_vq(mapl_plan pl, const void* payload, int64_t N, void* gX,
+                                    cudaStream_t stream) {
+  if (!pl) return fail(MAPL_ERR_INVALID_ARG, "plan is NULL");
+  if (!pl->gpool) return fail(MAPL_ERR_INVALID_ARG, "no gradient codebooks (mapl_plan_set_grad_codebooks)");
+  return decompress_common(pl, payload, nullptr, N, nullptr, gX, stream, false, true);
 }
 
 namespace {
@@ -986,6 +1047,20 @@ mapl_status mapl_decompress_host(mapl_plan pl, const void* payload, const int32_
   e = cudaMemcpyAsync(X_hat, w + h.x, static_cast<size_t>(N) * c.d * elt_size(c),
                       cudaMemcpyDeviceToHost, stream);
   if (e != cudaSuccess) return cuda_fail(e, "device -> host copy");
+  return MAPL_OK;
+}
+
+mapl_status mapl_store_probe(void* dst, size_t bytes, int32_t mode, cudaStream_t stream) {
+  if (!dst) return fail(MAPL_ERR_INVALID_ARG, "dst is NULL");
+  if (!aligned16(dst) || bytes % 16 != 0)
+    return fail(MAPL_ERR_INVALID_ARG, "dst must be 16-byte aligned and bytes a multiple of 16");
+  if (mode < 0 || mode > 2) return fail(MAPL_ERR_INVALID_ARG, "mode must be 0, 1 or 2");
+  if (bytes == 0) return MAPL_OK;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = launch_store_probe(dst, bytes, mode, sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "store probe");
   return MAPL_OK;
 }
 

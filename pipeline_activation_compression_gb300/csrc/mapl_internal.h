@@ -41,6 +41,7 @@ struct PlanDevice {
   float* cnorm = nullptr;           // R x G x K  ||c||^2 (fp32 of the exact value)
   float* cmax = nullptr;            // R x G      max_k ||c_k|| (rounded up)
   int* err = nullptr;               // device error word (bits kErrBadToken, kErrTimeout)
+  unsigned int* upd_ctr = nullptr;  // blocks of a codebook update done (0 between calls)
   void* pool = nullptr;             // single allocation holding everything above
 };
 
@@ -102,6 +103,9 @@ cudaError_t launch_prep_f32(const mapl_config& c, const void* A, const void* Ps,
 
 // One warp waits (bounded) on an mbarrier nothing arrives on; sets the
 // timeout bit of `err` when it gives up and writes the time waited.
+cudaError_t launch_store_probe(void* dst, size_t bytes, int mode, int num_sms, cudaStream_t s);
+cudaError_t launch_prep_books_bf16(const mapl_config& c, const void* C, __nv_bfloat16* Cb,
+                                   float* cnorm, float* cmax, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint64_t budget_ns, int* err, unsigned long long* waited,
                                  cudaStream_t s);
 cudaError_t launch_update_codes(const mapl_config& c, const int32_t* ids, int count,

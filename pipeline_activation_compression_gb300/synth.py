@@ -243,6 +243,23 @@ def make_boundary_grad(w: Workload | str, seed: int = 0, n_tokens: int | None = 
     return _store(scale * rng.standard_normal((n, w.d)), w.dtype)
 
 
+def make_grad_codebooks(w: Workload | str, seed: int = 0, scale: float = 0.01) -> np.ndarray:
+    """Codebooks for the MCVQ of backward gradients (R x G x K x gd, storage
+    dtype), from their own seeded stream.  The boundary gradient of
+    ``make_boundary_grad`` has N(0, scale) entries and A has orthonormal
+    columns, so gZ = dL/dX_hat A has N(0, scale) entries too: round 0 codes
+    are N(0, scale), and later rounds shrink by the ratio the forward books
+    of the workload use between their rounds (code_sigma)."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 7, 2]).spawn(1)[0]))
+    C = np.empty((w.R, w.G, w.K, w.gd))
+    for rho in range(w.R):
+        ratio = w.code_sigma[rho] / w.code_sigma[0] if w.code_sigma else 1.0
+        C[rho] = scale * ratio * rng.standard_normal((w.G, w.K, w.gd))
+    return _store(C, w.dtype)
+
+
 def make_first_boundary(w: Workload | str, seed: int = 0, n_tokens: int | None = None,
                         emb_std: float = 1.0) -> dict:
     """Inputs of the first boundary, where the anchor is the full token

@@ -341,46 +341,56 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // ======================================================================
-// decompress, persistent form (resident A operand, r <= 256)
+// decompress, persistent form (A operand in TMEM, r <= 256)
 // ======================================================================
-// One CTA per SM walks the tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+// One CTA per SM walks its own contiguous range of rows in tiles of up to
+// 128 rows.  A tile's A operand [Z_hat | E'[tids]] (128 rows, K = 2r; K = r
+// without the anchor term) lives in TMEM, two bf16 per 32-bit column (the
+// lower K index in the low half), where the builder warps write it, and the
+// tensor cores read it from there ([a-tmem] form).  Shared memory then holds
+// only the [A^T | P'^T] ring, as deep as it fits (the ring is L2-latency
+// bound), and the drain's staging.  TMEM columns: [acc 0 | acc 1 | A 0 |
+// A 1] = NC, NC, K/2, K/2 (one A buffer when two do not fit).
 // Warp roles (320 threads):
 //   warp 0 lane 0 : TMA producer of the [A^T | P'^T] ring (NC x 64 blocks)
 //   warp 1        : TMEM allocation; lane 0 issues every tcgen05.mma
-//   warps 2..5    : builders of the A operand [Z_hat | E'[tids]] of the next
-//                   tile (E' rows by TMA gather4, Z_hat by TMA or VQ decode)
+//   warps 2..5    : builders: warp w writes TMEM lanes 32 (w % 4).. (its
+//                   rows) of the next tile's A: the VQ decode (or the Z_hat
+//                   payload row) and the E' row of the token's id
 //   warps 6..9    : drain of the two TMEM accumulators (TMEM lane = row)
-// The A operand is double buffered when two copies fit in shared memory, so
-// the next tile is built while the current one runs on the tensor cores.
 constexpr int kPtThreads = 320;
-constexpr int kPtBuild0 = 2;      // first builder warp
 constexpr int kPtDrain0 = 6;      // first drain warp
-constexpr int kPtBuildBar = 2;    // named barrier of the builder warps
+constexpr int kPtMaxStages = 12;
 constexpr uint32_t kPtStagingBytes = 4 * 4096;   // per drain warp: 32 rows x 128 B
 
 struct CtlPt {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
-  uint64_t afull[2];      // A operand built (TMA bytes + one builder arrival)
+  uint64_t full[kPtMaxStages];
+  uint64_t empty[kPtMaxStages];
+  uint64_t afull[2];      // A operand written (one arrival per builder warp)
   uint64_t aempty[2];     // MMAs of the tile that used the buffer are complete
   uint64_t tfull[2];      // accumulator holds a finished chunk
   uint64_t tempty[2];     // accumulator drained (one arrival per drain warp)
   uint64_t done;          // every MMA of the CTA has completed
+  uint64_t efull;         // first tile: E' rows written by the drain warps
   uint32_t tmem_base;
   int abort;
-  int32_t ids[2][kTile];  // gather row ids of the tile in A buffer b
 };
 
-// One code row of book (rho, g) for index k, GD bf16 as GD/8 uint4 loads;
-// an index >= K is flagged and replaced by K - 1 (never read past the book).
-template <int GD>
-__device__ __forceinline__ void load_code(const DecompressArgs& a, const uint8_t* ip, int rho,
-                                          int g, uint4 (&w)[GD / 8]) {
+// Code index of (round rho, group g) in a VQ payload row; an index >= K is
+// flagged and replaced by K - 1 (never read past the book).
+__device__ __forceinline__ int code_index(const DecompressArgs& a, const uint8_t* ip, int rho,
+                                          int g) {
   int k = ip[rho * a.G + g];
   if (k >= a.K) {
     atomicOr(a.err, kErrBadIndex);
     k = a.K - 1;
   }
+  return k;
+}
+
+template <int GD>
+__device__ __forceinline__ void load_code(const DecompressArgs& a, int rho, int g, int k,
+                                          uint4 (&w)[GD / 8]) {
   const uint4* cr =
       reinterpret_cast<const uint4*>(a.Cb + (static_cast<size_t>(rho * a.G + g) * a.K + k) * GD);
 #pragma unroll
@@ -388,7 +398,7 @@ __device__ __forceinline__ void load_code(const DecompressArgs& a, const uint8_t
 }
 
 template <int GD>
-__device__ __forceinline__ void add_code(const uint4 (&w)[GD / 8], float (&acc)[GD]) {
+__device__ __forceinline__ void add_code(const uint4 (&w)[GD / 8], float* acc) {
 #pragma unroll
   for (int c = 0; c < GD / 8; ++c) {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w[c]);
@@ -401,93 +411,97 @@ __device__ __forceinline__ void add_code(const uint4 (&w)[GD / 8], float (&acc)[
   }
 }
 
+// Z_hat row n of the VQ payload into this thread's TMEM lane, columns
+// [ta, ta + r / 2): per 64 elements (64 / GD groups), the code indices of
+// every round first, then the codes of two rounds at a time in flight, each
+// group summed over the rounds in order in fp32, then rounded to bf16.
 template <int GD>
-__device__ __forceinline__ void store_group(uint32_t abuf, int row, int g, const float (&acc)[GD]) {
+__device__ __forceinline__ void decode_row_tm(const DecompressArgs& a, uint32_t ta, int n,
+                                              bool live) {
+  constexpr int GP = 64 / GD;   // groups per 64 elements
+  const int R = a.R;
+  const uint8_t* ip = a.idx + static_cast<size_t>(n) * R * a.G;
+  for (int g0 = 0; g0 < a.G; g0 += GP) {
+    float v[64];
 #pragma unroll
-  for (int c = 0; c < GD / 8; ++c) {
-    const int col = g * GD + c * 8;
-    uint4 v;
-    v.x = pack_bf16x2(acc[c * 8 + 0], acc[c * 8 + 1]);
-    v.y = pack_bf16x2(acc[c * 8 + 2], acc[c * 8 + 3]);
-    v.z = pack_bf16x2(acc[c * 8 + 4], acc[c * 8 + 5]);
-    v.w = pack_bf16x2(acc[c * 8 + 6], acc[c * 8 + 7]);
-    st_shared_v4(abuf + (col >> 6) * kBlockBytes + sw128_off(row, (col & 63) >> 3), v);
+    for (int i = 0; i < 64; ++i) v[i] = 0.f;
+    if (live) {
+      for (int r0 = 0; r0 < R; r0 += 2) {
+        int k[2][GP];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int x = 0; x < GP; ++x) k[j][x] = r0 + j < R ? code_index(a, ip, r0 + j, g0 + x) : 0;
+        uint4 w[2][GP][GD / 8];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int x = 0; x < GP; ++x)
+            if (r0 + j < R) load_code<GD>(a, r0 + j, g0 + x, k[j][x], w[j][x]);
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int x = 0; x < GP; ++x)
+            if (r0 + j < R) add_code<GD>(w[j][x], v + x * GD);
+      }
+    }
+    uint32_t u[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) u[c] = pack_bf16x2(v[2 * c], v[2 * c + 1]);
+    tmem_st32u(ta + static_cast<uint32_t>(g0 * GD / 2), u);
   }
 }
 
-template <int GD>
-__device__ __forceinline__ void decode_row_pt(const DecompressArgs& a, uint32_t abuf, int row,
-                                              int n, bool live) {
-  // Z_hat[n, g-block] = sum_rho C[rho][g][idx[n][rho][g]]  (fp32, rounds in
-  // order, then bf16).  With R <= 2 the lookups of two groups are in flight
-  // together; otherwise up to four rounds of one group at a time.
-  const int G = a.G, R = a.R;
-  const uint8_t* ip = a.idx + static_cast<size_t>(n) * R * G;
-  if (R <= 2) {
-    for (int g = 0; g < G; g += 2) {
-      const int ng = g + 1 < G ? 2 : 1;
-      uint4 w[2][2][GD / 8];   // [group][round]
+// A bf16 row (ncol 32-bit columns, a multiple of 32) into this thread's
+// TMEM lane from `src` (16-byte aligned), or zeros when !live.
+__device__ __forceinline__ void copy_row_tm(const __nv_bfloat16* src, int ncol, uint32_t ta,
+                                            bool live) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  for (int c0 = 0; c0 < ncol; c0 += 32) {
+    uint4 w[8];
 #pragma unroll
-      for (int x = 0; x < 2; ++x)
+    for (int j = 0; j < 8; ++j) w[j] = live ? __ldg(s4 + c0 / 4 + j) : make_uint4(0u, 0u, 0u, 0u);
+    uint32_t u[32];
 #pragma unroll
-        for (int rho = 0; rho < 2; ++rho)
-          if (live && x < ng && rho < R) load_code<GD>(a, ip, rho, g + x, w[x][rho]);
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        if (x >= ng) break;
-        float acc[GD];
-#pragma unroll
-        for (int i = 0; i < GD; ++i) acc[i] = 0.f;
-#pragma unroll
-        for (int rho = 0; rho < 2; ++rho)
-          if (live && rho < R) add_code<GD>(w[x][rho], acc);
-        store_group<GD>(abuf, row, g + x, acc);
-      }
+    for (int j = 0; j < 8; ++j) {
+      u[4 * j] = w[j].x;
+      u[4 * j + 1] = w[j].y;
+      u[4 * j + 2] = w[j].z;
+      u[4 * j + 3] = w[j].w;
     }
-    return;
-  }
-  for (int g = 0; g < G; ++g) {
-    float acc[GD];
-#pragma unroll
-    for (int i = 0; i < GD; ++i) acc[i] = 0.f;
-    if (live) {
-      for (int r0 = 0; r0 < R; r0 += 4) {
-        uint4 w[4][GD / 8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (r0 + j < R) load_code<GD>(a, ip, r0 + j, g, w[j]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (r0 + j < R) add_code<GD>(w[j], acc);
-      }
-    }
-    store_group<GD>(abuf, row, g, acc);
+    tmem_st32u(ta + static_cast<uint32_t>(c0), u);
   }
 }
 
 template <int GD>
 __global__ void __launch_bounds__(kPtThreads, 1)
     k_decompress_pt(const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmZ,
-                    const __grid_constant__ CUtensorMap tmE,
                     const __grid_constant__ CUtensorMap tmXh, const DecompressArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   const int nst = a.nstage, nab = a.nab;
   const uint32_t sb = a.stage_bytes;
-  const uint32_t abuf0 = smem_u32(base);                     // A buffers
-  const uint32_t ring = abuf0 + nab * a.a_bytes;
+  const uint32_t ring = smem_u32(base);
   const uint32_t stage0 = ring + nst * sb;                   // drain staging
-  CtlPt* ctl = reinterpret_cast<CtlPt*>(base + nab * a.a_bytes + nst * sb + kPtStagingBytes);
+  CtlPt* ctl = reinterpret_cast<CtlPt*>(base + nst * sb + kPtStagingBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NC = a.nc;
   const int nchunk = a.d / NC;
   const int nzb = a.r / 64;          // K-blocks of Z_hat (and of E')
   const int nka = a.anchor ? 2 * nzb : nzb;   // K-blocks of [Z_hat | E'] (or Z_hat alone)
-  const int ntiles = (a.N + kTile - 1) / kTile;
-  const int L = blockIdx.x < ntiles ? (ntiles - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
-  const uint32_t tmem_cols = 2u * NC < 32u ? 32u : 2u * NC;
+  const uint32_t acol0 = 2u * static_cast<uint32_t>(NC);     // TMEM column of A buffer 0
+  const uint32_t acols = static_cast<uint32_t>(nka) * 32u;   // TMEM columns of one A buffer
+  // this CTA's rows: a contiguous run of 32-row blocks, [rbeg, rend), walked
+  // in tiles of up to 128 rows, so every SM writes about the same number of
+  // rows; tile edges fall on 32-row boxes, so no TMA store crosses into the
+  // next CTA's rows
+  const int nb32 = (a.N + 31) / 32;
+  const int blk0 = static_cast<int>(static_cast<long long>(nb32) * blockIdx.x / gridDim.x);
+  const int blk1 = static_cast<int>(static_cast<long long>(nb32) * (blockIdx.x + 1) / gridDim.x);
+  const int rbeg = 32 * blk0, rend = 32 * blk1 < a.N ? 32 * blk1 : a.N;
+  const int L = (blk1 - blk0 + 3) / 4;
+  constexpr uint32_t tmem_cols = 512;
   const uint64_t bud = a.timeout_ns;
 
   if (threadIdx.x == 0) {
@@ -496,12 +510,13 @@ __global__ void __launch_bounds__(kPtThreads, 1)
       mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&ctl->afull[b]), 2);
+      mbar_init(smem_u32(&ctl->afull[b]), 4);
       mbar_init(smem_u32(&ctl->aempty[b]), 1);
       mbar_init(smem_u32(&ctl->tfull[b]), 1);
       mbar_init(smem_u32(&ctl->tempty[b]), 4);
     }
     mbar_init(smem_u32(&ctl->done), 1);
+    mbar_init(smem_u32(&ctl->efull), 4);
     ctl->abort = 0;
     fence_mbar_init();
     fence_async_shared();
@@ -519,13 +534,14 @@ __global__ void __launch_bounds__(kPtThreads, 1)
       int s = 0, issued = 0;
       uint32_t ph = 0;
       bool ok = true;
+      // a stage holds two 64-element K-blocks of NC rows: one 3-D box
       for (int it = 0; it < L && ok; ++it)
         for (int c = 0; c < nchunk && ok; ++c)
-          for (int kb = 0; kb < nka; ++kb) {
+          for (int kb = 0; kb < nka; kb += 2) {
             if (!(ok = mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, &ctl->abort, bud))) break;
             const uint32_t fb = smem_u32(&ctl->full[s]);
-            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(NC) * 128u);
-            tma_load_2d(ring + s * sb, &tmB, kb * 64, c * NC, fb);
+            mbar_arrive_expect_tx(fb, 2u * static_cast<uint32_t>(NC) * 128u);
+            tma_load_3d(ring + s * sb, &tmB, 0, c * NC, kb, fb);
             ++issued;
             if (++s == nst) {
               s = 0;
@@ -546,7 +562,6 @@ __global__ void __launch_bounds__(kPtThreads, 1)
     if (lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       const uint32_t idc = idesc_bf16(kTile, NC);
-      const uint64_t a_d = sw128_desc(abuf0);
       const uint64_t r_d = sw128_desc(ring);
       int s = 0, cc = 0;
       uint32_t ph = 0;
@@ -555,22 +570,27 @@ __global__ void __launch_bounds__(kPtThreads, 1)
         const int ab = nab == 2 ? (it & 1) : 0;
         const int ause = nab == 2 ? (it >> 1) : it;
         if (!(ok = mbar_wait(smem_u32(&ctl->afull[ab]), ause & 1, &ctl->abort, bud))) break;
+        if (it == 0 && a.anchor && !(ok = mbar_wait(smem_u32(&ctl->efull), 0, &ctl->abort, bud)))
+          break;
         tc_fence_after();
-        const uint64_t ad = a_d + ((static_cast<uint32_t>(ab) * a.a_bytes) >> 4);
+        const uint32_t at = tbase + acol0 + static_cast<uint32_t>(ab) * acols;
         for (int c = 0; c < nchunk && ok; ++c, ++cc) {
           const int acc = cc & 1;
           if (!(ok = mbar_wait(smem_u32(&ctl->tempty[acc]), ((cc >> 1) & 1) ^ 1, &ctl->abort,
                                bud)))
             break;
           tc_fence_after();
-          for (int kb = 0; kb < nka; ++kb) {
+          for (int kb = 0; kb < nka; kb += 2) {
             if (!(ok = mbar_wait(smem_u32(&ctl->full[s]), ph, &ctl->abort, bud))) break;
             tc_fence_after();
-            const uint64_t bd = r_d + ((static_cast<uint32_t>(s) * sb) >> 4);
-            const uint64_t akd = ad + ((static_cast<uint32_t>(kb) * kBlockBytes) >> 4);
+            for (int j = 0; j < 2 && kb + j < nka; ++j) {
+              const uint64_t bd =
+                  r_d + ((static_cast<uint32_t>(s) * sb + static_cast<uint32_t>(j * NC) * 128u) >> 4);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_bf16(tbase + acc * NC, akd + 2 * k, bd + 2 * k, idc, (kb | k) != 0 ? 1u : 0u);
+              for (int k = 0; k < 4; ++k)
+                mma_bf16_ta(tbase + acc * NC, at + static_cast<uint32_t>((kb + j) * 32 + k * 8),
+                            bd + 2 * k, idc, (kb + j + k) != 0 ? 1u : 0u);
+            }
             mma_commit(smem_u32(&ctl->empty[s]));
             if (++s == nst) {
               s = 0;
@@ -588,70 +608,44 @@ __global__ void __launch_bounds__(kPtThreads, 1)
     }
   } else if (warp < kPtDrain0) {
     // ------------------------------------------------------------- builders
-    const int bt = threadIdx.x - kPtBuild0 * 32;   // row of the tile
-    if (bt == 0) {
-      prefetch_tmap(&tmE);
-      if (!a.vq) prefetch_tmap(&tmZ);
-    }
-    int last_ab = -1, last_use = 0;
+    const int row = (warp & 3) * 32 + lane;   // this thread's TMEM lane and tile row
+    const uint32_t tq = static_cast<uint32_t>((warp & 3) * 32) << 16;
     for (int it = 0; it < L; ++it) {
-      const int tile = blockIdx.x + it * gridDim.x;
+      const int t0 = rbeg + it * kTile;
+      const int cnt = rend - t0 < kTile ? rend - t0 : kTile;   // rows of this tile
       const int ab = nab == 2 ? (it & 1) : 0;
       const int ause = nab == 2 ? (it >> 1) : it;
-      const bool ok = mbar_wait(smem_u32(&ctl->aempty[ab]), (ause & 1) ^ 1, &ctl->abort, bud);
-      // one decision for all builder warps (they meet at named barriers below)
-      if (named_bar_or(kPtBuildBar, 128, !ok || ctl->abort)) {
-        if (bt == 0) give_up(ctl, a.err);
+      bool ok = mbar_wait(smem_u32(&ctl->aempty[ab]), (ause & 1) ^ 1, &ctl->abort, bud);
+      ok = __all_sync(0xffffffffu, ok) && !ctl->abort;
+      if (!ok) {
+        if (lane == 0) give_up(ctl, a.err);
         break;
       }
-      const uint32_t abuf = abuf0 + ab * a.a_bytes;
-      const int n = tile * kTile + bt;
+      tc_fence_after();   // the MMAs that read this buffer have completed
+      const int n = t0 + row;
+      const uint32_t ta = tbase + tq + acol0 + static_cast<uint32_t>(ab) * acols;
       int t = 0;
-      bool live = false;
-      if (n < a.N) {
-        live = true;
-        if (a.anchor) {
-          t = __ldg(a.tids + n);
-          live = t >= 0 && t < a.V;
-          if (!live) {
-            atomicOr(a.err, kErrBadToken);
-            t = 0;
-          }
+      bool live = row < cnt;
+      if (live && a.anchor) {
+        t = __ldg(a.tids + n);
+        if (t < 0 || t >= a.V) {
+          atomicOr(a.err, kErrBadToken);
+          live = false;
         }
-      }
-      ctl->ids[ab][bt] = t;
-      named_bar_sync(kPtBuildBar, 128);
-      if (bt < 32) {
-        // Z_hat (non-VQ payload) and the anchor rows E'[tids] by TMA.  Each
-        // lane of the first builder warp issues one four-row gather per
-        // K-block (one thread issuing all of them held the build back);
-        // afull completes only after lane 0's arrivals below, so the lanes'
-        // copies may land in any order around its expect_tx.
-        const uint32_t fb = smem_u32(&ctl->afull[ab]);
-        if (bt == 0) {
-          mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nzb) * kBlockBytes *
-                                        ((a.vq ? 0u : 1u) + (a.anchor ? 1u : 0u)));
-          if (!a.vq)
-            for (int kb = 0; kb < nzb; ++kb)
-              tma_load_2d(abuf + kb * kBlockBytes, &tmZ, kb * 64, tile * kTile, fb);
-          last_ab = ab;
-          last_use = ause;
-        }
-        const int32_t* ids = ctl->ids[ab] + 4 * bt;
-        if (a.anchor)
-          for (int kb = 0; kb < nzb; ++kb)
-            tma_gather4(abuf + (nzb + kb) * kBlockBytes + bt * 512, &tmE, kb * 64, ids[0], ids[1],
-                        ids[2], ids[3], fb);
       }
       if (a.vq) {
-        if constexpr (GD > 0) decode_row_pt<GD>(a, abuf, bt, n, live);
-        fence_async_shared();
-        named_bar_sync(kPtBuildBar, 128);
+        if constexpr (GD > 0) decode_row_tm<GD>(a, ta, n, live);
+      } else {
+        copy_row_tm(a.Zp + static_cast<size_t>(live ? n : 0) * a.r, a.r / 2, ta, live);
       }
-      if (bt == 0) mbar_arrive(smem_u32(&ctl->afull[ab]));
+      if (a.anchor && it > 0)   // the first tile's E' rows come from the drain warps
+        copy_row_tm(a.E + static_cast<size_t>(t) * a.r, a.r / 2, ta + static_cast<uint32_t>(a.r / 2),
+                    live);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->afull[ab]));
     }
-    if (bt == 0 && last_ab >= 0 && ctl->abort)
-      mbar_wait(smem_u32(&ctl->afull[last_ab]), last_use & 1, &ctl->abort, bud / 16);
   } else {
     // ---------------------------------------------------------------- drain
     // TMEM -> bf16 -> a swizzled 32-row x 64-column staging tile -> TMA
@@ -659,25 +653,43 @@ __global__ void __launch_bounds__(kPtThreads, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t trow = tbase + (static_cast<uint32_t>(q * 32) << 16);
+    if (a.anchor && L > 0) {
+      // the first tile's anchor rows E'[tids], written beside the builders'
+      // Z_hat so that the two chains of dependent loads run side by side
+      const int cnt0 = rend - rbeg < kTile ? rend - rbeg : kTile;
+      int t = 0;
+      bool live = row < cnt0;
+      if (live) {
+        t = __ldg(a.tids + rbeg + row);
+        live = t >= 0 && t < a.V;   // the builder flags a bad id
+      }
+      copy_row_tm(a.E + static_cast<size_t>(live ? t : 0) * a.r, a.r / 2,
+                  trow + acol0 + static_cast<uint32_t>(a.r / 2), live);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->efull));
+    }
     const uint32_t stg = stage0 + (warp - kPtDrain0) * 4096u;
     if (lane == 0) prefetch_tmap(&tmXh);
     int cc = 0;
     bool alive = true;
     for (int it = 0; it < L && alive; ++it) {
-      const int tile = blockIdx.x + it * gridDim.x;
-      const int n = tile * kTile + row;
-      const int row0 = tile * kTile + q * 32;     // first row of this warp's box
-      const bool any = row0 < a.N;
+      const int t0 = rbeg + it * kTile;
+      const int cnt = rend - t0 < kTile ? rend - t0 : kTile;   // rows of this tile
+      const int n = t0 + row;
+      const int row0 = t0 + q * 32;               // first row of this warp's box
+      const bool any = q * 32 < cnt;
       bool bad = false;
       int t = 0;
-      if (n < a.N && (a.anchor || a.Eadd)) {
+      if (row < cnt && (a.anchor || a.Eadd)) {
         t = __ldg(a.tids + n);
         bad = t < 0 || t >= a.V;
         if (bad && !a.anchor) atomicOr(a.err, kErrBadToken);   // no builder saw this id
       }
       // first-boundary anchor: the full embedding row is added in fp32
       const __nv_bfloat16* erow =
-          (a.Eadd && n < a.N && !bad) ? a.Eadd + static_cast<size_t>(t) * a.d : nullptr;
+          (a.Eadd && row < cnt && !bad) ? a.Eadd + static_cast<size_t>(t) * a.d : nullptr;
       for (int c = 0; c < nchunk; ++c, ++cc) {
         const int acc = cc & 1;
         bool ok = mbar_wait(smem_u32(&ctl->tfull[acc]), (cc >> 1) & 1, &ctl->abort, bud);
@@ -795,8 +807,7 @@ cudaError_t launch_decompress_tc(const CUtensorMap& tmB, const CUtensorMap& tmZ,
 
 namespace mapl {
 
-cudaError_t launch_decompress_pt(const CUtensorMap& tmB, const CUtensorMap& tmZ,
-                                 const CUtensorMap& tmE, const CUtensorMap& tmXh,
+cudaError_t launch_decompress_pt(const CUtensorMap& tmB, const CUtensorMap& tmXh,
                                  const DecompressArgs& a, uint32_t smem_bytes, int grid,
                                  cudaStream_t s) {
   cudaError_t e;
@@ -804,17 +815,17 @@ cudaError_t launch_decompress_pt(const CUtensorMap& tmB, const CUtensorMap& tmZ,
     case 0:
       e = set_smem(k_decompress_pt<0>, smem_bytes);
       if (e != cudaSuccess) return e;
-      k_decompress_pt<0><<<grid, kPtThreads, smem_bytes, s>>>(tmB, tmZ, tmE, tmXh, a);
+      k_decompress_pt<0><<<grid, kPtThreads, smem_bytes, s>>>(tmB, tmXh, a);
       break;
     case 16:
       e = set_smem(k_decompress_pt<16>, smem_bytes);
       if (e != cudaSuccess) return e;
-      k_decompress_pt<16><<<grid, kPtThreads, smem_bytes, s>>>(tmB, tmZ, tmE, tmXh, a);
+      k_decompress_pt<16><<<grid, kPtThreads, smem_bytes, s>>>(tmB, tmXh, a);
       break;
     case 32:
       e = set_smem(k_decompress_pt<32>, smem_bytes);
       if (e != cudaSuccess) return e;
-      k_decompress_pt<32><<<grid, kPtThreads, smem_bytes, s>>>(tmB, tmZ, tmE, tmXh, a);
+      k_decompress_pt<32><<<grid, kPtThreads, smem_bytes, s>>>(tmB, tmXh, a);
       break;
     default:
       return cudaErrorInvalidValue;

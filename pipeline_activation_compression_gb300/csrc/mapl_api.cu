@@ -209,36 +209,32 @@ mapl_status geometry(mapl_plan_s* pl) {
   }
   const uint32_t ctl = decompress_ctl_bytes() + 64;
   // decompress.  r <= 256: persistent kernel, one CTA per SM, the A operand
-  // [Z_hat | E'] resident (double buffered when two copies leave room for a
-  // ring of three stages).  Larger r: one CTA per tile, A streamed per stage.
+  // [Z_hat | E'] in TMEM (two buffers when they fit beside the two NC-column
+  // accumulators in the 512 columns), shared memory for the [A^T | P'^T]
+  // ring, as many stages as fit (at most 12).  Larger r: one CTA per tile,
+  // A streamed per stage.
   {
     const uint32_t a_res = static_cast<uint32_t>(2 * c.r / 64) * 16384u;
     pl->d_stream = a_res > 131072u;
-    const uint32_t NC = (c.d % 256 == 0) ? 256u : ((c.d % 128 == 0) ? 128u : 64u);
+    // output columns per accumulator chunk: 128 beside the TMEM-resident A,
+    // up to 256 when A is streamed
+    const uint32_t NC = pl->d_stream ? ((c.d % 256 == 0) ? 256u : ((c.d % 128 == 0) ? 128u : 64u))
+                                     : ((c.d % 128 == 0) ? 128u : 64u);
     pl->d_nc = NC;
     if (!pl->d_stream) {
-      // first of: double-buffered A with NC-column chunks, the same with
-      // 128-column chunks, single A buffer; each with at least three stages
+      const uint32_t acols = static_cast<uint32_t>(c.r);   // K = 2r bf16, two per column
+      const int nab = 2 * NC + 2 * acols <= 512u ? 2 : (2 * NC + acols <= 512u ? 1 : 0);
+      if (nab == 0) return fail(MAPL_ERR_UNSUPPORTED, "decompress operands do not fit in TMEM");
       const uint32_t extra = decompress_pt_ctl_bytes() + 64 + slack;
-      const uint32_t cand_nc[3] = {NC, NC > 128u ? 128u : NC, NC};
-      const int cand_nab[3] = {2, 2, 1};
-      bool found = false;
-      for (int k = 0; k < 3 && !found; ++k) {
-        const uint32_t used = extra + cand_nab[k] * a_res;
-        if (used >= kSmemMax) continue;
-        const uint32_t st = cand_nc[k] * 128u;
-        int ns = static_cast<int>((kSmemMax - used) / st);
-        if (ns > 8) ns = 8;
-        if (ns < (k < 2 ? 3 : 2)) continue;
-        pl->d_nc = cand_nc[k];
-        pl->d_nab = cand_nab[k];
-        pl->d_abytes = a_res;
-        pl->d_nstage = ns;
-        pl->d_stage = st;
-        pl->d_smem = ns * st + used;
-        found = true;
-      }
-      if (!found) return fail(MAPL_ERR_UNSUPPORTED, "decompress stages do not fit in shared memory");
+      const uint32_t st = 2u * NC * 128u;   // two 64-element K-blocks of NC rows
+      int ns = static_cast<int>((kSmemMax - extra) / st);
+      if (ns > 12) ns = 12;
+      if (ns < 3) return fail(MAPL_ERR_UNSUPPORTED, "decompress stages do not fit in shared memory");
+      pl->d_nab = nab;
+      pl->d_abytes = 0;
+      pl->d_nstage = ns;
+      pl->d_stage = st;
+      pl->d_smem = ns * st + extra;
     } else {
       const uint32_t st = NC * 128u + 16384u;
       const uint32_t extra = ctl + slack;
@@ -263,7 +259,11 @@ mapl_status build_plan_maps(mapl_plan_s* pl) {
     return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (A^T)");
   if (!make_tmap(&pl->tmMt, pl->p.Mts, c.r, static_cast<uint64_t>(kNumSplit) * c.r, 64, nrow))
     return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (M splits)");
-  if (!make_tmap(&pl->tmB, pl->p.Bcat, 2 * c.r, c.d, 64, static_cast<uint32_t>(NC)))
+  // [A | P'^T] (d x 2r): the persistent decompress loads two K-blocks per
+  // stage as one 3-D box {64, NC, 2}; the streamed one loads 2-D boxes
+  if (!(pl->d_stream ? make_tmap(&pl->tmB, pl->p.Bcat, 2 * c.r, c.d, 64, static_cast<uint32_t>(NC))
+                     : make_tmap_atoms(&pl->tmB, pl->p.Bcat, 2 * c.r, c.d,
+                                       static_cast<uint32_t>(NC), 2)))
     return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed ([A | P'^T])");
   if (pl->vq) {
     // one book per load, rows of gd bf16 in the swizzle that matches the row
@@ -735,6 +735,7 @@ static mapl_status decompress_common(mapl_plan pl, const void* payload, const in
   a.E = reinterpret_cast<const __nv_bfloat16*>(E_recv);
   a.Cb = grad_books ? pl->Cb_g : pl->p.Cb;
   a.idx = vq ? reinterpret_cast<const uint8_t*>(payload) : nullptr;
+  a.Zp = vq ? nullptr : reinterpret_cast<const __nv_bfloat16*>(payload);
   a.Xh = reinterpret_cast<__nv_bfloat16*>(X_hat);
   a.err = pl->p.err;
   a.N = static_cast<int>(N);
@@ -757,14 +758,13 @@ static mapl_status decompress_common(mapl_plan pl, const void* payload, const in
   a.timeout_ns = pl->timeout_ns;
   const int ntiles = static_cast<int>((N + kTile - 1) / kTile);
   if (pl->d_nab > 0) {
-    CUtensorMap tmE = tmZ;   // unused without the anchor
-    if (a.anchor && !make_tmap(&tmE, E_recv, c.r, static_cast<uint64_t>(c.V), 64, 1))
-      return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (E')");
     CUtensorMap tmXh;
     if (!make_tmap(&tmXh, X_hat, c.d, static_cast<uint64_t>(N), 64, 32))
       return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (X_hat)");
-    const int grid = ntiles < pl->num_sms ? ntiles : pl->num_sms;
-    e = launch_decompress_pt(pl->tmB, tmZ, tmE, tmXh, a, pl->d_smem, grid, stream);
+    // one contiguous range of 32-row blocks per CTA
+    const int64_t nb32 = (N + 31) / 32;
+    const int grid = static_cast<int>(nb32 < pl->num_sms ? nb32 : pl->num_sms);
+    e = launch_decompress_pt(pl->tmB, tmXh, a, pl->d_smem, grid, stream);
   } else {
     if (emb) return fail(MAPL_ERR_UNSUPPORTED, "the embedding anchor needs the persistent decompress");
     e = launch_decompress_tc(pl->tmB, tmZ, a, pl->d_smem, ntiles, stream);

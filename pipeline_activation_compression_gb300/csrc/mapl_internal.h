@@ -72,6 +72,7 @@ struct DecompressArgs {
   const __nv_bfloat16* E;           // V x r (receiver)
   const __nv_bfloat16* Cb;
   const uint8_t* idx;               // VQ payload (N x R x G) or null
+  const __nv_bfloat16* Zp;          // bf16 payload Z_hat (N x r) when not VQ
   __nv_bfloat16* Xh;                // N x d
   int* err;
   int N, d, r, V, G, R, K, gd;
@@ -119,8 +120,7 @@ cudaError_t launch_compress_pipe(const CUtensorMap& tmX, const CUtensorMap& tmAt
                                  const CUtensorMap& tmMt, const CUtensorMap& tmC,
                                  const CUtensorMap& tmE, const CompressArgs& a,
                                  uint32_t smem_bytes, int grid, cudaStream_t s);
-cudaError_t launch_decompress_pt(const CUtensorMap& tmB, const CUtensorMap& tmZ,
-                                 const CUtensorMap& tmE, const CUtensorMap& tmXh,
+cudaError_t launch_decompress_pt(const CUtensorMap& tmB, const CUtensorMap& tmXh,
                                  const DecompressArgs& a, uint32_t smem_bytes, int grid,
                                  cudaStream_t s);
 // Projector gradient on the tensor cores (kernels_grad_tc.cu).  Output

@@ -32,14 +32,16 @@
 // step's operand is in place while this one is scanned).  The distance
 // product s_k = u_hi.c_k + u_lo.c_k runs in 64-code chunks into two TMEM
 // chunk slots per set (double buffered: chunk c + 1 is computed while chunk c
-// is scanned).  The scan keeps the two smallest packed keys
-// (bits of D~_k = ||c_k||^2 - 2 s_k with the low 8 bits replaced by the code
-// index): one compare network per pair of codes, exact ties to the lower
-// index.  When the two best keys are too close for the certified error bound
-// (MMA error, fp32 rounding, the 2^-15 key truncation), every code inside the
-// band is re-scored on CUDA cores with a double-float squared distance, so
-// the chosen index is the exact nearest code of the fp32 residual (lowest
-// index on exact ties).  The residual update is fp32.
+// is scanned).  Each 32-code half of a chunk is scanned in two passes over
+// D~_k = ||c_k||^2 - 2 s_k: its minimum (three-input minimums), then on the
+// FMA pipe a saturated indicator of every code within a certified band of
+// the running minimum, summed with weights 1 + k / 1024 so that the count of
+// such codes and, when it is one, the code's index are both exact in fp32.
+// The band bounds the error of the split and of the fp32 products, so when
+// one code is inside it that code is the exact nearest code of the fp32
+// residual; otherwise (rare) every code of the 32-code halves that held a
+// candidate is re-scored on CUDA cores with a double-float squared
+// distance, lowest index on exact ties.  The residual update is fp32.
 //
 // Every wait is time bounded (mbar_wait); a CTA that gives up sets the device
 // error word, waits (bounded) for its own copies and products in flight, and

@@ -184,15 +184,23 @@ mapl_status geometry(mapl_plan_s* pl) {
     pl->c_stage = st;
     pl->c_smem = ns * st + extra;
   }
-  // pipelined compress: deep X ring (HBM), shallow B ring (A^T and -M^T
-  // blocks from L2), codebook ring
+  // pipelined compress: X ring (HBM), B ring (A^T and -M^T blocks from L2),
+  // codebook ring
   pl->c_pipe = compress_pipe_supported(static_cast<int>(c.r), pl->vq, pl->gd, c.G);
   if (pl->c_pipe) {
     const uint32_t fixed = compress_pipe_ctl_bytes() + 64 + slack;
     const uint32_t bst = static_cast<uint32_t>(c.r) * 128u;
     const uint32_t cst = pl->vq ? ((static_cast<uint32_t>(c.K * pl->gd) * 2u + 1023u) & ~1023u) : 0u;
     const int ncb = pl->vq ? 4 : 0;   // two codebook stages per epilogue warp set
-    const int nb = bst > 16384u ? 3 : 4;
+    // without codebooks, half the shared memory goes to the B ring: its
+    // blocks are re-read from L2 for every tile, so it needs as many bytes
+    // in flight as the X ring
+    int nb = bst > 16384u ? 3 : 4;
+    if (!pl->vq) {
+      nb = static_cast<int>((kSmemMax - fixed) / 2u / bst);
+      if (nb > 8) nb = 8;
+      if (nb < 3) nb = 3;
+    }
     const uint32_t used = fixed + nb * bst + ncb * cst;
     int nx = used < kSmemMax ? static_cast<int>((kSmemMax - used) / 16384u) : 0;
     if (nx > 12) nx = 12;

@@ -15,11 +15,12 @@
 //   warp 3 lane 0 : TMA producer of the B ring: A^T blocks, then the -M^T
 //                   split blocks.  A^T comes from L2, so this ring is kept
 //                   shallow and the X ring deep: the two advance on their own.
-//   warp 2 lane 0 : TMA producer of the codebook ring (one book per VQ step).
-//   warp 1        : TMEM allocation; lane 0 issues every tcgen05.mma: the
-//                   projection of the tile into the Z accumulator and the VQ
-//                   distance products, in 64-code chunks, of two independent
-//                   step streams (one per epilogue warp set).
+//   warp 2 lane 0 : TMA producer of the codebook ring (one book per VQ step)
+//                   and issuer of the VQ distance products, in 128-code
+//                   chunks, of two independent step streams (one per
+//                   epilogue warp set).
+//   warp 1        : TMEM allocation; lane 0 issues the projection of each
+//                   tile into the Z accumulator.
 //   warps 4..11   : epilogue.  Warp w reads TMEM lanes 32 (w % 4).. (its token
 //                   rows); warp set j = (w - 4) / 4 owns the groups g = j mod 2
 //                   of those rows: their residuals stay in its registers through
@@ -27,21 +28,27 @@
 //                   result is merged across warps.
 //
 // VQ step (group g, round rho) of a warp set.  The residual u (fp32) is split
-// into u_hi = bf16(u) and u_lo = bf16(u - u_hi) and written to a TMEM operand
-// slot (two per set, alternating between consecutive steps, so the next
-// step's operand is in place while this one is scanned).  The distance
-// product s_k = u_hi.c_k + u_lo.c_k runs in 64-code chunks into two TMEM
-// chunk slots per set (double buffered: chunk c + 1 is computed while chunk c
-// is scanned).  Each 32-code half of a chunk is scanned in two passes over
-// D~_k = ||c_k||^2 - 2 s_k: its minimum (three-input minimums), then on the
-// FMA pipe a saturated indicator of every code within a certified band of
-// the running minimum, summed with weights 1 + k / 1024 so that the count of
-// such codes and, when it is one, the code's index are both exact in fp32.
-// The band bounds the error of the split and of the fp32 products, so when
-// one code is inside it that code is the exact nearest code of the fp32
-// residual; otherwise (rare) every code of the 32-code halves that held a
-// candidate is re-scored on CUDA cores with a double-float squared
-// distance, lowest index on exact ties.  The residual update is fp32.
+// into u_hi = bf16(u) and u_lo = bf16(u - u_hi), and -u_hi, -u_lo are written
+// to a TMEM operand slot (two per set, alternating between consecutive steps,
+// so the next step's operand is in place while this one is scanned).  One
+// accumulation per 128-code chunk gives
+//     t_k = ||c_k||^2 / 2 - u_hi.c_k - u_lo.c_k  (= D~_k / 2),
+// the norm entering as one more K = 16 product of a constant shared-memory
+// tile of rows [1, 1, 1, 0, ...] with the book's rows [h_hi, h_mid, h_lo, 0,
+// ...], the three bf16 terms of the fp32 ||c_k||^2 / 2 (loaded with the
+// codes), so the scan reads the distances straight from TMEM.  The chunk
+// lands in one TMEM slot per set; the other set's chunk is computed while
+// this one is scanned, and the slot is released as soon as its last quarter
+// is loaded.  Each 32-code quarter is scanned in two passes: its minimum
+// (three-input minimums), then on the FMA pipe a saturated indicator of every
+// code within a certified band of the running minimum, summed with weights
+// 1 + k / 1024 so that the count of such codes and, when it is one, the
+// code's index are both exact in fp32.  The band bounds the error of the
+// split, of the norm's split and of the fp32 accumulation, so when one code
+// is inside it that code is the exact nearest code of the fp32 residual;
+// otherwise (rare) every code of the 32-code quarters that held a candidate
+// is re-scored on CUDA cores with a double-float squared distance, lowest
+// index on exact ties.  The residual update is fp32.
 //
 // Every wait is time bounded (mbar_wait); a CTA that gives up sets the device
 // error word, waits (bounded) for its own copies and products in flight, and
@@ -62,7 +69,8 @@ constexpr uint32_t kXBytes = kTile * 128;   // 128 rows x 64 bf16, 128B swizzled
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr uint32_t kColOp = 128;            // TMEM columns of the operand slots
 constexpr uint32_t kColDist = 256;          // TMEM columns of the distance chunk slots
-constexpr int kChunk = 64;                  // codes per distance MMA
+constexpr int kChunk = 128;                 // codes per distance MMA (one TMEM slot per set)
+constexpr uint32_t kOnesBytes = 128 * 32;   // A tile of the norm product: 128 rows x 16 bf16
 static_assert(kTile == 4 * 32, "one four-row gather per lane of the producer warp");
 
 struct Ctl {
@@ -124,8 +132,10 @@ __device__ __forceinline__ Range cta_range(int N) {
   return r;
 }
 
-// Split of the residual into the TMEM operand [hi (GD) | lo (GD)] of the
-// distance MMA, two bf16 per column; returns ||u|| rounded up.
+// Split of the negated residual into the TMEM operand [-u_hi (GD) | -u_lo
+// (GD)] of the distance MMA, two bf16 per column (negation is exact and
+// commutes with round-to-nearest, so these are the negated terms of u's own
+// split); returns ||u|| rounded up.
 template <int GD>
 __device__ __forceinline__ float write_operand(uint32_t taddr, const float (&u)[GD]) {
   uint32_t w[GD];
@@ -138,8 +148,8 @@ __device__ __forceinline__ float write_operand(uint32_t taddr, const float (&u)[
     const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
     const float2 hf = __bfloat1622float2(h);
     const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-    w[e] = *reinterpret_cast<const uint32_t*>(&h);
-    w[GD / 2 + e] = *reinterpret_cast<const uint32_t*>(&l);
+    w[e] = *reinterpret_cast<const uint32_t*>(&h) ^ 0x80008000u;
+    w[GD / 2 + e] = *reinterpret_cast<const uint32_t*>(&l) ^ 0x80008000u;
   }
   if constexpr (GD == 32)
     tmem_st32u(taddr, w);
@@ -269,24 +279,16 @@ __device__ __forceinline__ float fma_sat(float a, float b, float c) {
   return r;
 }
 
-// Half of a 64-code chunk of the distance scan (32 codes), two passes over
-// the registers.  Pass 1: the minimum m of D~_k = ||c_k||^2 - 2 s_k
-// (three-input minimums, the only ALU-pipe work).  Pass 2, on the FMA pipe:
-// with thr = min(T, m) + band (T the minimum of the step's earlier codes),
-// sat((thr - D~_k) 2^60) is 1 for every code below thr and 0 for every code
-// at or above it, and acc = sum of sat(...) (1 + k / 1024) holds the number
-// of those codes in its integer part and, when there is exactly one, its
-// index k (< 256) in the fraction, both exact in fp32.  Returns m.
-__device__ __forceinline__ float scan_half(float (&v)[32], const float* cn, float T, float band,
-                                           float& acc) {
-#pragma unroll
-  for (int i = 0; i < 32; i += 4) {
-    const float4 f = __ldg(reinterpret_cast<const float4*>(cn + i));
-    v[i] = fmaf(-2.f, v[i], f.x);
-    v[i + 1] = fmaf(-2.f, v[i + 1], f.y);
-    v[i + 2] = fmaf(-2.f, v[i + 2], f.z);
-    v[i + 3] = fmaf(-2.f, v[i + 3], f.w);
-  }
+// A quarter of a 128-code chunk of the distance scan (32 codes), two passes over
+// the registers, which hold t_k = ||c_k||^2 / 2 - u.c_k = D~_k / 2 as the
+// distance MMA left it.  Pass 1: the minimum m (three-input minimums, the
+// only ALU-pipe work).  Pass 2, on the FMA pipe: with thr = min(T, m) + band
+// (T the minimum of the step's earlier codes), sat((thr - t_k) 2^60) is 1
+// for every code below thr and 0 for every code at or above it, and acc =
+// sum of sat(...) (1 + k / 1024) holds the number of those codes in its
+// integer part and, when there is exactly one, its index k (< 32) in the
+// fraction, both exact in fp32.  Returns m.
+__device__ __forceinline__ float scan_half(const float (&v)[32], float T, float band, float& acc) {
   float t[11];
 #pragma unroll
   for (int i = 0; i < 10; ++i) t[i] = fmin3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
@@ -423,45 +425,59 @@ __device__ void epilogue_vq(const CompressArgs& a, Ctl* ctl, const Range& rg, ui
         const uint32_t cph = (gstep >> 1) & 1u;
         const float* cn = a.cnorm + book * K;
         // band = twice the certified bound on |D~_k - D_k| for every code of
-        // the book (the two-term split of u, |u - u_hi - u_lo| <= 2^-18 |u|;
-        // fp32 accumulation of 2 GD exact products; fp32 rounding of ||c||^2
-        // and of the fma; |D~| <= ||c||^2 + 2 ||u|| ||c||), widened for the
-        // rounding of the scan's threshold test
+        // the book (the two-term split of u, |u - u_hi - u_lo| <= 2^-17 |u|;
+        // fp32 accumulation of 2 GD + 3 exact products, ||c||^2 / 2 among
+        // them; fp32 rounding of ||c||^2 and of its three-term split;
+        // |D~| <= ||c||^2 + 2 ||u|| ||c||), widened for the rounding of the
+        // scan's threshold test.  The scan runs on t = D~ / 2, so with half
+        // the band.
         const float cm = __ldg(a.cmax + book);
         const float nuv = nu[gi];
         const float dmax = cm * cm + 2.f * nuv * cm;
-        const float band = 2.f * (2e-5f * nuv * cm + 2.4e-7f * dmax) * 1.001f + 2.4e-7f * dmax;
-        // 1. scan all chunks of this step, keeping the step minimum T, an
-        // upper bound n on the number of codes within `band` of it and, for
-        // n == 1, that code's index
+        const float band = 2.f * (2e-5f * nuv * cm + 4.2e-6f * dmax) * 1.001f + 2.4e-7f * dmax;
+        const float band_t = 0.5f * band;
+        // 1. scan all chunks of this step, keeping the step minimum T (of
+        // t), an upper bound n on the number of codes within `band_t` of it
+        // and, for n == 1, that code's index
         float T = __int_as_float(0x7f800000);
         int ncand = 0;
         int K1 = 0;
         uint32_t halves = 0;
         for (int c = 0; c < nch; ++c) {
-          const uint32_t ds = 2 * j + (cc & 1u);
-          if (!warp_wait(smem_u32(&ctl->dfull[ds]), (cc >> 1) & 1u, ctl, bud)) {
+          const uint32_t ds = static_cast<uint32_t>(j);   // this set's chunk slot
+          if (!warp_wait(smem_u32(&ctl->dfull[ds]), cc & 1u, ctl, bud)) {
             give_up(ctl, a.err);
             alive = false;
             break;
           }
           tc_fence_after();
-          // the chunk in two halves of 32 codes (fewer live registers)
+          // the chunk in four quarters of 32 codes, each quarter's TMEM load
+          // overlapping the previous quarter's scan; the slot is released
+          // once the last quarter is in registers
+          const uint32_t td = tdist + ds * kChunk;
+          const int c0 = c * kChunk;
           float v[32], w[32];
           float acc;
-          tmem_ld32(tdist + ds * kChunk, v);
+          tmem_ld32(td, v);
           tmem_wait_ld();
-          // the second half's load overlaps the first half's scan
-          tmem_ld32(tdist + ds * kChunk + 32, w);
-          float m = scan_half(v, cn + c * kChunk, T, band, acc);
-          merge_half(m, acc, c * kChunk, band, T, ncand, K1, halves);
+          tmem_ld32(td + 32, w);
+          float m = scan_half(v, T, band_t, acc);
+          merge_half(m, acc, c0, band_t, T, ncand, K1, halves);
+          tmem_wait_ld();
+          tmem_ld32(td + 64, v);
+          m = scan_half(w, T, band_t, acc);
+          merge_half(m, acc, c0 + 32, band_t, T, ncand, K1, halves);
+          tmem_wait_ld();
+          tmem_ld32(td + 96, w);
+          m = scan_half(v, T, band_t, acc);
+          merge_half(m, acc, c0 + 64, band_t, T, ncand, K1, halves);
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&ctl->dempty[ds]));
           ++cc;
-          m = scan_half(w, cn + c * kChunk + 32, T, band, acc);
-          merge_half(m, acc, c * kChunk + 32, band, T, ncand, K1, halves);
+          m = scan_half(w, T, band_t, acc);
+          merge_half(m, acc, c0 + 96, band_t, T, ncand, K1, halves);
         }
         if (!alive) break;
         // 2. decision: a single code within the band of the minimum is the
@@ -476,9 +492,9 @@ __device__ void epilogue_vq(const CompressArgs& a, Ctl* ctl, const Range& rg, ui
         }
         const uint8_t* stage = cring_p + cs * cbsb;
         if (__any_sync(kFull, need)) {
-          // band of the candidates: the MMA band plus the error of the fp32
-          // CUDA-core dot products (GD exact products, fp32 sums)
-          const float thr = T + band + 4e-6f * nuv * cm + 2.4e-7f * dmax;
+          // band of the candidates, in D~: the MMA band plus the error of
+          // the fp32 CUDA-core dot products (GD exact products, fp32 sums)
+          const float thr = 2.f * T + band + 4e-6f * nuv * cm + 2.4e-7f * dmax;
           const int kb = refine<GD>(u[gi], cn, stage, uscr, thr, halves, need, K1, lane);
           if (need) K1 = kb;
         }
@@ -519,15 +535,18 @@ template <int GD, int NGW>
 __global__ void __launch_bounds__(kThreads, 1)
     k_compress_pipe(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmAt,
                     const __grid_constant__ CUtensorMap tmMt, const __grid_constant__ CUtensorMap tmC,
-                    const __grid_constant__ CUtensorMap tmE, const CompressArgs a) {
+                    const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmE,
+                    const CompressArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   constexpr bool vq = GD > 0;
   const int nx = a.nstage, nb = a.nbstage, ncb = vq ? a.ncb : 0;
   const uint32_t bsb = a.bstage_bytes;
   const uint32_t cbsb = a.cstage_bytes;
-  // shared memory: X ring | B ring | codebook ring (two stages per warp set)
-  // | control
+  // shared memory: X ring | B ring | codebook ring (two stages per warp set;
+  // a stage holds the book's codes, then its rows [h_hi, h_mid, h_lo, 0...]
+  // of ||c||^2 / 2 in three bf16 terms) | the constant A tile of the norm
+  // product (VQ) | control
   const uint32_t xring = smem_u32(base);
   uint32_t off = nx * kXBytes;
   const uint32_t bring = xring + off;
@@ -535,6 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t cring = xring + off;
   const uint32_t cring_off = off;
   off += ncb * cbsb;
+  const uint32_t ones = xring + off;
+  if (vq) off += kOnesBytes;
   Ctl* ctl = reinterpret_cast<Ctl*>(base + off);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -578,13 +599,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) tmem_alloc(smem_u32(&ctl->tmem_base), tmem_cols);
   if (vq && warp >= kEpiWarp0) {
-    // bring the code norms and the per-book bounds into L1 before the first
-    // step reads them
-    const int n4 = a.R * a.G * a.K / 4;
+    // the A operand of the norm product: 128 rows [1, 1, 1, 0, ..., 0] of 16
+    // bf16 (32 bytes, the 32-byte swizzle: 16-byte chunk c of row i sits at
+    // chunk c ^ ((i >> 2) & 1)); one 16-byte chunk per epilogue thread
+    const int x = threadIdx.x - kEpiWarp0 * 32;   // 0..255
+    const int row = x >> 1, chunk = x & 1;
+    const bool lead = (chunk ^ ((row >> 2) & 1)) == 0;
+    const uint32_t dst = ones + static_cast<uint32_t>(row * 32 + chunk * 16);
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %3};" ::"r"(dst),
+                 "r"(lead ? 0x3F803F80u : 0u), "r"(lead ? 0x00003F80u : 0u), "r"(0u)
+                 : "memory");
+    fence_async_shared();
+    // bring the per-book bounds into L1 before the first step reads them
     float acc = 0.f;
-    for (int x = threadIdx.x - kEpiWarp0 * 32; x < n4; x += 8 * 32)
-      acc += __ldg(reinterpret_cast<const float4*>(a.cnorm) + x).x;
-    for (int x = threadIdx.x - kEpiWarp0 * 32; x < a.R * a.G; x += 8 * 32) acc += __ldg(a.cmax + x);
+    for (int y = x; y < a.R * a.G; y += 8 * 32) acc += __ldg(a.cmax + y);
     if (acc == 12345.f) ctl->abort = 0;   // keeps the loads
   }
   tc_fence_before();
@@ -683,18 +711,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Lane 0 serves the two warp sets' step streams, each with its own two
     // codebook stages (set j: stages 2j, 2j + 1, alternating between its
     // steps), so neither set waits for the other's books.  Per set: load the
-    // next book once its stage is released, and issue the next 64-code chunk
+    // next book once its stage is released, and issue the next 128-code chunk
     // of the distance product once the step's operand is written, its book
     // has landed and the chunk's TMEM slot has been read.  Non-blocking
     // probes, a short sleep when nothing can move.
     if constexpr (vq) if (lane == 0) {
       prefetch_tmap(&tmC);
+      prefetch_tmap(&tmH);
       constexpr int kStepsC = GD / 16;
       constexpr int kRowB = 2 * GD;
       const int nch = a.K / kChunk;
       const uint32_t total = static_cast<uint32_t>(L * a.R * NGW);   // steps per set
       const uint32_t idd = idesc_bf16(kTile, kChunk);
-      const uint32_t cbytes = static_cast<uint32_t>(a.K * a.gd) * 2u;
+      const uint32_t cbytes = static_cast<uint32_t>(a.K * a.gd) * 2u;   // codes; the norm rows follow
+      const uint32_t hbytes = static_cast<uint32_t>(a.K) * 32u;
+      const uint64_t od = narrow_desc<32>(ones);
       uint32_t lb[2] = {0u, 0u};           // books loaded
       int lb_rho[2] = {0, 0}, lb_gi[2] = {0, 0};
       uint32_t x[2] = {0u, 0u};            // chunks issued
@@ -713,9 +744,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = 2 * j + static_cast<int>(lb[j] & 1u);
             if (mbar_test(smem_u32(&ctl->cempty[s]), ((lb[j] >> 1) & 1u) ^ 1u)) {
               const uint32_t fb = smem_u32(&ctl->cfull[s]);
-              mbar_arrive_expect_tx(fb, cbytes);
-              tma_load_2d(cring + s * cbsb, &tmC, 0, (lb_rho[j] * a.G + 2 * lb_gi[j] + j) * a.K,
-                          fb);
+              mbar_arrive_expect_tx(fb, cbytes + hbytes);
+              const int row0 = (lb_rho[j] * a.G + 2 * lb_gi[j] + j) * a.K;
+              tma_load_2d(cring + s * cbsb, &tmC, 0, row0, fb);
+              tma_load_2d(cring + s * cbsb + cbytes, &tmH, 0, row0, fb);
               ++lb[j];
               if (++lb_gi[j] == NGW) {
                 lb_gi[j] = 0;
@@ -731,18 +763,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!got_op[j])
               got_op[j] = mbar_test(smem_u32(&ctl->opready[2 * j + oslot]), (st[j] >> 1) & 1u);
             if (!got_cb[j]) got_cb[j] = mbar_test(smem_u32(&ctl->cfull[s]), (st[j] >> 1) & 1u);
-            const uint32_t ds = 2u * j + (x[j] & 1u);
+            const uint32_t ds = static_cast<uint32_t>(j);   // one chunk slot per set
             if (got_op[j] && got_cb[j] &&
-                mbar_test(smem_u32(&ctl->dempty[ds]), ((x[j] >> 1) & 1u) ^ 1u)) {
+                mbar_test(smem_u32(&ctl->dempty[ds]), (x[j] & 1u) ^ 1u)) {
               tc_fence_after();
               const uint32_t at = tbase + kColOp + (2u * j + oslot) * 32u;
               const uint32_t dt = tbase + kColDist + ds * kChunk;
+              const uint32_t sb = cring + static_cast<uint32_t>(s) * cbsb;
               const uint64_t bd = narrow_desc<(GD == 32 ? 64 : 32)>(
-                  cring + static_cast<uint32_t>(s) * cbsb +
-                  static_cast<uint32_t>(ch[j] * kChunk * kRowB));
+                  sb + static_cast<uint32_t>(ch[j] * kChunk * kRowB));
+              const uint64_t hd = narrow_desc<32>(sb + cbytes + static_cast<uint32_t>(ch[j] * kChunk * 32));
+              // t = ||c||^2 / 2 (ones x norm rows) - u_hi.c - u_lo.c
+              mma_bf16(dt, od, hd, idd, 0u);
 #pragma unroll
               for (int k = 0; k < 2 * kStepsC; ++k)
-                mma_bf16_ta(dt, at + 8 * k, bd + 2 * (k % kStepsC), idd, k != 0 ? 1u : 0u);
+                mma_bf16_ta(dt, at + 8 * k, bd + 2 * (k % kStepsC), idd, 1u);
               mma_commit(smem_u32(&ctl->dfull[ds]));
               issued = true;
               moved = true;
@@ -917,21 +952,23 @@ cudaError_t set_smem(KernelT k, uint32_t bytes) {
 
 template <int GD, int NGW>
 cudaError_t launch_one(const CUtensorMap& tmX, const CUtensorMap& tmAt, const CUtensorMap& tmMt,
-                       const CUtensorMap& tmC, const CUtensorMap& tmE, const CompressArgs& a,
-                       uint32_t smem, int grid, cudaStream_t s) {
+                       const CUtensorMap& tmC, const CUtensorMap& tmH, const CUtensorMap& tmE,
+                       const CompressArgs& a, uint32_t smem, int grid, cudaStream_t s) {
   const cudaError_t e = set_smem(k_compress_pipe<GD, NGW>, smem);
   if (e != cudaSuccess) return e;
-  k_compress_pipe<GD, NGW><<<grid, kThreads, smem, s>>>(tmX, tmAt, tmMt, tmC, tmE, a);
+  k_compress_pipe<GD, NGW><<<grid, kThreads, smem, s>>>(tmX, tmAt, tmMt, tmC, tmH, tmE, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 uint32_t compress_pipe_ctl_bytes() { return static_cast<uint32_t>(sizeof(Ctl)); }
+uint32_t compress_pipe_ones_bytes() { return kOnesBytes; }
 
-bool compress_pipe_supported(int r, bool vq, int gd, int G) {
+bool compress_pipe_supported(int r, bool vq, int gd, int G, int K) {
   if (!vq) return r % 64 == 0 && r <= 256;
   if (r != 64 && r != 128) return false;
+  if (K % kChunk != 0) return false;
   if (gd != 16 && gd != 32) return false;
   const int ngw = G / 2;
   return G % 2 == 0 && (ngw == 1 || ngw == 2 || ngw == 4) && ngw * gd * 2 == r;
@@ -939,15 +976,20 @@ bool compress_pipe_supported(int r, bool vq, int gd, int G) {
 
 cudaError_t launch_compress_pipe(const CUtensorMap& tmX, const CUtensorMap& tmAt,
                                  const CUtensorMap& tmMt, const CUtensorMap& tmC,
-                                 const CUtensorMap& tmE, const CompressArgs& a,
-                                 uint32_t smem_bytes, int grid, cudaStream_t s) {
+                                 const CUtensorMap& tmH, const CUtensorMap& tmE,
+                                 const CompressArgs& a, uint32_t smem_bytes, int grid,
+                                 cudaStream_t s) {
   if (a.mode != kModeVQ)
-    return launch_one<0, 1>(tmX, tmAt, tmMt, tmC, tmE, a, smem_bytes, grid, s);
+    return launch_one<0, 1>(tmX, tmAt, tmMt, tmC, tmH, tmE, a, smem_bytes, grid, s);
   const int ngw = a.G / 2;
-  if (a.gd == 32 && ngw == 2) return launch_one<32, 2>(tmX, tmAt, tmMt, tmC, tmE, a, smem_bytes, grid, s);
-  if (a.gd == 16 && ngw == 4) return launch_one<16, 4>(tmX, tmAt, tmMt, tmC, tmE, a, smem_bytes, grid, s);
-  if (a.gd == 32 && ngw == 1) return launch_one<32, 1>(tmX, tmAt, tmMt, tmC, tmE, a, smem_bytes, grid, s);
-  if (a.gd == 16 && ngw == 2) return launch_one<16, 2>(tmX, tmAt, tmMt, tmC, tmE, a, smem_bytes, grid, s);
+  if (a.gd == 32 && ngw == 2)
+    return launch_one<32, 2>(tmX, tmAt, tmMt, tmC, tmH, tmE, a, smem_bytes, grid, s);
+  if (a.gd == 16 && ngw == 4)
+    return launch_one<16, 4>(tmX, tmAt, tmMt, tmC, tmH, tmE, a, smem_bytes, grid, s);
+  if (a.gd == 32 && ngw == 1)
+    return launch_one<32, 1>(tmX, tmAt, tmMt, tmC, tmH, tmE, a, smem_bytes, grid, s);
+  if (a.gd == 16 && ngw == 2)
+    return launch_one<16, 2>(tmX, tmAt, tmMt, tmC, tmH, tmE, a, smem_bytes, grid, s);
   return cudaErrorInvalidValue;
 }
 

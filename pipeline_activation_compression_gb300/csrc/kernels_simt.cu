@@ -147,8 +147,26 @@ __global__ void k_prep_At32(const float* A, int d, int r, float* At) {
   At[idx] = A[static_cast<size_t>(i) * r + j];
 }
 
+// Norm row of a code for the distance MMA: h = cn / 2 (exact) as three bf16
+// terms h_hi = bf16(h), h_mid = bf16(h - h_hi), h_lo = bf16(h - h_hi -
+// h_mid) (each remainder is exact in fp32, and the three terms carry h's 24
+// significant bits), then 13 zeros: 32 bytes, two 16-byte stores.
+__device__ __forceinline__ void write_norm_row(float cn, __nv_bfloat16* row) {
+  const float h = 0.5f * cn;
+  const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+  const float r1 = h - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+  const uint32_t w0 = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
+                      (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16);
+  const uint32_t w1 = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
+  uint4* d = reinterpret_cast<uint4*>(row);
+  d[0] = make_uint4(w0, w1, 0u, 0u);
+  d[1] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 __global__ void k_prep_codes(const void* C, int nbooks, int K, int gd, bool bf,
-                             __nv_bfloat16* Cb, float* C32, float* cnorm) {
+                             __nv_bfloat16* Cb, __nv_bfloat16* Hs, float* C32, float* cnorm) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;   // code id over all books
   if (idx >= nbooks * K) return;
   double s = 0.0;
@@ -159,6 +177,7 @@ __global__ void k_prep_codes(const void* C, int nbooks, int K, int gd, bool bf,
     if (C32) C32[static_cast<size_t>(idx) * gd + i] = static_cast<float>(v);
   }
   cnorm[idx] = static_cast<float>(s);
+  if (Hs) write_norm_row(static_cast<float>(s), Hs + static_cast<size_t>(idx) * 16);
 }
 
 // max_k ||c_k|| of each book, rounded up: one warp per book (the maximum of
@@ -304,7 +323,7 @@ cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps
   if (!A_only && c.G > 0) {
     const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G);
     k_prep_codes<<<blocks_for(static_cast<size_t>(nb) * c.K, T), T, 0, s>>>(
-        C, nb, c.K, gd, true, p.Cb, nullptr, p.cnorm);
+        C, nb, c.K, gd, true, p.Cb, p.Hs, nullptr, p.cnorm);
     k_prep_cmax<<<blocks_for(static_cast<size_t>(nb) * 32, 256), 256, 0, s>>>(p.cnorm, nb, c.K, p.cmax);
   }
   return cudaGetLastError();
@@ -313,10 +332,10 @@ cudaError_t launch_prep_bf16(const mapl_config& c, const void* A, const void* Ps
 // A bf16 codebook set (R x G x K x gd) copied into plan storage with its
 // squared norms and per-book maxima (the gradient codebooks of §3.5).
 cudaError_t launch_prep_books_bf16(const mapl_config& c, const void* C, __nv_bfloat16* Cb,
-                                   float* cnorm, float* cmax, cudaStream_t s) {
+                                   __nv_bfloat16* Hs, float* cnorm, float* cmax, cudaStream_t s) {
   const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G);
-  k_prep_codes<<<blocks_for(static_cast<size_t>(nb) * c.K, 256), 256, 0, s>>>(C, nb, c.K, gd, true,
-                                                                              Cb, nullptr, cnorm);
+  k_prep_codes<<<blocks_for(static_cast<size_t>(nb) * c.K, 256), 256, 0, s>>>(
+      C, nb, c.K, gd, true, Cb, Hs, nullptr, cnorm);
   k_prep_cmax<<<blocks_for(static_cast<size_t>(nb) * 32, 256), 256, 0, s>>>(cnorm, nb, c.K, cmax);
   return cudaGetLastError();
 }
@@ -332,6 +351,7 @@ cudaError_t launch_split_negMt(const float* M, int r, __nv_bfloat16* Mts, cudaSt
 __device__ __forceinline__ void update_one_code(int id, int i, const void* __restrict__ codes,
                                                 int gd, int ncode, bool bf,
                                                 __nv_bfloat16* __restrict__ Cb,
+                                                __nv_bfloat16* __restrict__ Hs,
                                                 float* __restrict__ C32, float* __restrict__ cnorm,
                                                 int* err) {
   if (id < 0 || id >= ncode) {
@@ -374,6 +394,7 @@ __device__ __forceinline__ void update_one_code(int id, int i, const void* __res
     }
   }
   cnorm[id] = static_cast<float>(s);
+  if (Hs) write_norm_row(static_cast<float>(s), Hs + static_cast<size_t>(id) * 16);
 }
 
 // Streaming codebook update (§3.5, App. F): code ids[i] (flat over R x G x
@@ -384,11 +405,12 @@ __device__ __forceinline__ void update_one_code(int id, int i, const void* __res
 // so an update is one launch.
 __global__ void __launch_bounds__(128) k_update_codes(const int32_t* ids, int count,
                                                       const void* codes, int gd, int ncode,
-                                                      bool bf, __nv_bfloat16* Cb, float* C32,
-                                                      float* cnorm, int* err, int nbooks, int K,
-                                                      float* cmax, unsigned int* ctr) {
+                                                      bool bf, __nv_bfloat16* Cb, __nv_bfloat16* Hs,
+                                                      float* C32, float* cnorm, int* err,
+                                                      int nbooks, int K, float* cmax,
+                                                      unsigned int* ctr) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < count) update_one_code(ids[i], i, codes, gd, ncode, bf, Cb, C32, cnorm, err);
+  if (i < count) update_one_code(ids[i], i, codes, gd, ncode, bf, Cb, Hs, C32, cnorm, err);
   __shared__ bool last;
   __threadfence();
   __syncthreads();
@@ -435,7 +457,8 @@ cudaError_t launch_update_codes(const mapl_config& c, const int32_t* ids, int co
   const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G), ncode = nb * c.K;
   const bool bf = c.dtype == MAPL_BF16;
   k_update_codes<<<blocks_for(static_cast<size_t>(count), 128), 128, 0, s>>>(
-      ids, count, codes, gd, ncode, bf, p.Cb, p.C32, p.cnorm, p.err, nb, c.K, p.cmax, p.upd_ctr);
+      ids, count, codes, gd, ncode, bf, p.Cb, p.Hs, p.C32, p.cnorm, p.err, nb, c.K, p.cmax,
+      p.upd_ctr);
   return cudaGetLastError();
 }
 
@@ -452,7 +475,7 @@ cudaError_t launch_prep_f32(const mapl_config& c, const void* A, const void* Ps,
     if (c.G > 0) {
       const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G);
       k_prep_codes<<<blocks_for(static_cast<size_t>(nb) * c.K, T), T, 0, s>>>(
-          C, nb, c.K, gd, false, nullptr, p.C32, p.cnorm);
+          C, nb, c.K, gd, false, nullptr, nullptr, p.C32, p.cnorm);
       k_prep_cmax<<<blocks_for(static_cast<size_t>(nb) * 32, 256), 256, 0, s>>>(p.cnorm, nb, c.K, p.cmax);
     }
   }

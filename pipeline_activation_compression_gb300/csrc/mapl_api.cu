@@ -23,7 +23,7 @@ struct mapl_plan_s {
   bool tc = false;        // bf16 tensor-core path
   int gd = 0;
   PlanDevice p;
-  CUtensorMap tmAt{}, tmMt{}, tmC{}, tmB{};
+  CUtensorMap tmAt{}, tmMt{}, tmC{}, tmH{}, tmB{};
   uint64_t timeout_ns = kDefaultTimeoutNs;
   // launch geometry
   int c_nstage = 0;
@@ -49,12 +49,14 @@ struct mapl_plan_s {
   __nv_bfloat16* emb_tab = nullptr;
   CUtensorMap tmMt_emb{};
   // gradient codebooks (MCVQ of backward gradients): [Cb R x G x K x gd bf16
-  // | cnorm | cmax] in one allocation, and their tensor map
+  // | norm rows R x G x K x 16 bf16 | cnorm | cmax] in one allocation, and
+  // their tensor maps
   void* gpool = nullptr;
   __nv_bfloat16* Cb_g = nullptr;
+  __nv_bfloat16* Hs_g = nullptr;
   float* cnorm_g = nullptr;
   float* cmax_g = nullptr;
-  CUtensorMap tmC_g{};
+  CUtensorMap tmC_g{}, tmH_g{};
 };
 
 namespace {
@@ -186,11 +188,16 @@ mapl_status geometry(mapl_plan_s* pl) {
   }
   // pipelined compress: X ring (HBM), B ring (A^T and -M^T blocks from L2),
   // codebook ring
-  pl->c_pipe = compress_pipe_supported(static_cast<int>(c.r), pl->vq, pl->gd, c.G);
+  pl->c_pipe = compress_pipe_supported(static_cast<int>(c.r), pl->vq, pl->gd, c.G, c.K);
   if (pl->c_pipe) {
-    const uint32_t fixed = compress_pipe_ctl_bytes() + 64 + slack;
+    const uint32_t fixed = compress_pipe_ctl_bytes() + 64 + slack +
+                           (pl->vq ? compress_pipe_ones_bytes() : 0u);
     const uint32_t bst = static_cast<uint32_t>(c.r) * 128u;
-    const uint32_t cst = pl->vq ? ((static_cast<uint32_t>(c.K * pl->gd) * 2u + 1023u) & ~1023u) : 0u;
+    // a codebook stage: the book's codes, then its K norm rows of 32 bytes
+    const uint32_t cst =
+        pl->vq ? ((static_cast<uint32_t>(c.K * pl->gd) * 2u + static_cast<uint32_t>(c.K) * 32u +
+                   1023u) & ~1023u)
+               : 0u;
     const int ncb = pl->vq ? 4 : 0;   // two codebook stages per epilogue warp set
     // without codebooks, half the shared memory goes to the B ring: its
     // blocks are re-read from L2 for every tile, so it needs as many bytes
@@ -282,8 +289,13 @@ mapl_status build_plan_maps(mapl_plan_s* pl) {
                    static_cast<uint64_t>(c.R) * c.G * c.K, static_cast<uint32_t>(pl->gd),
                    static_cast<uint32_t>(c.K), swz))
       return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (codebooks)");
+    // norm rows: 16 bf16 (32 bytes) per code, one book per load
+    if (!make_tmap(&pl->tmH, pl->p.Hs, 16, static_cast<uint64_t>(c.R) * c.G * c.K, 16,
+                   static_cast<uint32_t>(c.K), CU_TENSOR_MAP_SWIZZLE_32B))
+      return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (norm rows)");
   } else {
     pl->tmC = pl->tmAt;   // unused
+    pl->tmH = pl->tmAt;   // unused
   }
   return MAPL_OK;
 }
@@ -352,7 +364,7 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
   // one pool for every plan-owned buffer
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off += up256(bytes); return o; };
-  size_t oAt = 0, oMts = 0, oBcat = 0, oCb = 0, oA32 = 0, oAt32 = 0, oM32 = 0,
+  size_t oAt = 0, oMts = 0, oBcat = 0, oCb = 0, oHs = 0, oA32 = 0, oAt32 = 0, oM32 = 0,
          oC32 = 0;
   const size_t oPs = take(d * r * elt_size(*cfg));
   const size_t oPr = take(d * r * elt_size(*cfg));
@@ -362,6 +374,7 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
     oMts = take(static_cast<size_t>(kNumSplit) * r * r * 2);
     oBcat = take(d * 2 * r * 2);
     if (vq) oCb = take(ncode * pl->gd * 2);
+    if (vq) oHs = take(ncode * 16 * 2);
   } else {
     oA32 = take(d * r * 4);
     oAt32 = take(d * r * 4);
@@ -386,6 +399,7 @@ mapl_status mapl_plan_create(mapl_plan* out, const mapl_config* cfg, const void*
     p.Mts = reinterpret_cast<__nv_bfloat16*>(b + oMts);
     p.Bcat = reinterpret_cast<__nv_bfloat16*>(b + oBcat);
     if (vq) p.Cb = reinterpret_cast<__nv_bfloat16*>(b + oCb);
+    if (vq) p.Hs = reinterpret_cast<__nv_bfloat16*>(b + oHs);
   } else {
     p.A32 = reinterpret_cast<float*>(b + oA32);
     p.At32 = reinterpret_cast<float*>(b + oAt32);
@@ -679,7 +693,8 @@ static mapl_status compress_common(mapl_plan pl, const void* X, const int32_t* t
     const int64_t want = (N + 63) / 64;
     const int grid = static_cast<int>(want < pl->num_sms ? want : pl->num_sms);
     e = launch_compress_pipe(tmX, pl->tmAt, emb ? pl->tmMt_emb : pl->tmMt,
-                             grad_books ? pl->tmC_g : pl->tmC, tmE, a, pl->p_smem, grid, stream);
+                             grad_books ? pl->tmC_g : pl->tmC, grad_books ? pl->tmH_g : pl->tmH,
+                             tmE, a, pl->p_smem, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "compress launch");
     return MAPL_OK;
   }
@@ -806,7 +821,8 @@ mapl_status mapl_plan_set_grad_codebooks(mapl_plan pl, const void* codebooks, cu
   if (st != MAPL_OK) return st;
   const mapl_config& c = pl->cfg;
   const size_t nb = static_cast<size_t>(c.R) * c.G, ncode = nb * c.K;
-  const size_t ocn = up256(ncode * pl->gd * sizeof(__nv_bfloat16));
+  const size_t ohs = up256(ncode * pl->gd * sizeof(__nv_bfloat16));
+  const size_t ocn = ohs + up256(ncode * 16 * sizeof(__nv_bfloat16));
   const size_t ocm = ocn + up256(ncode * sizeof(float));
   if (!pl->gpool) {
     cudaError_t e = cudaMalloc(&pl->gpool, ocm + up256(nb * sizeof(float)));
@@ -816,16 +832,19 @@ mapl_status mapl_plan_set_grad_codebooks(mapl_plan pl, const void* codebooks, cu
     }
     char* b = static_cast<char*>(pl->gpool);
     pl->Cb_g = reinterpret_cast<__nv_bfloat16*>(b);
+    pl->Hs_g = reinterpret_cast<__nv_bfloat16*>(b + ohs);
     pl->cnorm_g = reinterpret_cast<float*>(b + ocn);
     pl->cmax_g = reinterpret_cast<float*>(b + ocm);
     const CUtensorMapSwizzle swz =
         pl->gd == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
     if (!make_tmap(&pl->tmC_g, pl->Cb_g, static_cast<uint64_t>(pl->gd), ncode,
-                   static_cast<uint32_t>(pl->gd), static_cast<uint32_t>(c.K), swz))
+                   static_cast<uint32_t>(pl->gd), static_cast<uint32_t>(c.K), swz) ||
+        !make_tmap(&pl->tmH_g, pl->Hs_g, 16, ncode, 16, static_cast<uint32_t>(c.K),
+                   CU_TENSOR_MAP_SWIZZLE_32B))
       return fail(MAPL_ERR_CUDA, "cuTensorMapEncodeTiled failed (gradient codebooks)");
   }
-  const cudaError_t e = launch_prep_books_bf16(c, codebooks, pl->Cb_g, pl->cnorm_g, pl->cmax_g,
-                                               stream);
+  const cudaError_t e = launch_prep_books_bf16(c, codebooks, pl->Cb_g, pl->Hs_g, pl->cnorm_g,
+                                               pl->cmax_g, stream);
   if (e != cudaSuccess) return cuda_fail(e, "gradient codebook prep");
   return MAPL_OK;
 }

@@ -29,6 +29,9 @@ struct PlanDevice {
   __nv_bfloat16* Bcat = nullptr;    // d x 2r    [A | P_recv^T] (K-major B of decompress)
   __nv_bfloat16* Cb = nullptr;      // R x G x K x gd codebooks (B operand of the distance
                                     // MMA, decode lookups)
+  __nv_bfloat16* Hs = nullptr;      // R x G x K x 16 norm rows [h_hi, h_mid, h_lo, 0 ...]:
+                                    // ||c||^2 / 2 as three bf16 terms (B operand of the
+                                    // distance MMA's norm product)
   // fp32 CUDA-core path
   float* A32 = nullptr;             // d x r
   float* At32 = nullptr;            // r x d     A^T
@@ -63,7 +66,7 @@ struct CompressArgs {
   int nbstage;                      // pipelined kernel: B ring stages (A^T, -M^T blocks)
   uint32_t bstage_bytes;            //   r x 128 bytes
   int ncb;                          //   codebook ring stages (VQ)
-  uint32_t cstage_bytes;            //   K x gd x 2 bytes rounded up to 1024
+  uint32_t cstage_bytes;            //   K x gd x 2 bytes of codes + K x 32 bytes of norm rows
   uint64_t timeout_ns;
 };
 
@@ -90,9 +93,11 @@ struct DecompressArgs {
 
 uint32_t compress_ctl_bytes();      // control block of the compress kernel
 uint32_t compress_pipe_ctl_bytes(); // control block of the pipelined compress kernel
+uint32_t compress_pipe_ones_bytes(); // its constant A tile of the norm product (VQ)
 // Shapes the pipelined compress kernel handles: without VQ r <= 256; with
-// VQ r in {64, 128}, group width 16 or 32, an even number of groups.
-bool compress_pipe_supported(int r, bool vq, int gd, int G);
+// VQ r in {64, 128}, group width 16 or 32, an even number of groups, K a
+// multiple of 128.
+bool compress_pipe_supported(int r, bool vq, int gd, int G, int K);
 uint32_t decompress_ctl_bytes();    // control block of the decompress kernel
 uint32_t decompress_pt_ctl_bytes(); // control block + drain staging of the persistent kernel
 
@@ -106,7 +111,7 @@ cudaError_t launch_prep_f32(const mapl_config& c, const void* A, const void* Ps,
 // timeout bit of `err` when it gives up and writes the time waited.
 cudaError_t launch_store_probe(void* dst, size_t bytes, int mode, int num_sms, cudaStream_t s);
 cudaError_t launch_prep_books_bf16(const mapl_config& c, const void* C, __nv_bfloat16* Cb,
-                                   float* cnorm, float* cmax, cudaStream_t s);
+                                   __nv_bfloat16* Hs, float* cnorm, float* cmax, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint64_t budget_ns, int* err, unsigned long long* waited,
                                  cudaStream_t s);
 cudaError_t launch_update_codes(const mapl_config& c, const int32_t* ids, int count,
@@ -118,8 +123,9 @@ cudaError_t launch_compress_tc(const CUtensorMap& tmX, const CUtensorMap& tmAt,
                                uint32_t smem_bytes, int grid, cudaStream_t s);
 cudaError_t launch_compress_pipe(const CUtensorMap& tmX, const CUtensorMap& tmAt,
                                  const CUtensorMap& tmMt, const CUtensorMap& tmC,
-                                 const CUtensorMap& tmE, const CompressArgs& a,
-                                 uint32_t smem_bytes, int grid, cudaStream_t s);
+                                 const CUtensorMap& tmH, const CUtensorMap& tmE,
+                                 const CompressArgs& a, uint32_t smem_bytes, int grid,
+                                 cudaStream_t s);
 cudaError_t launch_decompress_pt(const CUtensorMap& tmB, const CUtensorMap& tmXh,
                                  const DecompressArgs& a, uint32_t smem_bytes, int grid,
                                  cudaStream_t s);

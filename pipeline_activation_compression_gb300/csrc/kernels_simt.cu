@@ -165,30 +165,70 @@ __device__ __forceinline__ void write_norm_row(float cn, __nv_bfloat16* row) {
   d[1] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// ||c||^2 of bf16 values in fp32: every square is exact in fp32 (8-bit
+// significands), the squares are added in index order with Knuth's two-sum
+// and the rounding errors carried beside the sum, and the pair is rounded
+// once at the end, so the result is the fp32 rounding of the exact value up
+// to a relative 2^-40 or so.  The plan's preparation and the streaming
+// update both use it, in the same order, so they give the same bits.
+struct Norm2 {
+  float s = 0.f, e = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float p = x * x;
+    const float t = s + p;
+    const float bp = t - s;
+    e += (s - (t - bp)) + (p - bp);
+    s = t;
+  }
+  __device__ __forceinline__ void add8(const uint4& w) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(h[k]);
+      add(f.x);
+      add(f.y);
+    }
+  }
+  __device__ __forceinline__ float value() const { return s + e; }
+};
+
 __global__ void k_prep_codes(const void* C, int nbooks, int K, int gd, bool bf,
                              __nv_bfloat16* Cb, __nv_bfloat16* Hs, float* C32, float* cnorm) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;   // code id over all books
   if (idx >= nbooks * K) return;
+  if (bf) {
+    const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(C) + static_cast<size_t>(idx) * gd;
+    Norm2 n;
+    for (int i = 0; i < gd; ++i) {
+      n.add(__bfloat162float(src[i]));
+      if (Cb) Cb[static_cast<size_t>(idx) * gd + i] = src[i];
+    }
+    cnorm[idx] = n.value();
+    if (Hs) write_norm_row(n.value(), Hs + static_cast<size_t>(idx) * 16);
+    return;
+  }
   double s = 0.0;
   for (int i = 0; i < gd; ++i) {
-    const double v = ld_f64(C, static_cast<size_t>(idx) * gd + i, bf);
+    const double v = ld_f64(C, static_cast<size_t>(idx) * gd + i, false);
     s = fma(v, v, s);
-    if (Cb) Cb[static_cast<size_t>(idx) * gd + i] = reinterpret_cast<const __nv_bfloat16*>(C)[static_cast<size_t>(idx) * gd + i];
     if (C32) C32[static_cast<size_t>(idx) * gd + i] = static_cast<float>(v);
   }
   cnorm[idx] = static_cast<float>(s);
-  if (Hs) write_norm_row(static_cast<float>(s), Hs + static_cast<size_t>(idx) * 16);
 }
 
 // max_k ||c_k|| of each book, rounded up: one warp per book (the maximum of
-// the fp32 norms is exact in any order; the square root is taken in fp64).
+// the fp32 norms is exact in any order; the correctly rounded fp32 square
+// root, within half an ulp, times 1 + 2^-20 is above the exact root).
+__device__ __forceinline__ float round_up_root(float m) { return sqrtf(m) * (1.f + 0x1p-20f); }
+
 __device__ __forceinline__ void book_max_warp(const float* cnorm, int b, int K, int lane,
                                               float* cmax) {
   float m = 0.f;
+#pragma unroll 8
   for (int k = lane; k < K; k += 32) m = fmaxf(m, __ldcg(cnorm + static_cast<size_t>(b) * K + k));
 #pragma unroll
   for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) cmax[b] = static_cast<float>(sqrt(static_cast<double>(m)) * (1.0 + 1e-6));
+  if (lane == 0) cmax[b] = round_up_root(m);
 }
 
 __global__ void k_prep_cmax(const float* cnorm, int nbooks, int K, float* cmax) {
@@ -346,71 +386,140 @@ cudaError_t launch_split_negMt(const float* M, int r, __nv_bfloat16* Mts, cudaSt
 }
 
 // One updated code: its values are read first (16-byte loads for bf16 rows
-// of 16 or 32 values, all in flight together), then written to the plan's
-// table, and ||c||^2 is formed from the registers in fp64.
-__device__ __forceinline__ void update_one_code(int id, int i, const void* __restrict__ codes,
+// of 16 or 32 values, issued together with the id's load), then written to
+// the plan's table with ||c||^2 (the preparation's Norm2 for bf16 rows, fp64
+// for fp32 rows) and, for bf16 plans, the norm row of the distance MMA.
+// A bf16 row of 16 or 32 values already in registers (w) written to code id;
+// returns its ||c||^2, or -1 (error word set) for an id outside the table.
+__device__ __forceinline__ float apply_code_bf16(int id, const uint4 (&w)[4], int gd, int ncode,
+                                                 __nv_bfloat16* __restrict__ Cb,
+                                                 __nv_bfloat16* __restrict__ Hs,
+                                                 float* __restrict__ cnorm, int* err) {
+  if (id < 0 || id >= ncode) {
+    atomicOr(err, kErrBadIndex);
+    return -1.f;
+  }
+  uint4* dst = reinterpret_cast<uint4*>(Cb) + static_cast<size_t>(id) * (gd / 8);
+  Norm2 n;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    if (c < gd / 8) {
+      dst[c] = w[c];
+      n.add8(w[c]);
+    }
+  cnorm[id] = n.value();
+  if (Hs) write_norm_row(n.value(), Hs + static_cast<size_t>(id) * 16);
+  return n.value();
+}
+
+__device__ __forceinline__ void load_code_bf16(const void* codes, int i, int gd, uint4 (&w)[4]) {
+  const uint4* src = reinterpret_cast<const uint4*>(codes) + static_cast<size_t>(i) * (gd / 8);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) w[c] = c < gd / 8 ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+__device__ __forceinline__ float update_one_code(int id, int i, const void* __restrict__ codes,
                                                 int gd, int ncode, bool bf,
                                                 __nv_bfloat16* __restrict__ Cb,
                                                 __nv_bfloat16* __restrict__ Hs,
                                                 float* __restrict__ C32, float* __restrict__ cnorm,
                                                 int* err) {
+  if (bf && (gd == 16 || gd == 32)) {
+    uint4 w[4];
+    load_code_bf16(codes, i, gd, w);
+    return apply_code_bf16(id, w, gd, ncode, Cb, Hs, cnorm, err);
+  }
   if (id < 0 || id >= ncode) {
     atomicOr(err, kErrBadIndex);
-    return;
+    return -1.f;
+  }
+  if (bf) {
+    Norm2 n;
+    for (int j = 0; j < gd; ++j) {
+      const __nv_bfloat16 v =
+          reinterpret_cast<const __nv_bfloat16*>(codes)[static_cast<size_t>(i) * gd + j];
+      Cb[static_cast<size_t>(id) * gd + j] = v;
+      n.add(__bfloat162float(v));
+    }
+    cnorm[id] = n.value();
+    if (Hs) write_norm_row(n.value(), Hs + static_cast<size_t>(id) * 16);
+    return n.value();
   }
   double s = 0.0;
-  if (bf && (gd == 16 || gd == 32)) {
-    const uint4* src = reinterpret_cast<const uint4*>(codes) + static_cast<size_t>(i) * (gd / 8);
-    uint4* dst = reinterpret_cast<uint4*>(Cb) + static_cast<size_t>(id) * (gd / 8);
-    uint4 w[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (c < gd / 8) w[c] = __ldg(src + c);
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (c < gd / 8) {
-        dst[c] = w[c];
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w[c]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __bfloat1622float2(h[e]);
-          s = fma(static_cast<double>(f.x), static_cast<double>(f.x), s);
-          s = fma(static_cast<double>(f.y), static_cast<double>(f.y), s);
-        }
-      }
-  } else {
-    for (int j = 0; j < gd; ++j) {
-      const size_t src = static_cast<size_t>(i) * gd + j, dst = static_cast<size_t>(id) * gd + j;
-      if (bf) {
-        const __nv_bfloat16 v = reinterpret_cast<const __nv_bfloat16*>(codes)[src];
-        Cb[dst] = v;
-        const double x = static_cast<double>(__bfloat162float(v));
-        s = fma(x, x, s);
-      } else {
-        const float v = reinterpret_cast<const float*>(codes)[src];
-        C32[dst] = v;
-        s = fma(static_cast<double>(v), static_cast<double>(v), s);
-      }
-    }
+  for (int j = 0; j < gd; ++j) {
+    const float v = reinterpret_cast<const float*>(codes)[static_cast<size_t>(i) * gd + j];
+    C32[static_cast<size_t>(id) * gd + j] = v;
+    s = fma(static_cast<double>(v), static_cast<double>(v), s);
   }
   cnorm[id] = static_cast<float>(s);
-  if (Hs) write_norm_row(static_cast<float>(s), Hs + static_cast<size_t>(id) * 16);
+  return static_cast<float>(s);
 }
 
 // Streaming codebook update (§3.5, App. F): code ids[i] (flat over R x G x
 // K) takes the values codes[i] (gd entries, plan dtype); its squared norm is
 // recomputed.  One thread per updated code; ids outside the table set the
-// error word and are skipped.  The last block to finish (a counter in the
-// plan, left at zero) recomputes every book's max ||c||, one warp per book,
-// so an update is one launch.
-__global__ void __launch_bounds__(128) k_update_codes(const int32_t* ids, int count,
-                                                      const void* codes, int gd, int ncode,
-                                                      bool bf, __nv_bfloat16* Cb, __nv_bfloat16* Hs,
-                                                      float* C32, float* cnorm, int* err,
-                                                      int nbooks, int K, float* cmax,
-                                                      unsigned int* ctr) {
+// error word and are skipped.  Then every book's max ||c|| is recomputed,
+// one warp per book, in the same launch:
+//  * one block (at most kUpdThreads codes, a table whose norms fit in
+//    shared memory): the block reads the table's old norms into shared
+//    memory while the new codes load, overwrites the updated entries and
+//    takes the maxima there, so the update costs one round trip to memory;
+//  * else the last block to finish (a counter in the plan, left at zero)
+//    reads the norms back from memory.
+constexpr int kUpdThreads = 512;
+constexpr int kUpdSmemCodes = 12288;   // 48 KB of norms
+
+__global__ void __launch_bounds__(kUpdThreads) k_update_codes_block(
+    const int32_t* ids, int count, const void* codes, int gd, int ncode, bool bf,
+    __nv_bfloat16* Cb, __nv_bfloat16* Hs, float* C32, float* cnorm, int* err, int nbooks, int K,
+    float* cmax) {
+  extern __shared__ float nrm[];
+  const int i = threadIdx.x;
+  const bool fast = bf && (gd == 16 || gd == 32);
+  // the id, the new values and the table's old norms, all loads in flight
+  // together
+  const int id = i < count ? __ldg(ids + i) : -1;
+  uint4 w[4];
+  if (fast && i < count) load_code_bf16(codes, i, gd, w);
+  for (int k0 = 0; k0 < ncode; k0 += 8 * kUpdThreads) {
+    float t[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int k = k0 + u * kUpdThreads + i;
+      t[u] = k < ncode ? __ldcg(cnorm + k) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int k = k0 + u * kUpdThreads + i;
+      if (k < ncode) nrm[k] = t[u];
+    }
+  }
+  __syncthreads();
+  if (i < count) {
+    const float v = fast ? apply_code_bf16(id, w, gd, ncode, Cb, Hs, cnorm, err)
+                         : update_one_code(id, i, codes, gd, ncode, bf, Cb, Hs, C32, cnorm, err);
+    if (v >= 0.f) nrm[id] = v;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  for (int b = threadIdx.x >> 5; b < nbooks; b += blockDim.x >> 5) {
+    float m = 0.f;
+    for (int k = lane; k < K; k += 32) m = fmaxf(m, nrm[b * K + k]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) cmax[b] = round_up_root(m);
+  }
+}
+
+__global__ void __launch_bounds__(kUpdThreads) k_update_codes(const int32_t* ids, int count,
+                                                              const void* codes, int gd, int ncode,
+                                                              bool bf, __nv_bfloat16* Cb,
+                                                              __nv_bfloat16* Hs, float* C32,
+                                                              float* cnorm, int* err, int nbooks,
+                                                              int K, float* cmax,
+                                                              unsigned int* ctr) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < count) update_one_code(ids[i], i, codes, gd, ncode, bf, Cb, Hs, C32, cnorm, err);
+  if (i < count) update_one_code(__ldg(ids + i), i, codes, gd, ncode, bf, Cb, Hs, C32, cnorm, err);
   __shared__ bool last;
   __threadfence();
   __syncthreads();
@@ -456,7 +565,12 @@ cudaError_t launch_update_codes(const mapl_config& c, const int32_t* ids, int co
                                 const void* codes, PlanDevice& p, cudaStream_t s) {
   const int nb = c.R * c.G, gd = static_cast<int>(c.r / c.G), ncode = nb * c.K;
   const bool bf = c.dtype == MAPL_BF16;
-  k_update_codes<<<blocks_for(static_cast<size_t>(count), 128), 128, 0, s>>>(
+  if (count <= kUpdThreads && ncode <= kUpdSmemCodes) {
+    k_update_codes_block<<<1, kUpdThreads, static_cast<size_t>(ncode) * sizeof(float), s>>>(
+        ids, count, codes, gd, ncode, bf, p.Cb, p.Hs, p.C32, p.cnorm, p.err, nb, c.K, p.cmax);
+    return cudaGetLastError();
+  }
+  k_update_codes<<<blocks_for(static_cast<size_t>(count), kUpdThreads), kUpdThreads, 0, s>>>(
       ids, count, codes, gd, ncode, bf, p.Cb, p.Hs, p.C32, p.cnorm, p.err, nb, c.K, p.cmax,
       p.upd_ctr);
   return cudaGetLastError();

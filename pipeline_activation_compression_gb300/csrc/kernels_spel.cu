@@ -229,6 +229,33 @@ __global__ void k_sumsq_partial(const float* __restrict__ x, long n, float* part
   if (threadIdx.x == 0) part[z * nblk + blockIdx.x] = red[0];
 }
 
+// m = beta m + (1 - beta)(G - AH) in place (AH = A H from the tensor-core
+// product), with the per-block partial sums of squares of the new m in the
+// same pass (same element order and block sums as k_sumsq_partial)
+__global__ void k_momentum_sumsq(float* __restrict__ m, const float* __restrict__ G,
+                                 const float* __restrict__ AH, float beta, long n,
+                                 float* part, long sX, int nblk) {
+  pdl_enter();
+  __shared__ float red[256];
+  const int z = blockIdx.y;
+  float* mp = m + z * sX;
+  const float* g = G + z * sX;
+  const float* c = AH + z * sX;
+  float s = 0.f;
+  for (long i = blockIdx.x * 256L + threadIdx.x; i < n; i += 256L * nblk) {
+    const float v = beta * mp[i] + (1.f - beta) * (g[i] - c[i]);
+    mp[i] = v;
+    s = fmaf(v, v, s);
+  }
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) part[z * nblk + blockIdx.x] = red[0];
+}
+
 __global__ void k_sumsq_final(const float* part, int nblk, float* inv) {
   pdl_enter();
   const int z = blockIdx.x;
@@ -407,11 +434,20 @@ cudaError_t launch_spel(float* A, const float* G, float* m, int d, int r, int ba
   mo.sG = w.dr;
   mo.sm = w.dr;
   mo.beta = beta;
-  if ((e = launch_chained(k_sgemm<false, kMomentum, TM>, gemm_grid(d, r, batch), dim3(64), 0, s, A,
-      w.S, nullptr, d, r, r, r, r, w.dr, w.rr, 0, 1, mo)) != cudaSuccess) return e;
+  if (w.tc) {
+    // A H on the tensor cores into the (still free) Y1 buffer, then the
+    // momentum update fused with the first pass of ||m||_F
+    e = launch_gemm3({A, r, w.dr, 0}, {w.S, r, w.rr, 1}, w.Y1, r, w.dr, 0, d, r, r, batch, 1, s);
+    if (e != cudaSuccess) return e;
+    if ((e = launch_chained(k_momentum_sumsq, dim3(kNormBlocks, batch), dim3(256), 0, s, m, G,
+        w.Y1, beta, w.dr, w.nrm_part, w.dr, kNormBlocks)) != cudaSuccess) return e;
+  } else {
+    if ((e = launch_chained(k_sgemm<false, kMomentum, TM>, gemm_grid(d, r, batch), dim3(64), 0, s,
+        A, w.S, nullptr, d, r, r, r, r, w.dr, w.rr, 0, 1, mo)) != cudaSuccess) return e;
+    if ((e = launch_chained(k_sumsq_partial, dim3(kNormBlocks, batch), dim3(256), 0, s, m, w.dr,
+        w.nrm_part, w.dr, kNormBlocks)) != cudaSuccess) return e;
+  }
   // Y = m / (||m||_F + 1e-7)
-  if ((e = launch_chained(k_sumsq_partial, dim3(kNormBlocks, batch), dim3(256), 0, s, m, w.dr,
-      w.nrm_part, w.dr, kNormBlocks)) != cudaSuccess) return e;
   if ((e = launch_chained(k_sumsq_final, batch, dim3(32), 0, s, w.nrm_part, kNormBlocks,
       w.inv)) != cudaSuccess) return e;
   if ((e = launch_chained(k_scale, dim3(256, batch), dim3(256), 0, s, m, w.inv, w.Y0, w.dr,

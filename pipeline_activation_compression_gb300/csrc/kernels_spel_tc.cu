@@ -203,15 +203,22 @@ __global__ void __launch_bounds__(kGThreads, 1)
   constexpr uint32_t idesc = idesc_bf16(128, TN);
   bool ok = true;
   int issued = 0;
-  float4 va[4], vb[TN / 32];
+  float4 va[4], vb[TN / 32];   // this K block
+  float4 na[4], nb[TN / 32];   // the next one, in flight while this one is split
+  if (nkb > 0) {
+    fetch_tile<128>(A, pa, m0, kbeg, tid, va);
+    fetch_tile<TN>(B, pb, n0, kbeg, tid, vb);
+  }
 
   for (int kb = 0; kb < nkb; ++kb) {
     const int b = kb & 1;
     const uint32_t buf = sbase + static_cast<uint32_t>(b) * kGBuf;
-    const int k0 = kbeg + kb * 64;
-    // the loads do not touch shared memory, so they start before the wait
-    fetch_tile<128>(A, pa, m0, k0, tid, va);
-    fetch_tile<TN>(B, pb, n0, k0, tid, vb);
+    // the loads do not touch shared memory: the next block's start before
+    // this block waits for its buffer and is split into it
+    if (kb + 1 < nkb) {
+      fetch_tile<128>(A, pa, m0, kbeg + (kb + 1) * 64, tid, na);
+      fetch_tile<TN>(B, pb, n0, kbeg + (kb + 1) * 64, tid, nb);
+    }
     // the MMAs that read this buffer two steps ago have completed (one
     // thread waits; the barrier releases the rest)
     if (kb >= 2 && tid == 0)
@@ -238,6 +245,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
       mma_commit(smem_u32(&mma_done[b]));
     }
     ++issued;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) va[i] = na[i];
+#pragma unroll
+    for (int i = 0; i < TN / 32; ++i) vb[i] = nb[i];
   }
   // the last commit arrives once every MMA issued before it has completed
   if (issued > 0) {

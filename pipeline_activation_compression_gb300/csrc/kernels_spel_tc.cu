@@ -174,7 +174,7 @@ template <int TN>
 __global__ void __launch_bounds__(kGThreads, 1)
     k_gemm3(GemmOp A, GemmOp B, float* __restrict__ C, long ldc, long sC, long sS, int K,
             int ksplit, uint64_t budget_ns) {
-  pdl_enter();
+  pdl_allow_next();
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t mma_done[2];
   __shared__ uint32_t tmem_base;
@@ -200,6 +200,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tacc = tmem_base;
+  // the setup above overlapped the kernels before this one; the operands
+  // they wrote are read only from here on
+  pdl_wait_prior();
   constexpr uint32_t idesc = idesc_bf16(128, TN);
   bool ok = true;
   int issued = 0;

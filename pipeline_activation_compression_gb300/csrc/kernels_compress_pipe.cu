@@ -54,6 +54,7 @@
 // error word, waits (bounded) for its own copies and products in flight, and
 // leaves through the common exit that frees TMEM.
 #include "mapl_internal.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 
 namespace mapl {
@@ -537,6 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmMt, const __grid_constant__ CUtensorMap tmC,
                     const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmE,
                     const CompressArgs a) {
+  // the next kernel in the stream may start its setup as this one's CTAs
+  // leave; this kernel's own setup (barriers, TMEM, the constant tile)
+  // overlaps the previous kernel, and nothing in memory is touched before
+  // pdl_wait_prior below
+  pdl_allow_next();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   constexpr bool vq = GD > 0;
@@ -610,16 +616,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                  "r"(lead ? 0x3F803F80u : 0u), "r"(lead ? 0x00003F80u : 0u), "r"(0u)
                  : "memory");
     fence_async_shared();
-    // bring the per-book bounds into L1 before the first step reads them
-    float acc = 0.f;
-    for (int y = x; y < a.R * a.G; y += 8 * 32) acc += __ldg(a.cmax + y);
-    if (acc == 12345.f) ctl->abort = 0;   // keeps the loads
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = ctl->tmem_base;
   const uint64_t bud = a.timeout_ns;
+  // the inputs (and the plan's tables) may come from the kernel before
+  pdl_wait_prior();
 
   if (warp == 0) {
     // ------------------------------------------------------ X ring producer
@@ -956,8 +960,8 @@ cudaError_t launch_one(const CUtensorMap& tmX, const CUtensorMap& tmAt, const CU
                        const CompressArgs& a, uint32_t smem, int grid, cudaStream_t s) {
   const cudaError_t e = set_smem(k_compress_pipe<GD, NGW>, smem);
   if (e != cudaSuccess) return e;
-  k_compress_pipe<GD, NGW><<<grid, kThreads, smem, s>>>(tmX, tmAt, tmMt, tmC, tmH, tmE, a);
-  return cudaGetLastError();
+  return launch_chained(k_compress_pipe<GD, NGW>, dim3(grid), dim3(kThreads), smem, s, tmX, tmAt,
+                        tmMt, tmC, tmH, tmE, a);
 }
 
 }  // namespace

@@ -10,6 +10,7 @@
 // Every wait is bounded (mbar_wait); on give-up the CTA sets the device error
 // word, writes nothing more and unwinds through the common exit.
 #include "mapl_internal.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 
 namespace mapl {
@@ -477,6 +478,9 @@ template <int GD>
 __global__ void __launch_bounds__(kPtThreads, 1)
     k_decompress_pt(const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmXh, const DecompressArgs a) {
+  // dependent launch: the setup below overlaps the kernel before this one;
+  // nothing in memory is touched before pdl_wait_prior
+  pdl_allow_next();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   const int nst = a.nstage, nab = a.nab;
@@ -526,6 +530,8 @@ __global__ void __launch_bounds__(kPtThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = ctl->tmem_base;
+  // the payload (and the plan's tables) may come from the kernel before
+  pdl_wait_prior();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -815,17 +821,23 @@ cudaError_t launch_decompress_pt(const CUtensorMap& tmB, const CUtensorMap& tmXh
     case 0:
       e = set_smem(k_decompress_pt<0>, smem_bytes);
       if (e != cudaSuccess) return e;
-      k_decompress_pt<0><<<grid, kPtThreads, smem_bytes, s>>>(tmB, tmXh, a);
+      e = launch_chained(k_decompress_pt<0>, dim3(grid), dim3(kPtThreads), smem_bytes, s, tmB, tmXh,
+                         a);
+      if (e != cudaSuccess) return e;
       break;
     case 16:
       e = set_smem(k_decompress_pt<16>, smem_bytes);
       if (e != cudaSuccess) return e;
-      k_decompress_pt<16><<<grid, kPtThreads, smem_bytes, s>>>(tmB, tmXh, a);
+      e = launch_chained(k_decompress_pt<16>, dim3(grid), dim3(kPtThreads), smem_bytes, s, tmB, tmXh,
+                         a);
+      if (e != cudaSuccess) return e;
       break;
     case 32:
       e = set_smem(k_decompress_pt<32>, smem_bytes);
       if (e != cudaSuccess) return e;
-      k_decompress_pt<32><<<grid, kPtThreads, smem_bytes, s>>>(tmB, tmXh, a);
+      e = launch_chained(k_decompress_pt<32>, dim3(grid), dim3(kPtThreads), smem_bytes, s, tmB, tmXh,
+                         a);
+      if (e != cudaSuccess) return e;
       break;
     default:
       return cudaErrorInvalidValue;

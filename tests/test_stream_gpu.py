@@ -77,3 +77,25 @@ def test_update_codes_rejects_bad_ids():
     with pytest.raises(mapl.MaplError) as ei:
         mapl.mapl_check(plan)
     assert ei.value.name == "MAPL_ERR_INVALID_ARG"
+
+
+@pytest.mark.parametrize("wname", ["vq_d1024_r128", "vq_d2048_r256"])
+def test_whole_table_update_equals_fresh_plan(wname):
+    """Every code replaced in one call (more codes than one block of the
+    update takes, so the multi-block form with the last-block maxima runs),
+    then the same payload and X_hat as a plan created from the new table."""
+    w = synth.WORKLOADS[wname]
+    n = 384
+    b = synth.make_boundary(w, seed=5, n_tokens=n)
+    total = w.R * w.G * w.K
+    assert total > 512
+    rng = np.random.default_rng(23)
+    C1 = synth.bf16_bits(synth.widen(b["C"]) * 0.9 + 0.05 * rng.standard_normal(b["C"].shape))
+    plan = _plan(w, b, b["C"])
+    ids = np.arange(total, dtype=np.int32)[::-1].copy()   # every code, in reverse order
+    flat1 = C1.reshape(total, w.gd)
+    mapl.mapl_plan_update_codes(plan, torch.from_numpy(ids).cuda(), to_dev(flat1[ids]))
+    fresh = _plan(w, b, C1)
+    got, want = _codec(plan, w, b, n), _codec(fresh, w, b, n)
+    assert np.array_equal(got[0], want[0])
+    assert np.array_equal(got[1], want[1])

@@ -80,9 +80,9 @@ struct Ctl {
   uint64_t cfull[kMaxC], cempty[kMaxC];
   uint64_t zfull[2], zempty[2];
   uint64_t opready[4];              // [set][slot]
-  uint64_t dfull[4], dempty[4];     // [set][slot]
+  uint64_t dfull[2], dempty[2];     // per warp set: its distance chunk slot
   uint64_t mmadone;                 // projection issuer's last products
-  uint64_t vqdone[2];               // distance-product issuer's last products
+  uint64_t vqdone;                  // distance-product issuer's last products
   uint32_t tmem_base;
   int abort;
   float uscr[8][32];                // per epilogue warp: the residual being refined
@@ -591,14 +591,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctl->zfull[z]), 1);
       mbar_init(smem_u32(&ctl->zempty[z]), 8);
     }
-    for (int s = 0; s < 4; ++s) {
-      mbar_init(smem_u32(&ctl->opready[s]), 4);
-      mbar_init(smem_u32(&ctl->dfull[s]), 1);
-      mbar_init(smem_u32(&ctl->dempty[s]), 4);
+    for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&ctl->opready[s]), 4);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(smem_u32(&ctl->dfull[j]), 1);
+      mbar_init(smem_u32(&ctl->dempty[j]), 4);
     }
     mbar_init(smem_u32(&ctl->mmadone), 1);
-    mbar_init(smem_u32(&ctl->vqdone[0]), 1);
-    mbar_init(smem_u32(&ctl->vqdone[1]), 1);
+    mbar_init(smem_u32(&ctl->vqdone), 1);
     ctl->abort = 0;
     fence_mbar_init();
     fence_async_shared();
@@ -809,8 +808,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every product issued has completed before TMEM can be freed, and no
       // book load is still landing
       if (issued) {
-        mma_commit(smem_u32(&ctl->vqdone[0]));
-        drain_wait(smem_u32(&ctl->vqdone[0]), 0u, ok ? bud : kDrainNs);
+        mma_commit(smem_u32(&ctl->vqdone));
+        drain_wait(smem_u32(&ctl->vqdone), 0u, ok ? bud : kDrainNs);
       }
       if (!ok) {
         for (int j = 0; j < 2; ++j)

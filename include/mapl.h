@@ -168,9 +168,10 @@ mapl_status mapl_decompress(mapl_plan plan, const void* payload, const int32_t* 
  *   codes[i * gd .. +gd) (device, plan dtype, 16-byte aligned); their ||c||^2 and every book's
  *   max ||c|| are refreshed.  An id outside [0, R*G*K) sets the error word
  *   (mapl_check reports MAPL_ERR_INVALID_ARG) and is skipped.  One launch
- *   (its last block recomputes the maxima through a counter the plan keeps),
- *   so calls on the same plan must not overlap on the GPU, as with every
- *   call that writes the plan.  Async.
+ *   (one block for up to 512 codes; for more, the last block to finish
+ *   recomputes the maxima through a counter the plan keeps), so calls on
+ *   the same plan must not overlap on the GPU, as with every call that
+ *   writes the plan.  Async.
  */
 mapl_status mapl_stream_subset(int64_t total, int64_t per_batch, uint64_t seed, int64_t step,
                                int32_t* ids, int32_t* count);
